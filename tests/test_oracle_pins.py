@@ -1,0 +1,360 @@
+"""Pins of the CPU oracle against facts fixed outside the oracle itself.
+
+Each test checks one oracle function against something it cannot agree with
+by construction: numbers printed on the pages (golden fixtures), closed forms,
+brute-force enumeration on tiny inputs, or a library routine (numpy/scipy)
+for a special case. No test retypes the oracle's own loop.
+"""
+import itertools
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+from scipy.special import expit
+
+import oracle
+import synth
+
+pytestmark = pytest.mark.filterwarnings("ignore::RuntimeWarning")
+
+
+def bf16(vals):
+    return synth.to_bf16_bits(np.asarray(vals, dtype=np.float64))
+
+
+def f32(bits):
+    return synth.bf16_bits_to_f32(bits).astype(np.float64)
+
+
+# ------------------------------------------------------------------ counts
+
+
+def test_counts_round_to_nearest():
+    # The single-layer d_ff=1024 workload states beta = 205 for a 20% dynamic
+    # ratio (0.2 * 1024 = 204.8), so counts round to nearest, not down.
+    assert oracle.cnt(0.2, 1024) == 205
+    assert oracle.cnt(0.4, 1024) - oracle.cnt(0.2, 1024) == 205
+    assert oracle.cnt(0.7, 1024) == 717
+    assert oracle.cnt(0.5, 3) == 2          # x.5 rounds up
+    assert oracle.cnt(0.0, 100) == 0 and oracle.cnt(1.0, 100) == 100
+
+
+def test_table1_fractions(golden_dir):
+    g = json.load(open(os.path.join(golden_dir, "selectinfer_table1.json")))
+    # static + dynamic = computed (phi = delta + epsilon), base + secondary = loaded
+    assert g["static_pct"] + g["dynamic_pct"] == g["computed_pct"]
+    assert g["static_pct"] + g["secondary_pct"] == g["loaded_pct"]
+    # the oracle's loading and selection realise exactly those fractions
+    N = 1000
+    rng = np.random.default_rng(1)
+    sc = rng.random(N).astype(np.float32)
+    loaded, st = oracle.rank_loaded(sc, sc, g["loaded_pct"] / 100, g["static_pct"] / 100)
+    assert len(loaded) == oracle.cnt(0.7, N) == 700
+    assert int(st.sum()) == oracle.cnt(0.3, N) == 300
+    A = synth.lognormal_absact(3, 8, len(loaded))
+    n_sel = oracle.cnt(g["computed_pct"] / 100, N)
+    S = oracle.select(A, 8, 1, len(loaded), st, 50, n_sel)
+    assert S.shape == (1, 400)
+    assert int(st[S[0]].sum()) == 300        # all static neurons are computed
+    assert len(S[0]) - 300 == 100            # dynamic = 10% of N
+
+
+def test_eq2_worked_example(golden_dir):
+    g = json.load(open(os.path.join(golden_dir, "selectinfer_eq2.json")))
+    # Eq. (2) with the printed numbers gives the printed 0.945 GB
+    dm = g["n_ffn_params"] * (1 - g["r_load"]) * g["r_layer"] * g["bytes_per_param"]
+    assert abs(dm / 1e9 - g["delta_m_gb"]) < 1e-9
+    # the oracle's byte accounting of selective loading on the real shape
+    s = g["llama32_3b_shape"]
+    d, N, L = s["d"], s["d_ff"], s["layers"]
+    n_ffn = 3 * d * N * L
+    assert abs(n_ffn / 2.1e9 - 1) < 0.01      # "N_ffn ~ 2.1B"
+    applied = round(g["r_layer"] * L)
+    full = 3 * d * N * g["bytes_per_param"]
+    kept = oracle.loaded_bytes(d, oracle.cnt(g["r_load"], N), g["bytes_per_param"])
+    saved = applied * (full - kept)
+    assert abs(saved / 1e9 - g["delta_m_gb"]) / g["delta_m_gb"] < 0.01
+
+
+# ------------------------------------------------------------- activations
+
+SILU2 = 1.0 + math.tanh(1.0)       # silu(2) = 2 * sigmoid(2), sigmoid(x) = (1 + tanh(x/2)) / 2
+SILUM2 = -(1.0 - math.tanh(1.0))   # silu(-2)
+SILU3 = 1.5 * (1.0 + math.tanh(1.5))
+
+
+def test_profile_closed_form():
+    # d = 2; tokens e1, -e1, e2. Neuron 0: g = 2*x0, u = x0; neuron 1: g = 2*x0, u = -x0;
+    # neuron 2: g = 3*x1, u = 0.5*x1; neuron 3: g = 0 (silu(0) = 0), u = 7*x0.
+    Wg = bf16([[2, 0], [2, 0], [0, 3], [0, 0]])
+    Wu = bf16([[1, 0], [-1, 0], [0, 0.5], [7, 0]])
+    X = bf16([[1, 0], [-1, 0], [0, 1]])
+    s = oracle.profile_scores(Wg, Wu, X)
+    # neuron 0: |silu(2)*1| + |silu(-2)*(-1)| + 0 = (1 + tanh 1) + (1 - tanh 1) = 2
+    assert s[0] == pytest.approx(2.0, rel=1e-15)
+    assert s[1] == pytest.approx(2.0, rel=1e-15)          # |a| keeps negative activations
+    assert s[2] == pytest.approx(0.5 * SILU3, rel=1e-15)
+    assert s[3] == 0.0
+    # accumulation over calls (scores are running sums)
+    s2 = oracle.profile_scores(Wg, Wu, X, scores=s.copy())
+    assert np.allclose(s2, 2 * s, rtol=1e-15)
+
+
+def _np_act(Wg, Wu, X):
+    g = f32(X) @ f32(Wg).T
+    u = f32(X) @ f32(Wu).T
+    return g * expit(g) * u
+
+
+def test_profile_vs_library():
+    Wg, Wu, _ = synth.layer_weights(7, 0, 64, 48)
+    X = synth.tokens(7, 0, synth.T_CALIB, 20, 64)
+    s = oracle.profile_scores(Wg, Wu, X)
+    ref = np.abs(_np_act(Wg, Wu, X)).sum(axis=0)
+    assert np.allclose(s, ref, rtol=1e-12, atol=0)
+
+
+def test_absact_and_dense_act_vs_library():
+    Wg, Wu, _ = synth.layer_weights(8, 0, 40, 30, sigma=1.5)
+    X = synth.tokens(8, 0, synth.T_PROMPT, 5, 40)
+    loaded = np.array([0, 3, 4, 9, 10, 29], np.int32)
+    A = oracle.absact(Wg, Wu, loaded, X)
+    ref = np.abs(_np_act(Wg, Wu, X))[:, loaded]
+    assert np.allclose(A, ref, rtol=1e-12, atol=1e-300)
+    a = oracle.dense_act(Wg, Wu, X[2])
+    assert np.allclose(a, _np_act(Wg, Wu, X[2:3])[0], rtol=1e-12)
+
+
+def test_silu_special_values():
+    Wg = bf16([[2], [-2], [3]])
+    Wu = bf16([[1], [1], [1]])
+    a = oracle.dense_act(Wg, Wu, bf16([1]))
+    assert a == pytest.approx([SILU2, SILUM2, SILU3], rel=1e-15)
+
+
+# ------------------------------------------------------------- sparse FFN
+
+
+def test_sparse_ffn_all_neurons_is_dense_ffn():
+    # gamma = phi = 1: no neuron is skipped, so the output is the dense SwiGLU FFN
+    d, N = 24, 40                       # d != N catches a transposed down matrix
+    Wg, Wu, Wd = synth.layer_weights(9, 0, d, N)
+    x = synth.tokens(9, 0, synth.T_DECODE, 1, d)[0]
+    loaded = np.arange(N, dtype=np.int32)
+    y = oracle.sparse_ffn(Wg, Wu, Wd, loaded, loaded, x)
+    ref = f32(Wd) @ _np_act(Wg, Wu, x[None, :])[0]
+    assert np.allclose(y, ref, rtol=1e-12, atol=1e-15)
+
+
+def test_sparse_ffn_subset_is_masked_dense():
+    d, N = 16, 50
+    Wg, Wu, Wd = synth.layer_weights(10, 0, d, N)
+    x = synth.tokens(10, 0, synth.T_DECODE, 1, d)[0]
+    loaded = np.array(sorted(np.random.default_rng(0).choice(N, 30, replace=False)), np.int32)
+    S = np.array([0, 2, 3, 7, 11, 29], np.int32)          # packed positions
+    y = oracle.sparse_ffn(Wg, Wu, Wd, loaded, S, x)
+    keep = loaded[S]
+    a = _np_act(Wg, Wu, x[None, :])[0]
+    ref = f32(Wd)[:, keep] @ a[keep]
+    assert np.allclose(y, ref, rtol=1e-12, atol=1e-15)
+
+
+# --------------------------------------------------------------- top-k
+
+
+def _brute_topk(vals, k):
+    """The unique k-subset whose members all precede every non-member in the
+    order (value desc, index asc), found by enumeration."""
+    n = len(vals)
+
+    def before(i, j):
+        return vals[i] > vals[j] or (vals[i] == vals[j] and i < j)
+
+    found = []
+    for sub in itertools.combinations(range(n), k):
+        s = set(sub)
+        if all(before(i, j) for i in s for j in range(n) if j not in s):
+            found.append(s)
+    assert len(found) == 1
+    return found[0]
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_topk_rows_brute_force(seed):
+    rng = np.random.default_rng(seed)
+    n = int(rng.integers(1, 9))
+    rows = 4
+    A = (rng.integers(0, 3, size=(rows, n)) / 2).astype(np.float32)   # many ties
+    for k in range(0, n + 1):
+        sel = oracle.topk_rows(A, k)
+        for r in range(rows):
+            assert set(np.nonzero(sel[r])[0]) == (_brute_topk(list(A[r]), k) if k else set())
+
+
+def test_topk_uses_magnitude_and_ld():
+    A = np.array([[-5.0, 1.0, 2.0, 99.0]], np.float32)   # column 3 outside n
+    sel = oracle.topk_rows(A, 1, n=3)
+    assert list(sel[0]) == [1, 0, 0]
+
+
+@pytest.mark.parametrize("seed", range(5))
+def test_select_brute_force(seed):
+    rng = np.random.default_rng(100 + seed)
+    n_loaded = int(rng.integers(3, 8))
+    T, B = int(rng.integers(1, 5)), int(rng.integers(1, 3))
+    st = np.zeros(n_loaded, np.uint8)
+    st[rng.choice(n_loaded, int(rng.integers(0, n_loaded)), replace=False)] = 1
+    n_static = int(st.sum())
+    alpha = int(rng.integers(1, n_loaded + 1))
+    n_sel = int(rng.integers(n_static, n_loaded + 1))
+    A = (rng.integers(0, 4, size=(B * T, n_loaded)) / 4).astype(np.float32)
+    S, counts, sel = oracle.select(A, T, B, n_loaded, st, alpha, n_sel, want_counts=True, want_sel=True)
+    for b in range(B):
+        lists = [_brute_topk(list(A[b * T + t]), alpha) for t in range(T)]
+        for t in range(T):
+            assert set(np.nonzero(sel[b * T + t])[0]) == lists[t]
+        ref_cnt = np.bincount([p for l in lists for p in l], minlength=n_loaded)
+        assert np.array_equal(counts[b], ref_cnt)
+        cand = [p for p in range(n_loaded) if not st[p]]
+        beta = n_sel - n_static
+        # top-beta of the counts among non-static positions, by enumeration
+        cv = [float(ref_cnt[p]) for p in cand]
+        dyn = {cand[i] for i in _brute_topk(cv, beta)} if beta else set()
+        expect = sorted(set(np.nonzero(st)[0]) | dyn)
+        assert list(S[b]) == expect
+
+
+def test_select_zero_counts_fill_by_lower_index():
+    # one token, alpha=1: only position 4 gets a count; beta=3 takes 4 then 0, 1
+    A = np.array([[0, 0, 0, 0, 9, 0]], np.float32)
+    st = np.zeros(6, np.uint8)
+    S = oracle.select(A, 1, 1, 6, st, 1, 3)
+    assert list(S[0]) == [0, 1, 4]
+
+
+# --------------------------------------------------------------- loading
+
+
+@pytest.mark.parametrize("seed", range(5))
+def test_rank_loaded_brute_force(seed):
+    rng = np.random.default_rng(200 + seed)
+    N = int(rng.integers(2, 9))
+    task = (rng.integers(0, 4, N) / 2).astype(np.float32)
+    model = (rng.integers(0, 4, N) / 2).astype(np.float32)
+    gamma = float(rng.integers(1, N + 1)) / N
+    delta = float(rng.integers(0, int(round(gamma * N)) + 1)) / N
+    loaded, st = oracle.rank_loaded(task, model, gamma, delta)
+    nb, nl = oracle.cnt(delta, N), oracle.cnt(gamma, N)
+    base = _brute_topk(list(task), nb) if nb else set()
+    rest = [n for n in range(N) if n not in base]
+    sec = {rest[i] for i in _brute_topk([float(model[n]) for n in rest], nl - nb)} if nl > nb else set()
+    assert list(loaded) == sorted(base | sec)
+    assert {int(loaded[p]) for p in range(len(loaded)) if st[p]} == base
+
+
+def test_rank_loaded_single_file_is_top_gamma():
+    rng = np.random.default_rng(5)
+    s = rng.random(300).astype(np.float32)
+    loaded, st = oracle.rank_loaded(s, s, 0.7, 0.2)
+    assert set(loaded) == set(np.argsort(-s, kind="stable")[:210])
+    assert set(loaded[st == 1]) == set(np.argsort(-s, kind="stable")[:60])
+
+
+def test_merge_scores_hand_computed():
+    # file 1: scores (2, 4) over 2 tokens; file 2: (9, 3) over 3 tokens
+    out = oracle.merge_scores([np.array([2, 4], np.float32), np.array([9, 3], np.float32)], [2, 3])
+    assert list(out) == [4.0, 3.0]
+    out1 = oracle.merge_scores([np.array([6, 1.5], np.float32)], [3])
+    assert list(out1) == [2.0, 0.5]
+
+
+# ------------------------------------------------------------------ SpAx
+
+
+def test_spax_encode_bound_and_layout():
+    d, N = 256, 6
+    _, _, Wd = synth.layer_weights(11, 0, d, N)
+    codes, params = oracle.spax_encode(Wd, 4, 128)
+    w = f32(Wd)
+    for n in range(N):
+        q = np.zeros(d, np.int64)
+        q[0::2] = codes[n] & 0xF
+        q[1::2] = codes[n] >> 4
+        for g in range(d // 128):
+            scale, mn = params[n, g]
+            grp = w[g * 128:(g + 1) * 128, n]
+            assert mn == grp.min()
+            assert scale == pytest.approx((grp.max() - grp.min()) / 15, rel=1e-6)
+            rec = mn + q[g * 128:(g + 1) * 128] * float(scale)
+            assert np.all(np.abs(rec - grp) <= float(scale) / 2 * (1 + 1e-5) + 1e-12)
+
+
+def test_spax_encode_constant_and_ramp_groups():
+    d, N = 256, 2
+    W = np.zeros((d, N))
+    W[:128, 0] = 0.375                      # constant group: scale 0, codes 0, exact
+    W[128:, 0] = np.arange(128) % 16 * 0.5  # ramp 0..7.5: min 0, scale 0.5, codes = ramp
+    W[:, 1] = -1.25
+    Wd = bf16(W)
+    codes, params = oracle.spax_encode(Wd, 4, 128)
+    assert params[0, 0, 0] == 0.0 and params[0, 0, 1] == np.float32(0.375)
+    assert np.all(codes[0, :64] == 0)
+    assert params[0, 1, 0] == np.float32(0.5) and params[0, 1, 1] == 0.0
+    ramp = np.arange(128) % 16
+    assert np.array_equal(codes[0, 64:], (ramp[0::2] | (ramp[1::2] << 4)).astype(np.uint8))
+    assert codes[0, 64] == 0x10             # element 2i in the low nibble
+    assert np.all(params[1, :, 0] == 0.0) and np.all(params[1, :, 1] == np.float32(-1.25))
+
+
+def test_spax_encode_other_widths():
+    d, N = 128, 3
+    _, _, Wd = synth.layer_weights(12, 0, d, N)
+    for bits in (2, 8):
+        codes, params = oracle.spax_encode(Wd, bits, 64)
+        assert codes.shape == (N, d * bits // 8)
+        qmax = (1 << bits) - 1
+        w = f32(Wd)
+        per = 8 // bits
+        q = np.zeros((N, d), np.int64)
+        for k in range(per):
+            q[:, k::per] = (codes >> (k * bits)) & qmax
+        for n in range(N):
+            for g in range(2):
+                scale, mn = params[n, g]
+                rec = mn + q[n, g * 64:(g + 1) * 64] * float(scale)
+                assert np.all(np.abs(rec - w[g * 64:(g + 1) * 64, n]) <= float(scale) / 2 * (1 + 1e-5) + 1e-12)
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_spax_tiers_brute_force(seed):
+    rng = np.random.default_rng(300 + seed)
+    N = int(rng.integers(2, 9))
+    a = ((rng.integers(0, 5, N) - 2) / 2).astype(np.float32)   # signs and ties
+    k_top = int(rng.integers(0, N + 1))
+    k_mid = int(rng.integers(0, N - k_top + 1))
+    top, mid = oracle.spax_tiers(a, k_top, k_mid)
+    mag = list(np.abs(a))
+    t = _brute_topk(mag, k_top) if k_top else set()
+    tm = _brute_topk(mag, k_top + k_mid) if k_top + k_mid else set()
+    assert list(top) == sorted(t)
+    assert list(mid) == sorted(tm - t)
+
+
+def test_spax_down_limits():
+    d, N = 256, 40
+    _, _, Wd = synth.layer_weights(13, 0, d, N)
+    a = synth.normal(13, 0, synth.T_SPAX_A, N).astype(np.float32)
+    codes, params = oracle.spax_encode(Wd, 4, 128)
+    allc = np.arange(N, dtype=np.int32)
+    none = np.zeros(0, np.int32)
+    # top = 100%: the dense down projection
+    y = oracle.spax_down(a, Wd, codes, params, allc, none)
+    assert np.allclose(y, f32(Wd) @ a.astype(np.float64), rtol=1e-12, atol=1e-14)
+    # mid = 100%: within the quantisation error bound of the dense result
+    y2 = oracle.spax_down(a, Wd, codes, params, none, allc)
+    bound = (np.abs(a.astype(np.float64))[None, :] * np.repeat(params[:, :, 0].T, 128, axis=0) / 2).sum(axis=1)
+    assert np.all(np.abs(y2 - f32(Wd) @ a.astype(np.float64)) <= bound * (1 + 1e-5) + 1e-12)
+    # nothing selected: zero
+    assert np.all(oracle.spax_down(a, Wd, codes, params, none, none) == 0)
