@@ -1,0 +1,18 @@
+"""activation_sparse_gb300 -- neuron-level activation-sparse FFN inference on
+GB300 (sm_103a): SelectInfer profiling / selective loading / prefill selection /
+sparse decode, and the SpAx three-tier down-projection.
+
+The compute lives in ``libsi.so`` (CUDA kernels behind the C ABI of
+``include/si.h``); this package is its thin binding. Importing it loads the
+library and raises when it cannot be found or built.
+"""
+from ._binding import (  # noqa: F401
+    SIGNATURES, SIError, Layer, SpaxLayer, load, lib_path,
+    si_count, si_counts, si_packed_bytes, si_device_error,
+    si_profile_scores, si_merge_scores, si_pack_loaded,
+    si_select_dynamic, si_select_from_absact, si_decode_plan, si_sparse_ffn_decode,
+    spax_encode, spax_dense_act, spax_tiered_down, spax_ffn_decode,
+    SI_OK, SI_ERR_INVALID_ARG, SI_ERR_CUDA, SI_ERR_OOM, SI_ERR_UNSUPPORTED, SI_ERR_DEVICE,
+)
+
+load()

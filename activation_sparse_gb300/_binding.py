@@ -1,0 +1,290 @@
+"""ctypes binding of ``libsi.so`` (declared in ``include/si.h``).
+
+Argument marshalling only: torch tensors supply device pointers, the current
+CUDA stream is passed through, status codes become exceptions. Every step of
+the method runs in the library's CUDA kernels; there is no fallback. When the
+library is missing, importing this module raises.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+from . import _build
+
+SI_OK, SI_ERR_INVALID_ARG, SI_ERR_CUDA, SI_ERR_OOM, SI_ERR_UNSUPPORTED, SI_ERR_DEVICE = range(6)
+SI_DEVERR_WAIT_TIMEOUT, SI_DEVERR_COUNT = 1, 2
+
+# every symbol include/si.h declares, with (restype, argtypes)
+_vp, _i, _d, _ll, _u32p = C.c_void_p, C.c_int, C.c_double, C.c_longlong, C.POINTER(C.c_uint32)
+_ip = C.POINTER(C.c_int)
+SIGNATURES = {
+    "si_last_error_string": (C.c_char_p, []),
+    "si_abi_version": (_i, []),
+    "si_count": (_ll, [_d, _ll]),
+    "si_counts": (_i, [_i, _d, _d, _d, _ip, _ip, _ip, _ip]),
+    "si_packed_bytes": (_ll, [_i, _i]),
+    "si_device_error": (_i, [_u32p, _i]),
+    "si_profile_scores": (_i, [_vp, _vp, _i, _i, _vp, _i, _vp, _vp]),
+    "si_merge_scores": (_i, [C.POINTER(_vp), C.POINTER(_ll), _i, _i, _vp, _vp]),
+    "si_pack_loaded": (_i, [_vp, _vp, _vp, _i, _i, _vp, _vp, _d, _d, C.POINTER(_vp), _vp]),
+    "si_layer_info": (_i, [_vp, _ip, _ip, _ip, _ip, _ip]),
+    "si_layer_buffers": (_i, [_vp, C.POINTER(_vp), C.POINTER(_vp), C.POINTER(_vp)]),
+    "si_layer_destroy": (_i, [_vp]),
+    "si_select_dynamic": (_i, [_vp, _vp, _i, _i, _i, _d, _vp, _vp, _vp]),
+    "si_select_from_absact": (_i, [_vp, _vp, _i, _i, _i, _i, _d, _vp, _vp, _vp, _vp]),
+    "si_decode_plan": (_i, [_vp, _vp, _i, _i, _vp]),
+    "si_sparse_ffn_decode": (_i, [_vp, _vp, _i, _i, _vp, _vp, _vp]),
+    "spax_encode": (_i, [_vp, _i, _i, _i, _i, C.POINTER(_vp), _vp]),
+    "spax_layer_info": (_i, [_vp, _ip, _ip, _ip, _ip, _ip]),
+    "spax_layer_buffers": (_i, [_vp, C.POINTER(_vp), C.POINTER(_vp), C.POINTER(_vp)]),
+    "spax_layer_destroy": (_i, [_vp]),
+    "spax_dense_act": (_i, [_vp, _vp, _i, _i, _vp, _vp, _vp]),
+    "spax_tiered_down": (_i, [_vp, _vp, _d, _d, _vp, _vp, _vp, _vp]),
+    "spax_ffn_decode": (_i, [_vp, _vp, _vp, _vp, _d, _d, _vp, _vp, _vp]),
+}
+
+_lib = None
+
+
+class SIError(RuntimeError):
+    def __init__(self, code, msg):
+        super().__init__("si error %d: %s" % (code, msg))
+        self.code = code
+
+
+def lib_path() -> str:
+    return _build.LIB
+
+
+def load(build_if_missing: bool = True):
+    """Loads libsi.so (building it first when absent or stale and nvcc exists)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if build_if_missing and not _build.up_to_date():
+        _build.build()
+    if not os.path.exists(_build.LIB):
+        raise ImportError("libsi.so is not built; run __graft_entry__.build() first")
+    L = C.CDLL(_build.LIB)
+    for name, (res, args) in SIGNATURES.items():
+        f = getattr(L, name)
+        f.restype, f.argtypes = res, args
+    _lib = L
+    return L
+
+
+def _check(rc):
+    if rc != SI_OK:
+        raise SIError(rc, _lib.si_last_error_string().decode())
+
+
+# ------------------------------------------------------------------ helpers
+
+def _torch():
+    import torch
+    return torch
+
+
+def _ptr(t, dtype=None, name="tensor"):
+    if t is None:
+        return None
+    torch = _torch()
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError("%s must have dtype %s, got %s" % (name, dtype, t.dtype))
+    return C.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    torch = _torch()
+    s = torch.cuda.current_stream() if stream is None else stream
+    return C.c_void_p(s.cuda_stream)
+
+
+def _bf16(t, name):
+    """bf16 tensors travel as their bit patterns: accept torch.bfloat16 or int16/uint16 views."""
+    torch = _torch()
+    if t.dtype not in (torch.bfloat16, torch.int16, torch.uint16):
+        raise ValueError("%s must be bf16 (or its 16-bit pattern)" % name)
+    return _ptr(t, None, name)
+
+
+# ------------------------------------------------------------------ API
+
+
+def si_count(ratio: float, n: int) -> int:
+    return int(load().si_count(float(ratio), int(n)))
+
+
+def si_counts(N, gamma, delta, phi):
+    L = load()
+    a, b, c, d = C.c_int(), C.c_int(), C.c_int(), C.c_int()
+    _check(L.si_counts(int(N), float(gamma), float(delta), float(phi), C.byref(a), C.byref(b), C.byref(c),
+                       C.byref(d)))
+    return a.value, b.value, c.value, d.value
+
+
+def si_packed_bytes(d, n_loaded) -> int:
+    return int(load().si_packed_bytes(int(d), int(n_loaded)))
+
+
+def si_device_error(clear: bool = True) -> int:
+    L = load()
+    v = C.c_uint32()
+    _check(L.si_device_error(C.byref(v), 1 if clear else 0))
+    return v.value
+
+
+def si_profile_scores(Wg, Wu, X, scores, stream=None):
+    N, d = Wg.shape
+    _check(load().si_profile_scores(_bf16(Wg, "Wg"), _bf16(Wu, "Wu"), d, N, _bf16(X, "X"), X.shape[0],
+                                    _ptr(scores, _torch().float32, "scores"), _stream(stream)))
+    return scores
+
+
+def si_merge_scores(score_list, token_counts, out, stream=None):
+    torch = _torch()
+    ptrs = (C.c_void_p * len(score_list))(*[s.data_ptr() for s in score_list])
+    for s in score_list:
+        _ptr(s, torch.float32, "scores")
+    toks = (C.c_longlong * len(score_list))(*[int(t) for t in token_counts])
+    _check(load().si_merge_scores(ptrs, toks, len(score_list), out.shape[0], _ptr(out, torch.float32, "out"),
+                                  _stream(stream)))
+    return out
+
+
+class Layer:
+    """A packed SelectInfer layer (owns the library handle)."""
+
+    def __init__(self, handle):
+        self._h = handle
+        L = load()
+        v = [C.c_int() for _ in range(5)]
+        _check(L.si_layer_info(self._h, *[C.byref(x) for x in v]))
+        self.d, self.N, self.n_loaded, self.n_static, self.n_pad = [x.value for x in v]
+
+    @property
+    def handle(self):
+        return self._h
+
+    def buffers(self):
+        """(loaded_idx, is_static, packed) device pointers as ints."""
+        a, b, c = C.c_void_p(), C.c_void_p(), C.c_void_p()
+        _check(load().si_layer_buffers(self._h, C.byref(a), C.byref(b), C.byref(c)))
+        return a.value, b.value, c.value
+
+    def close(self):
+        if self._h:
+            load().si_layer_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def si_pack_loaded(Wg, Wu, Wd, task_scores, model_scores, gamma, delta, stream=None) -> Layer:
+    torch = _torch()
+    N, d = Wg.shape
+    h = C.c_void_p()
+    _check(load().si_pack_loaded(_bf16(Wg, "Wg"), _bf16(Wu, "Wu"), _bf16(Wd, "Wd"), d, N,
+                                 _ptr(task_scores, torch.float32, "task_scores"),
+                                 _ptr(model_scores, torch.float32, "model_scores"), float(gamma), float(delta),
+                                 C.byref(h), _stream(stream)))
+    return Layer(h)
+
+
+def si_select_dynamic(layer: Layer, X, T, B, alpha, phi, S, absact_out=None, stream=None):
+    torch = _torch()
+    _check(load().si_select_dynamic(layer.handle, _bf16(X, "X"), int(T), int(B), int(alpha), float(phi),
+                                    _ptr(S, torch.int32, "S"), _ptr(absact_out, torch.float32, "absact_out"),
+                                    _stream(stream)))
+    return S
+
+
+def si_select_from_absact(layer: Layer, absA, T, B, alpha, phi, S, topmask=None, counts=None, stream=None):
+    torch = _torch()
+    u32 = torch.int32  # uint32 words travel in int32 tensors
+    _check(load().si_select_from_absact(layer.handle, _ptr(absA, torch.float32, "absA"), absA.shape[1], int(T),
+                                        int(B), int(alpha), float(phi), _ptr(S, torch.int32, "S"),
+                                        _ptr(topmask, u32, "topmask"), _ptr(counts, u32, "counts"),
+                                        _stream(stream)))
+    return S
+
+
+def si_decode_plan(layer: Layer, S, n_sel, B, stream=None):
+    _check(load().si_decode_plan(layer.handle, _ptr(S, _torch().int32, "S"), int(n_sel), int(B), _stream(stream)))
+
+
+def si_sparse_ffn_decode(layer: Layer, S, n_sel, B, x, y, stream=None):
+    torch = _torch()
+    _check(load().si_sparse_ffn_decode(layer.handle, _ptr(S, torch.int32, "S"), int(n_sel), int(B), _bf16(x, "x"),
+                                       _ptr(y, torch.float32, "y"), _stream(stream)))
+    return y
+
+
+class SpaxLayer:
+    """An encoded SpAx down-projection (owns the library handle)."""
+
+    def __init__(self, handle):
+        self._h = handle
+        v = [C.c_int() for _ in range(5)]
+        _check(load().spax_layer_info(self._h, *[C.byref(x) for x in v]))
+        self.d, self.N, self.bits, self.group, self.ngp = [x.value for x in v]
+
+    @property
+    def handle(self):
+        return self._h
+
+    def buffers(self):
+        """(WdT, codes, params) device pointers as ints."""
+        a, b, c = C.c_void_p(), C.c_void_p(), C.c_void_p()
+        _check(load().spax_layer_buffers(self._h, C.byref(a), C.byref(b), C.byref(c)))
+        return a.value, b.value, c.value
+
+    def close(self):
+        if self._h:
+            load().spax_layer_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def spax_encode(Wd, bits=4, group=128, stream=None) -> SpaxLayer:
+    d, N = Wd.shape
+    h = C.c_void_p()
+    _check(load().spax_encode(_bf16(Wd, "Wd"), d, N, int(bits), int(group), C.byref(h), _stream(stream)))
+    return SpaxLayer(h)
+
+
+def spax_dense_act(Wg, Wu, x, a, stream=None):
+    N, d = Wg.shape
+    _check(load().spax_dense_act(_bf16(Wg, "Wg"), _bf16(Wu, "Wu"), d, N, _bf16(x, "x"),
+                                 _ptr(a, _torch().float32, "a"), _stream(stream)))
+    return a
+
+
+def spax_tiered_down(layer: SpaxLayer, a, top_frac, mid_frac, y, top_idx=None, mid_idx=None, stream=None):
+    torch = _torch()
+    _check(load().spax_tiered_down(layer.handle, _ptr(a, torch.float32, "a"), float(top_frac), float(mid_frac),
+                                   _ptr(y, torch.float32, "y"), _ptr(top_idx, torch.int32, "top_idx"),
+                                   _ptr(mid_idx, torch.int32, "mid_idx"), _stream(stream)))
+    return y
+
+
+def spax_ffn_decode(layer: SpaxLayer, Wg, Wu, x, top_frac, mid_frac, y, a_out=None, stream=None):
+    torch = _torch()
+    _check(load().spax_ffn_decode(layer.handle, _bf16(Wg, "Wg"), _bf16(Wu, "Wu"), _bf16(x, "x"), float(top_frac),
+                                  float(mid_frac), _ptr(y, torch.float32, "y"),
+                                  _ptr(a_out, torch.float32, "a_out"), _stream(stream)))
+    return y

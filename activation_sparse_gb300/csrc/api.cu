@@ -1,0 +1,591 @@
+// api.cu -- the C ABI declared in include/si.h: argument validation, handle
+// lifetime, scratch management and kernel launches. No arithmetic of the
+// method happens here; every step runs in the kernels.
+#include <cmath>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "../../include/si.h"
+#include "internal.h"
+
+namespace {
+
+thread_local std::string g_msg;
+
+int fail(int code, const std::string& msg) {
+    g_msg = msg;
+    return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+    g_msg = std::string(what) + ": " + cudaGetErrorString(e);
+    return e == cudaErrorMemoryAllocation ? SI_ERR_OOM : SI_ERR_CUDA;
+}
+
+#define SI_CK(call)                                        \
+    do {                                                   \
+        cudaError_t e_ = (call);                           \
+        if (e_ != cudaSuccess) return cuda_fail(e_, #call); \
+    } while (0)
+
+long long count_of(double r, long long n) { return (long long)std::floor(r * (double)n + 0.5); }
+
+int round_up(int x, int m) { return (x + m - 1) / m * m; }
+
+bool capturing(cudaStream_t st) {
+    cudaStreamCaptureStatus s = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(st, &s) != cudaSuccess) return false;
+    return s != cudaStreamCaptureStatusNone;
+}
+
+// Device error word, one per device, allocated on first use.
+std::mutex g_err_mu;
+unsigned* g_err_word[128] = {};
+
+int err_word(unsigned** out) {
+    int dev = 0;
+    SI_CK(cudaGetDevice(&dev));
+    if (dev < 0 || dev >= 128) return fail(SI_ERR_UNSUPPORTED, "device ordinal out of range");
+    std::lock_guard<std::mutex> lk(g_err_mu);
+    if (!g_err_word[dev]) {
+        unsigned* p = nullptr;
+        SI_CK(cudaMalloc(&p, sizeof(unsigned)));
+        SI_CK(cudaMemset(p, 0, sizeof(unsigned)));
+        g_err_word[dev] = p;
+    }
+    *out = g_err_word[dev];
+    return SI_OK;
+}
+
+template <class T>
+int dalloc(T** p, size_t count, const char* what) {
+    *p = nullptr;
+    if (count == 0) count = 1;
+    cudaError_t e = cudaMalloc(reinterpret_cast<void**>(p), count * sizeof(T));
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        return fail(SI_ERR_OOM, std::string("cudaMalloc failed for ") + what);
+    }
+    return SI_OK;
+}
+
+template <class T>
+void dfree(T*& p) {
+    if (p) cudaFree(p);
+    p = nullptr;
+}
+
+bool ratios_ok(double delta, double phi, double gamma) {
+    return std::isfinite(delta) && std::isfinite(phi) && std::isfinite(gamma) && delta >= 0.0 && delta <= phi &&
+           phi <= gamma && gamma <= 1.0;
+}
+
+}  // namespace
+
+struct si_layer {
+    int device = 0;
+    int d = 0, N = 0, n_loaded = 0, n_static = 0, n_pad = 0;
+    int32_t* loaded = nullptr;
+    uint8_t* is_static = nullptr;
+    uint16_t* packed = nullptr;
+    uint32_t* counts = nullptr;
+    int counts_B = 0;
+    float* absA = nullptr;
+    size_t absA_floats = 0;
+    float* part = nullptr;
+    long long part_floats = 0;
+    unsigned* tickets = nullptr;
+    int32_t* plan_pos = nullptr;
+    uint32_t* plan_mask = nullptr;
+    int* plan_n = nullptr;
+    const int32_t* plan_S = nullptr;
+    int plan_nsel = -1, plan_B = 0;
+};
+
+struct spax_layer {
+    int device = 0;
+    int d = 0, N = 0, bits = 0, group = 0, ngp = 0;
+    uint16_t* WdT = nullptr;
+    uint8_t* codes = nullptr;
+    float* params = nullptr;
+    int32_t* top = nullptr;
+    int32_t* mid = nullptr;
+    float* a = nullptr;
+    float* part = nullptr;
+    long long part_floats = 0;
+    unsigned* tickets = nullptr;
+};
+
+namespace {
+
+int grow_part(float** part, long long* cap, int d, int B) {
+    const long long need = si::decode_max_partial_floats(d, B);
+    if (need <= 0) return fail(SI_ERR_CUDA, "cannot query the device for the decode grid");
+    if (*cap >= need) return SI_OK;
+    dfree(*part);
+    *cap = 0;
+    int rc = dalloc(part, (size_t)need, "decode partials");
+    if (rc) return rc;
+    *cap = need;
+    return SI_OK;
+}
+
+void destroy_layer(si_layer* L) {
+    if (!L) return;
+    dfree(L->loaded);
+    dfree(L->is_static);
+    dfree(L->packed);
+    dfree(L->counts);
+    dfree(L->absA);
+    dfree(L->part);
+    dfree(L->tickets);
+    dfree(L->plan_pos);
+    dfree(L->plan_mask);
+    dfree(L->plan_n);
+    delete L;
+}
+
+void destroy_spax(spax_layer* L) {
+    if (!L) return;
+    dfree(L->WdT);
+    dfree(L->codes);
+    dfree(L->params);
+    dfree(L->top);
+    dfree(L->mid);
+    dfree(L->a);
+    dfree(L->part);
+    dfree(L->tickets);
+    delete L;
+}
+
+int select_core(si_layer* L, const float* absA, int ld, int T, int B, int alpha, double phi, int32_t* S,
+                uint32_t* topmask, uint32_t* counts, cudaStream_t st) {
+    const long long n_sel = count_of(phi, L->N);
+    if (n_sel < L->n_static || n_sel > L->n_loaded)
+        return fail(SI_ERR_INVALID_ARG, "phi must give n_static <= n_sel <= n_loaded");
+    const int beta = (int)n_sel - L->n_static;
+    unsigned* err = nullptr;
+    int rc = err_word(&err);
+    if (rc) return rc;
+    uint32_t* cnt = counts;
+    if (!cnt) {
+        if (L->counts_B < B) {
+            if (capturing(st)) return fail(SI_ERR_INVALID_ARG, "count scratch must grow; call once before capture");
+            dfree(L->counts);
+            L->counts_B = 0;
+            rc = dalloc(&L->counts, (size_t)B * L->n_loaded, "selection counts");
+            if (rc) return rc;
+            L->counts_B = B;
+        }
+        cnt = L->counts;
+    }
+    SI_CK(cudaMemsetAsync(cnt, 0, (size_t)B * L->n_loaded * sizeof(uint32_t), st));
+    SI_CK(si::launch_topk_alpha(absA, ld, L->n_loaded, T, B, alpha, cnt, topmask, st));
+    SI_CK(si::launch_topk_beta(cnt, L->is_static, L->n_loaded, B, beta, (int)n_sel, S, err, st));
+    return SI_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* si_last_error_string(void) { return g_msg.c_str(); }
+
+int si_abi_version(void) { return 1; }
+
+long long si_count(double ratio, long long n) { return count_of(ratio, n); }
+
+int si_counts(int N, double gamma, double delta, double phi, int* n_loaded, int* n_static, int* n_sel, int* beta) {
+    if (N < 1 || !ratios_ok(delta, phi, gamma))
+        return fail(SI_ERR_INVALID_ARG, "need N >= 1 and 0 <= delta <= phi <= gamma <= 1");
+    const long long nl = count_of(gamma, N), ns = count_of(delta, N), nq = count_of(phi, N);
+    if (n_loaded) *n_loaded = (int)nl;
+    if (n_static) *n_static = (int)ns;
+    if (n_sel) *n_sel = (int)nq;
+    if (beta) *beta = (int)(nq - ns);
+    return SI_OK;
+}
+
+long long si_packed_bytes(int d, int n_loaded) { return 3LL * d * n_loaded * 2; }
+
+int si_device_error(uint32_t* code, int clear) {
+    if (!code) return fail(SI_ERR_INVALID_ARG, "code is NULL");
+    unsigned* w = nullptr;
+    int rc = err_word(&w);
+    if (rc) return rc;
+    SI_CK(cudaDeviceSynchronize());
+    unsigned v = 0;
+    SI_CK(cudaMemcpy(&v, w, sizeof v, cudaMemcpyDeviceToHost));
+    if (clear) SI_CK(cudaMemset(w, 0, sizeof(unsigned)));
+    *code = v;
+    return SI_OK;
+}
+
+// ------------------------------------------------------------------ a1
+
+int si_profile_scores(const uint16_t* Wg, const uint16_t* Wu, int d, int N, const uint16_t* X, int T, float* scores,
+                      void* stream) {
+    if (!Wg || !Wu || !X || !scores) return fail(SI_ERR_INVALID_ARG, "NULL pointer");
+    if (d < 64 || d % 64 || N < 1 || T < 1) return fail(SI_ERR_INVALID_ARG, "need d % 64 == 0, N >= 1, T >= 1");
+    unsigned* err = nullptr;
+    int rc = err_word(&err);
+    if (rc) return rc;
+    si::ActGemmParams P = {};
+    P.X = X;
+    P.M = T;
+    P.K = d;
+    P.Wgate = Wg;
+    P.Wup = Wu;
+    P.w_stride = d;
+    P.Nrows = N;
+    P.Nvalid = N;
+    P.mode = 1;
+    P.colsum = scores;
+    P.err = err;
+    SI_CK(si::launch_act_gemm(P, (cudaStream_t)stream));
+    return SI_OK;
+}
+
+int si_merge_scores(const float* const* scores, const long long* token_counts, int nfiles, int N, float* out,
+                    void* stream) {
+    if (!scores || !token_counts || !out) return fail(SI_ERR_INVALID_ARG, "NULL pointer");
+    if (nfiles < 1 || nfiles > 16 || N < 1) return fail(SI_ERR_INVALID_ARG, "need 1 <= nfiles <= 16, N >= 1");
+    float tok[16];
+    for (int f = 0; f < nfiles; ++f) {
+        if (!scores[f]) return fail(SI_ERR_INVALID_ARG, "NULL score file");
+        if (token_counts[f] < 1) return fail(SI_ERR_INVALID_ARG, "token counts must be >= 1");
+        tok[f] = (float)token_counts[f];
+    }
+    SI_CK(si::launch_merge_scores(scores, tok, nfiles, N, out, (cudaStream_t)stream));
+    return SI_OK;
+}
+
+// ------------------------------------------------------------------ a2
+
+int si_pack_loaded(const uint16_t* Wg, const uint16_t* Wu, const uint16_t* Wd, int d, int N, const float* task_scores,
+                   const float* model_scores, double gamma, double delta, si_layer** out, void* stream) {
+    if (!out) return fail(SI_ERR_INVALID_ARG, "out is NULL");
+    *out = nullptr;
+    if (!Wg || !Wu || !Wd || !task_scores || !model_scores) return fail(SI_ERR_INVALID_ARG, "NULL pointer");
+    if (d < 64 || d % 64) return fail(SI_ERR_INVALID_ARG, "need d % 64 == 0");
+    if (N < 1 || N > 32768) return fail(SI_ERR_INVALID_ARG, "need 1 <= N <= 32768");
+    if (!ratios_ok(delta, delta, gamma)) return fail(SI_ERR_INVALID_ARG, "need 0 <= delta <= gamma <= 1");
+    const int n_loaded = (int)count_of(gamma, N), n_static = (int)count_of(delta, N);
+    if (n_loaded < 1) return fail(SI_ERR_INVALID_ARG, "gamma loads no neuron");
+    cudaStream_t st = (cudaStream_t)stream;
+    if (capturing(st)) return fail(SI_ERR_INVALID_ARG, "si_pack_loaded allocates; not allowed during capture");
+    unsigned* err = nullptr;
+    int rc = err_word(&err);
+    if (rc) return rc;
+    si_layer* L = new si_layer();
+    SI_CK(cudaGetDevice(&L->device));
+    L->d = d;
+    L->N = N;
+    L->n_loaded = n_loaded;
+    L->n_static = n_static;
+    L->n_pad = round_up(n_loaded, 128);
+    if ((rc = dalloc(&L->loaded, n_loaded, "loaded index")) || (rc = dalloc(&L->is_static, n_loaded, "static flags")) ||
+        (rc = dalloc(&L->packed, (size_t)L->n_pad * 3 * d, "packed weights")) ||
+        (rc = dalloc(&L->tickets, 16, "tickets")) || (rc = grow_part(&L->part, &L->part_floats, d, 1))) {
+        destroy_layer(L);
+        return rc;
+    }
+    cudaError_t e = cudaMemsetAsync(L->tickets, 0, 16 * sizeof(unsigned), st);
+    if (e == cudaSuccess) e = si::launch_rank_loaded(task_scores, model_scores, N, n_static, n_loaded, L->loaded,
+                                                     L->is_static, err, st);
+    if (e == cudaSuccess) e = si::launch_pack_loaded(Wg, Wu, Wd, d, N, L->loaded, n_loaded, L->n_pad, L->packed, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) {
+        destroy_layer(L);
+        return cuda_fail(e, "si_pack_loaded");
+    }
+    *out = L;
+    return SI_OK;
+}
+
+int si_layer_info(const si_layer* L, int* d, int* N, int* n_loaded, int* n_static, int* n_pad) {
+    if (!L) return fail(SI_ERR_INVALID_ARG, "layer is NULL");
+    if (d) *d = L->d;
+    if (N) *N = L->N;
+    if (n_loaded) *n_loaded = L->n_loaded;
+    if (n_static) *n_static = L->n_static;
+    if (n_pad) *n_pad = L->n_pad;
+    return SI_OK;
+}
+
+int si_layer_buffers(const si_layer* L, const int32_t** loaded_idx, const uint8_t** is_static,
+                     const uint16_t** packed) {
+    if (!L) return fail(SI_ERR_INVALID_ARG, "layer is NULL");
+    if (loaded_idx) *loaded_idx = L->loaded;
+    if (is_static) *is_static = L->is_static;
+    if (packed) *packed = L->packed;
+    return SI_OK;
+}
+
+int si_layer_destroy(si_layer* L) {
+    if (!L) return SI_OK;
+    cudaDeviceSynchronize();
+    destroy_layer(L);
+    return SI_OK;
+}
+
+// ------------------------------------------------------------ a3 .. a6
+
+int si_select_from_absact(si_layer* L, const float* absA, int ld, int T, int B, int alpha, double phi, int32_t* S,
+                          uint32_t* topmask, uint32_t* counts, void* stream) {
+    if (!L || !absA || !S) return fail(SI_ERR_INVALID_ARG, "NULL pointer");
+    if (T < 1 || B < 1 || ld < L->n_loaded) return fail(SI_ERR_INVALID_ARG, "need T, B >= 1 and ld >= n_loaded");
+    if (alpha < 1 || alpha > L->n_loaded) return fail(SI_ERR_INVALID_ARG, "need 1 <= alpha <= n_loaded");
+    if (!std::isfinite(phi)) return fail(SI_ERR_INVALID_ARG, "phi is not finite");
+    return select_core(L, absA, ld, T, B, alpha, phi, S, topmask, counts, (cudaStream_t)stream);
+}
+
+int si_select_dynamic(si_layer* L, const uint16_t* X, int T, int B, int alpha, double phi, int32_t* S,
+                      float* absact_out, void* stream) {
+    if (!L || !X || !S) return fail(SI_ERR_INVALID_ARG, "NULL pointer");
+    if (T < 1 || B < 1) return fail(SI_ERR_INVALID_ARG, "need T, B >= 1");
+    if ((long long)T * B > (1LL << 30) / L->n_pad) return fail(SI_ERR_INVALID_ARG, "T * B too large");
+    if (alpha < 1 || alpha > L->n_loaded) return fail(SI_ERR_INVALID_ARG, "need 1 <= alpha <= n_loaded");
+    if (!std::isfinite(phi)) return fail(SI_ERR_INVALID_ARG, "phi is not finite");
+    const long long n_sel = count_of(phi, L->N);
+    if (n_sel < L->n_static || n_sel > L->n_loaded)
+        return fail(SI_ERR_INVALID_ARG, "phi must give n_static <= n_sel <= n_loaded");
+    cudaStream_t st = (cudaStream_t)stream;
+    unsigned* err = nullptr;
+    int rc = err_word(&err);
+    if (rc) return rc;
+    const int M = T * B;
+    float* A = absact_out;
+    if (!A) {
+        const size_t need = (size_t)M * L->n_pad;
+        if (L->absA_floats < need) {
+            if (capturing(st)) return fail(SI_ERR_INVALID_ARG, "|A| scratch must grow; call once before capture");
+            dfree(L->absA);
+            L->absA_floats = 0;
+            rc = dalloc(&L->absA, need, "|A| scratch");
+            if (rc) return rc;
+            L->absA_floats = need;
+        }
+        A = L->absA;
+    }
+    si::ActGemmParams P = {};
+    P.X = X;
+    P.M = M;
+    P.K = L->d;
+    P.Wgate = L->packed;
+    P.Wup = L->packed + L->d;
+    P.w_stride = 3LL * L->d;
+    P.Nrows = L->n_pad;
+    P.Nvalid = L->n_pad;
+    P.mode = 0;
+    P.out = A;
+    P.ldo = L->n_pad;
+    P.err = err;
+    SI_CK(si::launch_act_gemm(P, st));
+    return select_core(L, A, L->n_pad, T, B, alpha, phi, S, nullptr, nullptr, st);
+}
+
+// ------------------------------------------------------------------ a7
+
+int si_decode_plan(si_layer* L, const int32_t* S, int n_sel, int B, void* stream) {
+    if (!L || !S) return fail(SI_ERR_INVALID_ARG, "NULL pointer");
+    if (B < 1 || B > 8) return fail(SI_ERR_INVALID_ARG, "need 1 <= B <= 8");
+    if (n_sel < 0 || n_sel > L->n_loaded) return fail(SI_ERR_INVALID_ARG, "need 0 <= n_sel <= n_loaded");
+    cudaStream_t st = (cudaStream_t)stream;
+    unsigned* err = nullptr;
+    int rc = err_word(&err);
+    if (rc) return rc;
+    if (!L->plan_pos) {
+        if (capturing(st)) return fail(SI_ERR_INVALID_ARG, "plan buffers must be allocated before capture");
+        if ((rc = dalloc(&L->plan_pos, L->n_loaded, "plan positions")) ||
+            (rc = dalloc(&L->plan_mask, L->n_loaded, "plan masks")) || (rc = dalloc(&L->plan_n, 1, "plan count")))
+            return rc;
+    }
+    if (L->part_floats < si::decode_max_partial_floats(L->d, B)) {
+        if (capturing(st)) return fail(SI_ERR_INVALID_ARG, "partials must grow; call once before capture");
+        rc = grow_part(&L->part, &L->part_floats, L->d, B);
+        if (rc) return rc;
+    }
+    SI_CK(si::launch_decode_plan(S, n_sel, B, L->n_loaded, L->plan_pos, L->plan_mask, L->plan_n, err, st));
+    L->plan_S = S;
+    L->plan_nsel = n_sel;
+    L->plan_B = B;
+    return SI_OK;
+}
+
+int si_sparse_ffn_decode(si_layer* L, const int32_t* S, int n_sel, int B, const uint16_t* x, float* y,
+                         void* stream) {
+    if (!L || !S || !x || !y) return fail(SI_ERR_INVALID_ARG, "NULL pointer");
+    if (B < 1 || B > 8) return fail(SI_ERR_INVALID_ARG, "need 1 <= B <= 8");
+    if (n_sel < 0 || n_sel > L->n_loaded) return fail(SI_ERR_INVALID_ARG, "need 0 <= n_sel <= n_loaded");
+    if (L->d > 4096) return fail(SI_ERR_UNSUPPORTED, "decode supports d <= 4096");
+    if (B > 1 && (L->plan_S != S || L->plan_nsel != n_sel || L->plan_B != B))
+        return fail(SI_ERR_INVALID_ARG, "B > 1 needs si_decode_plan with the same S, n_sel and B first");
+    unsigned* err = nullptr;
+    int rc = err_word(&err);
+    if (rc) return rc;
+    si::SparseDecodeParams P = {};
+    P.packed = L->packed;
+    P.n_records = L->n_pad;
+    P.d = L->d;
+    P.x = x;
+    P.y = y;
+    P.part = L->part;
+    P.part_floats = L->part_floats;
+    P.tickets = L->tickets;
+    P.err = err;
+    P.R = si::sparse_decode_stages(L->d, B);
+    if (P.R < 8) return fail(SI_ERR_UNSUPPORTED, "d too large for the decode ring");
+    if (B == 1) {
+        P.pos = S;
+        P.pmask = nullptr;
+        P.n_dev = nullptr;
+        P.n_host = n_sel;
+    } else {
+        P.pos = L->plan_pos;
+        P.pmask = L->plan_mask;
+        P.n_dev = L->plan_n;
+        P.n_host = 0;
+    }
+    SI_CK(si::launch_sparse_decode(P, B, (cudaStream_t)stream));
+    return SI_OK;
+}
+
+// ------------------------------------------------------------------ SpAx
+
+int spax_encode(const uint16_t* Wd, int d, int N, int bits, int group, spax_layer** out, void* stream) {
+    if (!out) return fail(SI_ERR_INVALID_ARG, "out is NULL");
+    *out = nullptr;
+    if (!Wd) return fail(SI_ERR_INVALID_ARG, "NULL pointer");
+    if (bits != 4) return fail(SI_ERR_UNSUPPORTED, "only 4-bit codes are implemented");
+    if (group < 8 || group % 8 || d < 64 || d % 64 || d % group)
+        return fail(SI_ERR_INVALID_ARG, "need group % 8 == 0, d % 64 == 0, d % group == 0");
+    if (d > 4096) return fail(SI_ERR_UNSUPPORTED, "tiered decode supports d <= 4096");
+    if (N < 1 || N > 32768) return fail(SI_ERR_INVALID_ARG, "need 1 <= N <= 32768");
+    cudaStream_t st = (cudaStream_t)stream;
+    if (capturing(st)) return fail(SI_ERR_INVALID_ARG, "spax_encode allocates; not allowed during capture");
+    spax_layer* L = new spax_layer();
+    SI_CK(cudaGetDevice(&L->device));
+    L->d = d;
+    L->N = N;
+    L->bits = bits;
+    L->group = group;
+    L->ngp = round_up(d / group, 2);
+    int rc;
+    if ((rc = dalloc(&L->WdT, (size_t)N * d, "column-major Wd")) ||
+        (rc = dalloc(&L->codes, (size_t)N * d / 2, "codes")) ||
+        (rc = dalloc(&L->params, (size_t)N * L->ngp * 2, "code params")) || (rc = dalloc(&L->top, N, "top tier")) ||
+        (rc = dalloc(&L->mid, N, "mid tier")) || (rc = dalloc(&L->a, N, "activations")) ||
+        (rc = dalloc(&L->tickets, 16, "tickets")) || (rc = grow_part(&L->part, &L->part_floats, d, 1))) {
+        destroy_spax(L);
+        return rc;
+    }
+    cudaError_t e = cudaMemsetAsync(L->tickets, 0, 16 * sizeof(unsigned), st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(L->params, 0, (size_t)N * L->ngp * 2 * sizeof(float), st);
+    if (e == cudaSuccess) e = si::launch_spax_encode(Wd, d, N, group, L->ngp, L->WdT, L->codes, L->params, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) {
+        destroy_spax(L);
+        return cuda_fail(e, "spax_encode");
+    }
+    *out = L;
+    return SI_OK;
+}
+
+int spax_layer_info(const spax_layer* L, int* d, int* N, int* bits, int* group, int* ngp) {
+    if (!L) return fail(SI_ERR_INVALID_ARG, "layer is NULL");
+    if (d) *d = L->d;
+    if (N) *N = L->N;
+    if (bits) *bits = L->bits;
+    if (group) *group = L->group;
+    if (ngp) *ngp = L->ngp;
+    return SI_OK;
+}
+
+int spax_layer_buffers(const spax_layer* L, const uint16_t** WdT, const uint8_t** codes, const float** params) {
+    if (!L) return fail(SI_ERR_INVALID_ARG, "layer is NULL");
+    if (WdT) *WdT = L->WdT;
+    if (codes) *codes = L->codes;
+    if (params) *params = L->params;
+    return SI_OK;
+}
+
+int spax_layer_destroy(spax_layer* L) {
+    if (!L) return SI_OK;
+    cudaDeviceSynchronize();
+    destroy_spax(L);
+    return SI_OK;
+}
+
+int spax_dense_act(const uint16_t* Wg, const uint16_t* Wu, int d, int N, const uint16_t* x, float* a, void* stream) {
+    if (!Wg || !Wu || !x || !a) return fail(SI_ERR_INVALID_ARG, "NULL pointer");
+    if (d < 8 || d % 8 || N < 1) return fail(SI_ERR_INVALID_ARG, "need d % 8 == 0, N >= 1");
+    if (d > 4096) return fail(SI_ERR_UNSUPPORTED, "dense activation pass supports d <= 4096");
+    unsigned* err = nullptr;
+    int rc = err_word(&err);
+    if (rc) return rc;
+    si::DenseActParams P = {};
+    P.Wg = Wg;
+    P.Wu = Wu;
+    P.d = d;
+    P.N = N;
+    P.x = x;
+    P.a = a;
+    P.err = err;
+    P.R = si::dense_act_stages(d);
+    if (P.R < 2) return fail(SI_ERR_UNSUPPORTED, "d too large for the activation ring");
+    SI_CK(si::launch_dense_act(P, (cudaStream_t)stream));
+    return SI_OK;
+}
+
+int spax_tiered_down(spax_layer* L, const float* a, double top_frac, double mid_frac, float* y, int32_t* top_idx,
+                     int32_t* mid_idx, void* stream) {
+    if (!L || !a || !y) return fail(SI_ERR_INVALID_ARG, "NULL pointer");
+    if (!(top_frac >= 0.0 && mid_frac >= 0.0 && top_frac <= 1.0 && mid_frac <= 1.0))
+        return fail(SI_ERR_INVALID_ARG, "tier fractions must be in [0, 1]");
+    const long long k_top = count_of(top_frac, L->N), k_mid = count_of(mid_frac, L->N);
+    if (k_top + k_mid > L->N) return fail(SI_ERR_INVALID_ARG, "top + mid tiers exceed N");
+    cudaStream_t st = (cudaStream_t)stream;
+    unsigned* err = nullptr;
+    int rc = err_word(&err);
+    if (rc) return rc;
+    int32_t* top = top_idx ? top_idx : L->top;
+    int32_t* mid = mid_idx ? mid_idx : L->mid;
+    SI_CK(si::launch_spax_tiers(a, L->N, (int)k_top, (int)k_mid, top, mid, err, st));
+    si::TieredDownParams P = {};
+    P.WdT = L->WdT;
+    P.codes = L->codes;
+    P.params = L->params;
+    P.a = a;
+    P.top = top;
+    P.mid = mid;
+    P.d = L->d;
+    P.group = L->group;
+    P.ngp = L->ngp;
+    P.k_top = (int)k_top;
+    P.k_mid = (int)k_mid;
+    P.N = L->N;
+    P.y = y;
+    P.part = L->part;
+    P.part_floats = L->part_floats;
+    P.tickets = L->tickets;
+    P.err = err;
+    const int gmin = si::streaming_grid_upper_bound() / 4;  // grids are at least a quarter of the SMs
+    P.aux_floats = round_up((int)(L->N / (gmin > 0 ? gmin : 1)) * 2 + 8, 32);
+    P.R = si::tiered_down_stages(L->d, P.aux_floats);
+    if (P.R < 2) return fail(SI_ERR_UNSUPPORTED, "d too large for the tier ring");
+    SI_CK(si::launch_tiered_down(P, st));
+    return SI_OK;
+}
+
+int spax_ffn_decode(spax_layer* L, const uint16_t* Wg, const uint16_t* Wu, const uint16_t* x, double top_frac,
+                    double mid_frac, float* y, float* a_out, void* stream) {
+    if (!L) return fail(SI_ERR_INVALID_ARG, "layer is NULL");
+    float* a = a_out ? a_out : L->a;
+    int rc = spax_dense_act(Wg, Wu, L->d, L->N, x, a, stream);
+    if (rc) return rc;
+    return spax_tiered_down(L, a, top_frac, mid_frac, y, nullptr, nullptr, stream);
+}
+
+}  // extern "C"

@@ -1,0 +1,104 @@
+// internal.h -- launcher interface between the C-ABI layer (api.cu) and the
+// kernels. Not installed; not part of the public ABI.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace si {
+
+struct SparseDecodeParams {
+    const uint16_t* packed;   // [n_pad][3][d] bf16
+    int d;
+    const int32_t* pos;       // plan positions
+    int n_records;            // records in `packed` (positions must be below it)
+    const uint32_t* pmask;    // per-entry sequence mask, or nullptr (all sequences)
+    const int* n_dev;         // device-resident entry count, or nullptr
+    int n_host;               // entry count when n_dev == nullptr
+    const uint16_t* x;        // [B][d] bf16
+    float* y;                 // [B][d] fp32
+    float* part;              // [clusters][B*d] scratch
+    long long part_floats;    // capacity of part
+    unsigned* tickets;        // [16], zero between launches
+    unsigned* err;            // device error word
+    int R;                    // ring stages
+};
+
+struct DenseActParams {
+    const uint16_t* Wg;
+    const uint16_t* Wu;
+    int d, N;
+    const uint16_t* x;
+    float* a;
+    unsigned* err;
+    int R;
+};
+
+struct TieredDownParams {
+    const uint16_t* WdT;      // [N][d] bf16
+    const uint8_t* codes;     // [N][d/2]
+    const float* params;      // [N][ngp][2]
+    const float* a;           // [N]
+    const int32_t* top;       // [k_top]
+    const int32_t* mid;       // [k_mid]
+    int d, group, ngp, k_top, k_mid;
+    int N;                    // columns (indices must be below it)
+    float* y;                 // [d]
+    float* part;
+    long long part_floats;
+    unsigned* tickets;
+    unsigned* err;
+    int R;
+    int aux_floats;           // capacity of the per-CTA activation buffer
+};
+
+// select.cu
+cudaError_t launch_topk_alpha(const float* absA, int ld, int n, int T, int B, int alpha, uint32_t* counts,
+                              uint32_t* topmask, cudaStream_t st);
+cudaError_t launch_topk_beta(const uint32_t* counts, const uint8_t* is_static, int n, int B, int beta, int n_sel,
+                             int32_t* S, unsigned* err, cudaStream_t st);
+cudaError_t launch_rank_loaded(const float* task, const float* model, int N, int n_base, int n_load,
+                               int32_t* loaded, uint8_t* is_static, unsigned* err, cudaStream_t st);
+cudaError_t launch_decode_plan(const int32_t* S, int n_sel, int B, int n, int32_t* pos, uint32_t* pmask,
+                               int* count, unsigned* err, cudaStream_t st);
+cudaError_t launch_spax_tiers(const float* a, int N, int k_top, int k_mid, int32_t* top, int32_t* mid,
+                              unsigned* err, cudaStream_t st);
+cudaError_t launch_merge_scores(const float* const* s, const float* tok, int nfiles, int N, float* out,
+                                cudaStream_t st);
+
+// pack.cu
+cudaError_t launch_pack_loaded(const uint16_t* Wg, const uint16_t* Wu, const uint16_t* Wd, int d, int N,
+                               const int32_t* loaded, int n_loaded, int n_pad, uint16_t* packed, cudaStream_t st);
+cudaError_t launch_spax_encode(const uint16_t* Wd, int d, int N, int group, int ngp, uint16_t* WdT, uint8_t* codes,
+                               float* params, cudaStream_t st);
+
+// decode.cu
+int sparse_decode_stages(int d, int B);
+int decode_max_partial_floats(int d, int B);
+cudaError_t launch_sparse_decode(SparseDecodeParams P, int B, cudaStream_t st);
+int dense_act_stages(int d);
+cudaError_t launch_dense_act(DenseActParams P, cudaStream_t st);
+int tiered_down_stages(int d, int aux_floats);
+cudaError_t launch_tiered_down(TieredDownParams P, cudaStream_t st);
+int streaming_grid_upper_bound();
+
+// gemm.cu -- tcgen05 activation GEMM: rows of X against gate/up row pairs.
+//   mode 0: out[r * ldo + p] = |silu(g) * u| for r < M, p < Npad (fp32)
+//   mode 1: colsum[p] += sum_r |silu(g) * u| over r < M, p < Nvalid
+struct ActGemmParams {
+    const uint16_t* X;        // [M][K] bf16
+    int M, K;
+    const uint16_t* Wgate;    // row p at Wgate + p * w_stride (elements)
+    const uint16_t* Wup;      // row p at Wup + p * w_stride
+    long long w_stride;       // elements between consecutive neuron rows
+    int Nrows;                // rows addressable in the weight tensors
+    int Nvalid;               // columns written / summed
+    int mode;
+    float* out;
+    long long ldo;
+    float* colsum;
+    unsigned* err;
+};
+cudaError_t launch_act_gemm(const ActGemmParams& P, cudaStream_t st);
+
+}  // namespace si

@@ -1,0 +1,401 @@
+// select.cu -- exact top-k selection kernels.
+//
+// Every ranking of the method is "the k largest by a key, ties to the lower
+// index": per-token top-alpha of |a| and top-beta of counts (SelectInfer
+// section 5, Fig. 7), base/secondary neurons by profiler score (section 4,
+// Fig. 6), and the SpAx tiers by |a| (abstract, Fig. 2). All of them use one
+// block-wide primitive:
+//   block_topk_cut   4 passes of an 8-bit radix histogram over 32-bit
+//                    order-preserving keys find the k-th largest key `thr`
+//                    and how many elements equal to it are still needed;
+//   block_topk_emit  walks the elements in index order with warp ballots,
+//                    takes every key > thr and the first `take_eq` keys == thr,
+//                    and reports each selected element with its rank.
+// Only integer compares decide, so results are bit-exact and independent of
+// thread scheduling.
+#include <climits>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace si {
+
+struct TopkCut {
+    uint32_t thr;
+    int take_eq;
+};
+
+// Scratch: hist[257], state[2] in shared memory.
+template <int NT, class KeyF, class EligF>
+__device__ TopkCut block_topk_cut(int n, int k, KeyF key, EligF elig, uint32_t* hist, uint32_t* state) {
+    TopkCut cut;
+    if (k <= 0) {
+        cut.thr = 0xFFFFFFFFu;
+        cut.take_eq = 0;
+        return cut;
+    }
+    const int lane = threadIdx.x & 31;
+    uint32_t prefix = 0, pmask = 0;
+    int kk = k;
+    const int rounds = (n + NT - 1) / NT;
+    for (int shift = 24; shift >= 0; shift -= 8) {
+        for (int i = threadIdx.x; i < 257; i += NT) hist[i] = 0;
+        __syncthreads();
+        for (int r = 0; r < rounds; ++r) {
+            const int i = r * NT + threadIdx.x;
+            uint32_t bin = 256;
+            if (i < n && elig(i)) {
+                const uint32_t kv = key(i);
+                if ((kv & pmask) == prefix) bin = (kv >> shift) & 255u;
+            }
+            const uint32_t peers = __match_any_sync(0xFFFFFFFFu, bin);
+            if (bin != 256u && lane == __ffs(peers) - 1) atomicAdd(&hist[bin], (uint32_t)__popc(peers));
+        }
+        __syncthreads();
+        if (threadIdx.x < 32) {
+            // lane l owns bins 255-8l .. 248-8l, visited from the top down
+            uint32_t c[8], sum = 0;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                c[j] = hist[255 - 8 * lane - j];
+                sum += c[j];
+            }
+            uint32_t inc = sum;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, inc, o);
+                if (lane >= o) inc += v;
+            }
+            const uint32_t exc = inc - sum;
+            const bool hit = exc < (uint32_t)kk && (uint32_t)kk <= inc;
+            if (hit) {
+                uint32_t run = exc;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    if (run + c[j] >= (uint32_t)kk) {
+                        state[0] = (uint32_t)(255 - 8 * lane - j);
+                        state[1] = (uint32_t)kk - run;
+                        break;
+                    }
+                    run += c[j];
+                }
+            }
+            if (__ballot_sync(0xFFFFFFFFu, hit) == 0u && lane == 0) state[0] = 0xFFFFFFFFu;
+        }
+        __syncthreads();
+        const uint32_t digit = state[0];
+        const int nkk = (int)state[1];
+        __syncthreads();
+        if (digit == 0xFFFFFFFFu) {  // fewer eligible elements than k: take them all
+            cut.thr = 0u;
+            cut.take_eq = INT_MAX;
+            return cut;
+        }
+        prefix |= digit << shift;
+        pmask |= 0xFFu << shift;
+        kk = nkk;
+    }
+    cut.thr = prefix;
+    cut.take_eq = kk;
+    return cut;
+}
+
+// Scratch: scnt[2 * NT / 32]. Calls out(i, rank) for each selected element
+// (rank = position among selected ones in index order) and, when WORDS,
+// word(i / 32, ballot) once per 32 elements. Returns the number selected.
+template <int NT, bool WORDS, class KeyF, class EligF, class OutF, class WordF>
+__device__ int block_topk_emit(int n, TopkCut cut, KeyF key, EligF elig, OutF out, WordF word,
+                               uint32_t* scnt) {
+    constexpr int NW = NT / 32;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int eq_base = 0, sel_base = 0;
+    const int rounds = (n + NT - 1) / NT;
+    for (int r = 0; r < rounds; ++r) {
+        const int i = r * NT + threadIdx.x;
+        bool gt = false, eq = false;
+        if (i < n && elig(i)) {
+            const uint32_t kv = key(i);
+            gt = kv > cut.thr;
+            eq = kv == cut.thr;
+        }
+        const uint32_t meq = __ballot_sync(0xFFFFFFFFu, eq);
+        if (lane == 0) scnt[warp] = (uint32_t)__popc(meq);
+        __syncthreads();
+        int eq_off = 0, eq_tot = 0;
+        for (int w = 0; w < NW; ++w) {
+            const int c = (int)scnt[w];
+            eq_off += (w < warp) ? c : 0;
+            eq_tot += c;
+        }
+        const int eq_rank = eq_base + eq_off + __popc(meq & lanemask_lt());
+        const bool s = gt || (eq && eq_rank < cut.take_eq);
+        const uint32_t ms = __ballot_sync(0xFFFFFFFFu, s);
+        if (lane == 0) {
+            scnt[NW + warp] = (uint32_t)__popc(ms);
+            if (WORDS && r * NT + warp * 32 < n) word((r * NT + warp * 32) >> 5, ms);
+        }
+        __syncthreads();
+        int s_off = 0, s_tot = 0;
+        for (int w = 0; w < NW; ++w) {
+            const int c = (int)scnt[NW + w];
+            s_off += (w < warp) ? c : 0;
+            s_tot += c;
+        }
+        if (s) out(i, sel_base + s_off + __popc(ms & lanemask_lt()));
+        eq_base += eq_tot;
+        sel_base += s_tot;
+        __syncthreads();
+    }
+    return sel_base;
+}
+
+struct NoWord {
+    __device__ void operator()(int, uint32_t) const {}
+};
+
+// Ordered compaction: out(i, rank) for every i with pred(i), in index order.
+template <int NT, class PredF, class OutF>
+__device__ int block_compact(int n, PredF pred, OutF out, uint32_t* scnt) {
+    TopkCut all;
+    all.thr = 0u;
+    all.take_eq = 0;
+    auto key = [&](int i) -> uint32_t { return pred(i) ? 1u : 0u; };
+    auto elig = [](int) { return true; };
+    return block_topk_emit<NT, false>(n, all, key, elig, out, NoWord(), scnt);
+}
+
+// ------------------------------------------------------------------- kernels
+
+constexpr int kSelNT = 512;
+
+// a4 + a5: one CTA per token row. Per-token top-alpha over the loaded
+// positions by |A| (SelectInfer section 5); every selected position adds 1 to
+// its sequence's count. Optional bit mask of the selection per row.
+__global__ void __launch_bounds__(kSelNT) k_topk_alpha(const float* __restrict__ absA, int ld, int n, int T,
+                                                      int alpha, uint32_t* __restrict__ counts,
+                                                      uint32_t* __restrict__ topmask, int words) {
+    extern __shared__ __align__(16) uint32_t s_keys[];
+    __shared__ uint32_t hist[257], state[2], scnt[2 * kSelNT / 32];
+    const int row = blockIdx.x;
+    const int b = row / T;
+    const float* src = absA + (size_t)row * ld;
+    for (int i = threadIdx.x; i < n; i += kSelNT) s_keys[i] = abs_key(__ldg(src + i));
+    __syncthreads();
+    auto key = [&](int i) -> uint32_t { return s_keys[i]; };
+    auto elig = [](int) { return true; };
+    const TopkCut cut = block_topk_cut<kSelNT>(n, alpha, key, elig, hist, state);
+    uint32_t* cnt = counts + (size_t)b * n;
+    uint32_t* tm = topmask ? topmask + (size_t)row * words : nullptr;
+    auto out = [&](int i, int) { atomicAdd(cnt + i, 1u); };
+    auto word = [&](int wi, uint32_t bits) {
+        if (tm) tm[wi] = bits;
+    };
+    block_topk_emit<kSelNT, true>(n, cut, key, elig, out, word, scnt);
+}
+
+// a6: one CTA per sequence. Top-beta of the counts among non-static positions
+// (ties to the lower position), united with the static positions, written as
+// an ascending list of n_sel positions.
+__global__ void __launch_bounds__(1024) k_topk_beta(const uint32_t* __restrict__ counts,
+                                                   const uint8_t* __restrict__ is_static, int n, int beta,
+                                                   int n_sel, int32_t* __restrict__ S, unsigned* err) {
+    extern __shared__ __align__(16) uint32_t s_keys[];  // n keys, then n flag bytes
+    uint8_t* s_take = reinterpret_cast<uint8_t*>(s_keys + n);
+    __shared__ uint32_t hist[257], state[2], scnt[2 * 1024 / 32];
+    const int b = blockIdx.x;
+    for (int i = threadIdx.x; i < n; i += 1024) {
+        s_keys[i] = counts[(size_t)b * n + i];
+        s_take[i] = is_static[i] ? 1 : 0;
+    }
+    __syncthreads();
+    auto key = [&](int i) -> uint32_t { return s_keys[i]; };
+    auto elig = [&](int i) { return is_static[i] == 0; };
+    const TopkCut cut = block_topk_cut<1024>(n, beta, key, elig, hist, state);
+    auto mark = [&](int i, int) { s_take[i] = 1; };
+    block_topk_emit<1024, false>(n, cut, key, elig, mark, NoWord(), scnt);
+    __syncthreads();
+    int32_t* dst = S + (size_t)b * n_sel;
+    auto pred = [&](int i) { return s_take[i] != 0; };
+    auto put = [&](int i, int r) {
+        if (r < n_sel) dst[r] = i;
+    };
+    const int total = block_compact<1024>(n, pred, put, scnt);
+    if (threadIdx.x == 0 && total != n_sel) atomicOr(err, SI_DEVERR_COUNT);
+}
+
+// a2: selective loading ranking (SelectInfer section 4, Fig. 6), one CTA.
+// base = top n_base by task score; secondary = top (n_load - n_base) by model
+// score among the rest; loaded positions ascending by neuron index.
+__global__ void __launch_bounds__(1024) k_rank_loaded(const float* __restrict__ task,
+                                                     const float* __restrict__ model, int N, int n_base,
+                                                     int n_load, int32_t* __restrict__ loaded,
+                                                     uint8_t* __restrict__ is_static, unsigned* err) {
+    extern __shared__ __align__(16) uint8_t s_flags[];  // N base flags, N take flags
+    uint8_t* s_base = s_flags;
+    uint8_t* s_take = s_flags + N;
+    __shared__ uint32_t hist[257], state[2], scnt[2 * 1024 / 32];
+    for (int i = threadIdx.x; i < N; i += 1024) {
+        s_base[i] = 0;
+        s_take[i] = 0;
+    }
+    __syncthreads();
+    auto key1 = [&](int i) -> uint32_t { return value_key(task[i]); };
+    auto all = [](int) { return true; };
+    const TopkCut c1 = block_topk_cut<1024>(N, n_base, key1, all, hist, state);
+    auto mark1 = [&](int i, int) {
+        s_base[i] = 1;
+        s_take[i] = 1;
+    };
+    block_topk_emit<1024, false>(N, c1, key1, all, mark1, NoWord(), scnt);
+    __syncthreads();
+    auto key2 = [&](int i) -> uint32_t { return value_key(model[i]); };
+    auto notbase = [&](int i) { return s_base[i] == 0; };
+    const TopkCut c2 = block_topk_cut<1024>(N, n_load - n_base, key2, notbase, hist, state);
+    auto mark2 = [&](int i, int) { s_take[i] = 1; };
+    block_topk_emit<1024, false>(N, c2, key2, notbase, mark2, NoWord(), scnt);
+    __syncthreads();
+    auto pred = [&](int i) { return s_take[i] != 0; };
+    auto put = [&](int i, int r) {
+        if (r < n_load) {
+            loaded[r] = i;
+            is_static[r] = s_base[i];
+        }
+    };
+    const int total = block_compact<1024>(N, pred, put, scnt);
+    if (threadIdx.x == 0 && total != n_load) atomicOr(err, SI_DEVERR_COUNT);
+}
+
+// Decode plan for B sequences: union of the B position lists with a per-entry
+// mask of the sequences that selected it (one CTA).
+__global__ void __launch_bounds__(1024) k_decode_plan(const int32_t* __restrict__ S, int n_sel, int B, int n,
+                                                     int32_t* __restrict__ pos, uint32_t* __restrict__ pmask,
+                                                     int* __restrict__ count, unsigned* err) {
+    extern __shared__ __align__(16) uint32_t s_mask[];
+    __shared__ uint32_t scnt[2 * 1024 / 32];
+    for (int i = threadIdx.x; i < n; i += 1024) s_mask[i] = 0;
+    __syncthreads();
+    for (int j = threadIdx.x; j < B * n_sel; j += 1024) {
+        const int p = S[j];
+        if (p >= 0 && p < n)
+            atomicOr(&s_mask[p], 1u << (j / n_sel));
+        else
+            atomicOr(err, SI_DEVERR_COUNT);
+    }
+    __syncthreads();
+    auto pred = [&](int i) { return s_mask[i] != 0u; };
+    auto put = [&](int i, int r) {
+        pos[r] = i;
+        pmask[r] = s_mask[i];
+    };
+    const int total = block_compact<1024>(n, pred, put, scnt);
+    if (threadIdx.x == 0) *count = total;
+}
+
+// SpAx tiers (abstract, Fig. 2): top = k_top largest |a|, mid = next k_mid,
+// ties to the lower column; both lists ascending. One CTA.
+__global__ void __launch_bounds__(1024) k_spax_tiers(const float* __restrict__ a, int N, int k_top, int k_mid,
+                                                    int32_t* __restrict__ top, int32_t* __restrict__ mid,
+                                                    unsigned* err) {
+    extern __shared__ __align__(16) uint32_t s_keys[];  // N keys, N flag bytes
+    uint8_t* s_top = reinterpret_cast<uint8_t*>(s_keys + N);
+    __shared__ uint32_t hist[257], state[2], scnt[2 * 1024 / 32];
+    for (int i = threadIdx.x; i < N; i += 1024) {
+        s_keys[i] = abs_key(a[i]);
+        s_top[i] = 0;
+    }
+    __syncthreads();
+    auto key = [&](int i) -> uint32_t { return s_keys[i]; };
+    auto all = [](int) { return true; };
+    const TopkCut c1 = block_topk_cut<1024>(N, k_top, key, all, hist, state);
+    auto put1 = [&](int i, int r) {
+        s_top[i] = 1;
+        if (r < k_top) top[r] = i;
+    };
+    const int n1 = block_topk_emit<1024, false>(N, c1, key, all, put1, NoWord(), scnt);
+    __syncthreads();
+    auto nottop = [&](int i) { return s_top[i] == 0; };
+    const TopkCut c2 = block_topk_cut<1024>(N, k_mid, key, nottop, hist, state);
+    auto put2 = [&](int i, int r) {
+        if (r < k_mid) mid[r] = i;
+    };
+    const int n2 = block_topk_emit<1024, false>(N, c2, key, nottop, put2, NoWord(), scnt);
+    if (threadIdx.x == 0 && (n1 != k_top || n2 != k_mid)) atomicOr(err, SI_DEVERR_COUNT);
+}
+
+// Score-file merge (SelectInfer section 3): out[n] = sum_f s_f[n] / T_f in
+// float32, files in order, each step rounded (no contraction).
+struct MergeArgs {
+    const float* s[16];
+    float tok[16];
+    int nfiles;
+};
+
+__global__ void k_merge_scores(MergeArgs args, int N, float* __restrict__ out) {
+    for (int n = blockIdx.x * blockDim.x + threadIdx.x; n < N; n += gridDim.x * blockDim.x) {
+        float acc = 0.0f;
+        for (int f = 0; f < args.nfiles; ++f) acc = __fadd_rn(acc, __fdiv_rn(args.s[f][n], args.tok[f]));
+        out[n] = acc;
+    }
+}
+
+// ------------------------------------------------------------------ launchers
+
+cudaError_t launch_topk_alpha(const float* absA, int ld, int n, int T, int B, int alpha, uint32_t* counts,
+                              uint32_t* topmask, cudaStream_t st) {
+    const size_t smem = (size_t)n * 4;
+    cudaError_t e = cudaFuncSetAttribute(k_topk_alpha, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    k_topk_alpha<<<B * T, kSelNT, smem, st>>>(absA, ld, n, T, alpha, counts, topmask, (n + 31) / 32);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_topk_beta(const uint32_t* counts, const uint8_t* is_static, int n, int B, int beta, int n_sel,
+                             int32_t* S, unsigned* err, cudaStream_t st) {
+    const size_t smem = (size_t)n * 5 + 16;
+    cudaError_t e = cudaFuncSetAttribute(k_topk_beta, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    k_topk_beta<<<B, 1024, smem, st>>>(counts, is_static, n, beta, n_sel, S, err);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_rank_loaded(const float* task, const float* model, int N, int n_base, int n_load,
+                               int32_t* loaded, uint8_t* is_static, unsigned* err, cudaStream_t st) {
+    const size_t smem = (size_t)N * 2 + 16;
+    cudaError_t e = cudaFuncSetAttribute(k_rank_loaded, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    k_rank_loaded<<<1, 1024, smem, st>>>(task, model, N, n_base, n_load, loaded, is_static, err);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_decode_plan(const int32_t* S, int n_sel, int B, int n, int32_t* pos, uint32_t* pmask,
+                               int* count, unsigned* err, cudaStream_t st) {
+    const size_t smem = (size_t)n * 4;
+    cudaError_t e = cudaFuncSetAttribute(k_decode_plan, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    k_decode_plan<<<1, 1024, smem, st>>>(S, n_sel, B, n, pos, pmask, count, err);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_spax_tiers(const float* a, int N, int k_top, int k_mid, int32_t* top, int32_t* mid,
+                              unsigned* err, cudaStream_t st) {
+    const size_t smem = (size_t)N * 5 + 16;
+    cudaError_t e = cudaFuncSetAttribute(k_spax_tiers, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    k_spax_tiers<<<1, 1024, smem, st>>>(a, N, k_top, k_mid, top, mid, err);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_merge_scores(const float* const* s, const float* tok, int nfiles, int N, float* out,
+                                cudaStream_t st) {
+    MergeArgs a;
+    for (int f = 0; f < 16; ++f) {
+        a.s[f] = f < nfiles ? s[f] : nullptr;
+        a.tok[f] = f < nfiles ? tok[f] : 1.0f;
+    }
+    a.nfiles = nfiles;
+    const int blocks = (N + 255) / 256 < 1024 ? (N + 255) / 256 : 1024;
+    k_merge_scores<<<blocks, 256, 0, st>>>(a, N, out);
+    return cudaGetLastError();
+}
+
+}  // namespace si

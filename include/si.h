@@ -1,0 +1,247 @@
+/*
+ * si.h -- C ABI of the GB300 (sm_103a) activation-sparse FFN library.
+ *
+ * Method sources (cited per entry point below):
+ *   [SI]   "SelectInfer: Selective Neuron Loading and Computation for
+ *          On-Device LLMs" (arXiv 2607.18081v1): section 3 LLM Profiler,
+ *          Eq. (1); section 4 Selective Loading, Fig. 6; section 5 Selective
+ *          Computation, Fig. 7; section 6.6 Eq. (2); Table 1.
+ *   [SPAX] "Activation Sparsity with Weight Approximation for Faster LLM
+ *          Decoding on Offloaded Weights": abstract; Fig. 2 (offline
+ *          encoding, per-token tier choice); Fig. 3 (middle-tier column
+ *          rebuilt from its own b-bit codes).
+ *   [LS]   "LeanStream: A Speculate-and-Refine Streaming Framework for
+ *          Efficient on-Device LLM Inference", permutation-invariant
+ *          execution: a SwiGLU FFN output is a sum over hidden neurons, so
+ *          neuron order in memory is free.
+ *
+ * Conventions (all entry points):
+ *   - Every function returns an int status: SI_OK, or an SI_ERR_* code;
+ *     si_last_error_string() then describes the failure (thread-local).
+ *     Nothing throws or aborts across this boundary.
+ *   - Pointers are DEVICE pointers unless the argument is marked (host).
+ *     The caller owns inputs and outputs; the library owns the si_layer /
+ *     spax_layer handles and everything inside them.
+ *   - bf16 tensors are passed as uint16_t bit patterns. HF layouts:
+ *     Wg, Wu are [N x d] row-major (neuron n = row n), Wd is [d x N]
+ *     row-major (neuron n = column n). Activations X are [rows x d].
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream). Work is enqueued asynchronously on it; calls that allocate
+ *     (layer creation, first use of a larger scratch size) do so before
+ *     enqueueing and must not run during stream capture.
+ *   - Ratios follow the pages' parameters (gamma loaded, delta static, phi
+ *     computed = delta + epsilon, tier fractions); a count is
+ *     si_count(ratio, N) = floor(ratio*N + 0.5) in double.
+ *   - Calls that use the same handle must not overlap on the GPU (they
+ *     share the handle's scratch); order them on one stream.
+ *   - Kernels never spin without a bound. A bounded wait that runs out sets
+ *     a device error word, read with si_device_error().
+ */
+#ifndef SI_H
+#define SI_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SI_OK 0
+#define SI_ERR_INVALID_ARG 1
+#define SI_ERR_CUDA 2
+#define SI_ERR_OOM 3
+#define SI_ERR_UNSUPPORTED 4
+#define SI_ERR_DEVICE 5
+
+typedef struct si_layer si_layer;
+typedef struct spax_layer spax_layer;
+
+/* ------------------------------------------------------------ utilities */
+
+/* Message of the last failing call on this thread ("" if none). The string
+ * is owned by the library and valid until the next call on this thread. */
+const char *si_last_error_string(void);
+
+/* ABI version of this header (increments on incompatible change). */
+int si_abi_version(void);
+
+/* Count of neurons for a ratio: floor(ratio * n + 0.5) computed in double.
+ * [SI] section 4/5 and Table 1 give ratios; counts round to nearest. */
+long long si_count(double ratio, long long n);
+
+/* Counts used by selective loading/computation for a layer of N neurons:
+ * n_loaded = si_count(gamma, N), n_static = si_count(delta, N),
+ * n_sel = si_count(phi, N), beta = n_sel - n_static ([SI] section 5:
+ * static + dynamic until phi = delta + epsilon). Any output pointer (host)
+ * may be NULL. Fails with SI_ERR_INVALID_ARG unless
+ * 0 <= delta <= phi <= gamma <= 1 and N >= 1. */
+int si_counts(int N, double gamma, double delta, double phi,
+              int *n_loaded, int *n_static, int *n_sel, int *beta);
+
+/* Bytes one packed layer keeps for n_loaded neurons of width d: gate row, up
+ * row and down column per neuron at 2 bytes per parameter (the complement of
+ * [SI] Eq. (2)'s saving, before tile padding). */
+long long si_packed_bytes(int d, int n_loaded);
+
+/* Reads (and with clear != 0 resets) the device error word of the current
+ * device. *code (host) receives 0 when no kernel reported a failure, else a
+ * bit set of SI_DEVERR_* values. Synchronises the device. */
+#define SI_DEVERR_WAIT_TIMEOUT 1u   /* a bounded mbarrier / TMEM wait ran out */
+#define SI_DEVERR_COUNT 2u          /* an internal count check failed */
+int si_device_error(uint32_t *code, int clear);
+
+/* --------------------------------------------------- a1: profiler score */
+
+/* Profiler score, [SI] section 3 Eq. (1): scores[n] += sum_t |a_n(x_t)| with
+ * a_n(x) = silu(Wg[n].x) * (Wu[n].x), the down_proj input. Runs on the
+ * tcgen05 tensor cores (bf16 inputs, fp32 accumulation).
+ *   Wg, Wu  bf16 [N x d]; X bf16 [T x d]; scores fp32 [N], accumulated (the
+ *   caller zeroes it and keeps the token count for merging).
+ * Requires d % 64 == 0, N >= 1, T >= 1. */
+int si_profile_scores(const uint16_t *Wg, const uint16_t *Wu, int d, int N,
+                      const uint16_t *X, int T, float *scores, void *stream);
+
+/* Merge of score files, [SI] section 3: out[n] = sum over files f (in the
+ * given order) of scores[f][n] / (float)token_counts[f], in float32.
+ *   scores (host array of nfiles DEVICE pointers, each fp32 [N]);
+ *   token_counts (host) int64 [nfiles], each >= 1; out fp32 [N] (device).
+ * 1 <= nfiles <= 16. */
+int si_merge_scores(const float *const *scores, const long long *token_counts, int nfiles,
+                    int N, float *out, void *stream);
+
+/* ------------------------------------------------- a2: selective loading */
+
+/* Selective loading, [SI] section 4 / Fig. 6: base (static) neurons are the
+ * top si_count(delta, N) by task_scores; secondary neurons are the top by
+ * model_scores among the rest until si_count(gamma, N) neurons are loaded.
+ * Ties go to the lower neuron index. Pass the same pointer twice for a single
+ * score file. The loaded neurons are kept in ascending index order in a
+ * neuron-major packed buffer [n_pad][3][d] bf16 (gate row, up row, down
+ * column contiguous per neuron; [LS] permutation invariance makes the order
+ * free), n_pad = n_loaded rounded up to 128, pad rows zero.
+ *   Wg, Wu bf16 [N x d], Wd bf16 [d x N]; task_scores, model_scores fp32 [N]
+ *   (finite). *out (host) receives a new handle. Synchronous: allocates, then
+ *   enqueues the ranking and packing kernels on `stream` and waits for them.
+ * Requires d % 64 == 0, N <= 32768, 0 <= delta <= gamma <= 1, n_loaded >= 1. */
+int si_pack_loaded(const uint16_t *Wg, const uint16_t *Wu, const uint16_t *Wd, int d, int N,
+                   const float *task_scores, const float *model_scores, double gamma,
+                   double delta, si_layer **out, void *stream);
+
+/* Shape of a packed layer; any output (host) may be NULL. */
+int si_layer_info(const si_layer *layer, int *d, int *N, int *n_loaded, int *n_static,
+                  int *n_pad);
+
+/* Device buffers owned by the layer (read-only for the caller):
+ * loaded_idx int32 [n_loaded] (original neuron index of packed position p,
+ * ascending), is_static uint8 [n_loaded], packed bf16 [n_pad][3][d].
+ * Outputs (host) may be NULL. */
+int si_layer_buffers(const si_layer *layer, const int32_t **loaded_idx,
+                     const uint8_t **is_static, const uint16_t **packed);
+
+/* Frees the handle and its device memory (synchronises the device first). */
+int si_layer_destroy(si_layer *layer);
+
+/* ------------------------------------------ a3..a6: prefill selection */
+
+/* Dynamic neuron selection during prefill, [SI] section 5 / Fig. 7, for B
+ * prompts of T tokens each (X rows are sequence-major: row b*T + t):
+ *   a3  |A|[r, p] = |a_{loaded[p]}(x_r)| for every loaded neuron, on the
+ *       tcgen05 tensor cores (bf16 x bf16 -> fp32, SiLU*up epilogue);
+ *   a4  per token, the top-alpha loaded positions by |A| (ties to the lower
+ *       position, which is the lower neuron index);
+ *   a5  per prompt, how often each position occurs in those lists;
+ *   a6  the top-beta positions by count among non-static positions (ties to
+ *       the lower position), beta = si_count(phi,N) - n_static, combined with
+ *       the static positions.
+ *   X bf16 [B*T x d]; S int32 [B x n_sel] receives ascending packed
+ *   positions, n_sel = si_count(phi, N); absact_out (optional, may be NULL)
+ *   fp32 [B*T x n_pad] receives |A| (pad columns zero).
+ * Requires 1 <= alpha <= n_loaded, n_static <= n_sel <= n_loaded, T, B >= 1. */
+int si_select_dynamic(si_layer *layer, const uint16_t *X, int T, int B, int alpha, double phi,
+                      int32_t *S, float *absact_out, void *stream);
+
+/* Steps a4..a6 of si_select_dynamic on a given |A| matrix (fp32 [B*T x ld],
+ * ld >= n_loaded, finite; only the first n_loaded columns are read, and they
+ * are ranked by magnitude). Optional outputs (may be NULL): topmask
+ * uint32 [B*T x ceil(n_loaded/32)] (bit p%32 of word p/32 set when p is in
+ * the row's top-alpha) and counts uint32 [B x n_loaded] (step a5). */
+int si_select_from_absact(si_layer *layer, const float *absA, int ld, int T, int B, int alpha,
+                          double phi, int32_t *S, uint32_t *topmask, uint32_t *counts,
+                          void *stream);
+
+/* --------------------------------------------------- a7: sparse decode */
+
+/* Builds, inside the handle, the decode plan for B > 1 sequences that each
+ * have their own computed set: the union of the B lists S[b][0..n_sel) with,
+ * per union entry, a bit mask of the sequences that selected it, so decode
+ * reads each selected neuron once. S must stay unchanged while the plan is
+ * used. Not needed for B == 1. Requires 1 <= B <= 8. */
+int si_decode_plan(si_layer *layer, const int32_t *S, int n_sel, int B, void *stream);
+
+/* Sparse decode FFN on the computed set, [SI] section 5 (only the selected
+ * neurons are computed at decode):
+ *   y[b, :] = sum over p in S[b] of a_{loaded[p]}(x_b) * Wd[:, loaded[p]].
+ * Reads only the selected packed records (gate row, up row, down column) with
+ * bulk copies, reduces over neurons inside the kernel (split over neurons
+ * across the SMs, cluster shared-memory reduction, then a fixed-order
+ * cross-cluster sum, so results are deterministic).
+ *   S int32 [B x n_sel] ascending positions (as written by the selection
+ *   calls); x bf16 [B x d]; y fp32 [B x d] (overwritten).
+ * For B > 1, si_decode_plan(layer, S, n_sel, B) must have been called with
+ * the same S pointer, n_sel and B. No allocation: safe to capture. */
+int si_sparse_ffn_decode(si_layer *layer, const int32_t *S, int n_sel, int B,
+                         const uint16_t *x, float *y, void *stream);
+
+/* ------------------------------------------------------------- SpAx */
+
+/* SpAx offline encoding, [SPAX] Fig. 2 / Fig. 3: for each column n of Wd and
+ * each group of `group` consecutive rows: scale = (max - min) / (2^bits - 1),
+ * q = clamp(floor((w - min) / scale + 0.5), 0, 2^bits - 1) (q = 0 when
+ * scale == 0), all in float32; a middle-tier weight is rebuilt as
+ * min + q * scale. The handle keeps a column-major bf16 copy of Wd (top tier,
+ * one contiguous column per neuron), the codes [N][d*bits/8] bytes (element
+ * 2i in the low nibble for bits = 4) and fp32 (scale, min) pairs
+ * [N][ng_pad][2], ng_pad = d/group rounded up to even.
+ *   Wd bf16 [d x N]. Synchronous (allocates, enqueues, waits).
+ * Requires bits == 4, group % 8 == 0, d % group == 0, d % 64 == 0. */
+int spax_encode(const uint16_t *Wd, int d, int N, int bits, int group, spax_layer **out,
+                void *stream);
+
+/* Shape of an encoded layer; outputs (host) may be NULL. */
+int spax_layer_info(const spax_layer *layer, int *d, int *N, int *bits, int *group, int *ng_pad);
+
+/* Device buffers of an encoded layer (read-only): WdT bf16 [N][d], codes
+ * uint8 [N][d*bits/8], params fp32 [N][ng_pad][2] = (scale, min). */
+int spax_layer_buffers(const spax_layer *layer, const uint16_t **WdT, const uint8_t **codes,
+                       const float **params);
+
+/* Frees the handle (synchronises the device first). */
+int spax_layer_destroy(spax_layer *layer);
+
+/* Dense gate/up pass of a SpAx decode token: a[n] = silu(Wg[n].x) *
+ * (Wu[n].x) for every neuron (the activation magnitudes that choose the
+ * tiers, [SPAX] Fig. 2). Wg, Wu bf16 [N x d]; x bf16 [d]; a fp32 [N]. */
+int spax_dense_act(const uint16_t *Wg, const uint16_t *Wu, int d, int N, const uint16_t *x,
+                   float *a, void *stream);
+
+/* Three-tier down-projection for one token, [SPAX] abstract / Fig. 2:
+ * k_top = si_count(top_frac, N) columns with the largest |a| are read in
+ * bf16, the next k_mid = si_count(mid_frac, N) are rebuilt from their codes,
+ * the rest skipped (ranking by |a| descending, ties to the lower index):
+ *   y = sum_{n in top} a[n] Wd[:, n] + sum_{n in mid} a[n] w^_n.
+ *   a fp32 [N] (finite); y fp32 [d] (overwritten); top_idx / mid_idx
+ *   (optional, may be NULL) int32 [k_top] / [k_mid] receive the tier lists in
+ *   ascending column order. Requires top_frac + mid_frac <= 1. */
+int spax_tiered_down(spax_layer *layer, const float *a, double top_frac, double mid_frac,
+                     float *y, int32_t *top_idx, int32_t *mid_idx, void *stream);
+
+/* One SpAx decode token: spax_dense_act, then spax_tiered_down on its a.
+ * a_out (optional) fp32 [N] receives the activations. */
+int spax_ffn_decode(spax_layer *layer, const uint16_t *Wg, const uint16_t *Wu,
+                    const uint16_t *x, double top_frac, double mid_frac, float *y,
+                    float *a_out, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SI_H */

@@ -16,3 +16,15 @@ def pytest_configure(config):
 @pytest.fixture(scope="session")
 def golden_dir():
     return os.path.join(ROOT, "tests", "golden")
+
+
+@pytest.fixture(autouse=True)
+def _device_error_word_clean(request):
+    """After every GPU test, no kernel may have reported a failed bounded wait
+    or a failed internal count check."""
+    yield
+    if request.node.get_closest_marker("gpu") is None:
+        return
+    import activation_sparse_gb300 as si
+    code = si.si_device_error(clear=True)
+    assert code == 0, "device error word = %#x" % code

@@ -1,0 +1,121 @@
+"""GPU parity: the sparse SwiGLU decode FFN on the computed set (one token per
+sequence) against the oracle, within the FFN tolerance."""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from gpu_util import TOL, Guarded, dev, dev_bf16, rel_err, torch
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def si():
+    import activation_sparse_gb300 as si
+    return si
+
+
+class Case:
+    def __init__(self, si, d, N, gamma, delta, phi, alpha, T, B, sigma=1.0, seed=40):
+        self.Wg, self.Wu, self.Wd = synth.layer_weights(seed, 0, d, N, sigma)
+        s = synth.lognormal_absact(seed, 1, N)[0]
+        self.layer = si.si_pack_loaded(dev_bf16(self.Wg), dev_bf16(self.Wu), dev_bf16(self.Wd), dev(s), dev(s),
+                                       gamma, delta)
+        self.loaded, self.st = oracle.rank_loaded(s, s, gamma, delta)
+        self.n_sel = si.si_count(phi, N)
+        nl = len(self.loaded)
+        A = synth.lognormal_absact(seed + 1, B * T, nl)
+        self.S = oracle.select(A, T, B, nl, self.st, min(alpha, nl), self.n_sel)
+        self.d, self.N, self.B = d, N, B
+
+
+DECODE_CASES = [
+    # d, N, gamma, delta, phi, alpha, T, B, sigma
+    (256, 1024, 0.7, 0.2, 0.4, 64, 32, 1, 1.0),          # single-layer workload
+    (2048, 8192, 0.7, 0.2, 0.4, 1024, 64, 1, 1.0),       # Llama3.2-1B layer
+    (3072, 8192, 0.7, 0.25, 0.5, 1024, 64, 1, 1.0),      # Llama3.2-3B layer
+    (2048, 11008, 0.8, 0.25, 0.5, 1024, 16, 8, 1.5),     # Qwen2.5-3B layer, 8 sequences
+    (2048, 11008, 0.8, 0.25, 0.5, 1024, 16, 3, 1.5),     # 3 sequences
+    (4096, 2048, 0.5, 0.2, 0.3, 64, 8, 1, 1.0),          # widest supported d
+    (64, 100, 1.0, 0.0, 1.0, 8, 4, 1, 1.0),              # phi = gamma = 1: dense FFN
+    (1088, 300, 0.9, 0.1, 0.2, 8, 4, 2, 1.0),            # d not a multiple of 256
+]
+
+
+@pytest.mark.parametrize("d,N,gamma,delta,phi,alpha,T,B,sigma", DECODE_CASES)
+def test_sparse_decode_parity(si, d, N, gamma, delta, phi, alpha, T, B, sigma):
+    c = Case(si, d, N, gamma, delta, phi, alpha, T, B, sigma)
+    S_dev = dev(c.S)
+    if B > 1:
+        si.si_decode_plan(c.layer, S_dev, c.n_sel, B)
+    for tok in range(2):
+        x = synth.tokens(41, tok, synth.T_DECODE, B, d)
+        y = Guarded((B, d), torch().float32, fill=float("nan"))
+        si.si_sparse_ffn_decode(c.layer, S_dev, c.n_sel, B, dev_bf16(x), y.t)
+        got = y.numpy()
+        for b in range(B):
+            ref = oracle.sparse_ffn(c.Wg, c.Wu, c.Wd, c.loaded, c.S[b], x[b])
+            err = rel_err(got[b], ref)
+            assert err <= TOL, (tok, b, err)
+            assert err <= 2e-5      # fp32 accumulation of bf16 products stays far inside the bar
+    c.layer.close()
+
+
+def test_sparse_decode_dense_limit_matches_library_dense_ffn(si):
+    # every neuron loaded and computed: the output is the dense SwiGLU FFN (numpy)
+    from scipy.special import expit
+    d, N = 512, 768
+    c = Case(si, d, N, 1.0, 0.0, 1.0, 16, 4, 1)
+    assert np.array_equal(c.S[0], np.arange(N))
+    x = synth.tokens(42, 0, synth.T_DECODE, 1, d)
+    y = Guarded((1, d), torch().float32)
+    si.si_sparse_ffn_decode(c.layer, dev(c.S), N, 1, dev_bf16(x), y.t)
+    xf = synth.bf16_bits_to_f32(x[0]).astype(np.float64)
+    g = synth.bf16_bits_to_f32(c.Wg).astype(np.float64) @ xf
+    u = synth.bf16_bits_to_f32(c.Wu).astype(np.float64) @ xf
+    ref = synth.bf16_bits_to_f32(c.Wd).astype(np.float64) @ (g * expit(g) * u)
+    assert rel_err(y.numpy()[0], ref) <= 2e-5
+    c.layer.close()
+
+
+def test_sparse_decode_edge_sets(si):
+    d, N = 256, 1024
+    c = Case(si, d, N, 0.7, 0.0, 0.4, 64, 8, 1)
+    x = synth.tokens(43, 0, synth.T_DECODE, 1, d)
+    for S in (np.zeros((1, 0), np.int32), np.array([[5]], np.int32), np.array([[c.layer.n_loaded - 1]], np.int32),
+              np.arange(c.layer.n_loaded, dtype=np.int32)[None, :]):
+        y = Guarded((1, d), torch().float32, fill=float("nan"))
+        si.si_sparse_ffn_decode(c.layer, dev(S), S.shape[1], 1, dev_bf16(x), y.t)
+        ref = oracle.sparse_ffn(c.Wg, c.Wu, c.Wd, c.loaded, S[0], x[0])
+        got = y.numpy()[0]
+        if S.shape[1] == 0:
+            assert np.all(got == 0)
+        else:
+            assert rel_err(got, ref) <= 2e-5
+    c.layer.close()
+
+
+def test_sparse_decode_deterministic_and_repeatable(si):
+    d, N = 2048, 8192
+    c = Case(si, d, N, 0.7, 0.2, 0.4, 1024, 16, 1)
+    x = dev_bf16(synth.tokens(44, 0, synth.T_DECODE, 1, d))
+    S = dev(c.S)
+    ys = []
+    for _ in range(5):
+        y = Guarded((1, d), torch().float32)
+        si.si_sparse_ffn_decode(c.layer, S, c.n_sel, 1, x, y.t)
+        ys.append(y.numpy())
+    for y in ys[1:]:
+        assert np.array_equal(y.view(np.uint32), ys[0].view(np.uint32))
+    c.layer.close()
+
+
+def test_decode_plan_required_for_batches(si):
+    c = Case(si, 256, 1024, 0.7, 0.2, 0.4, 64, 8, 2)
+    x = dev_bf16(synth.tokens(45, 0, synth.T_DECODE, 2, 256))
+    y = dev(np.zeros((2, 256), np.float32))
+    with pytest.raises(si.SIError) as e:
+        si.si_sparse_ffn_decode(c.layer, dev(c.S), c.n_sel, 2, x, y)
+    assert e.value.code == si.SI_ERR_INVALID_ARG
+    c.layer.close()

@@ -1,0 +1,118 @@
+"""GPU parity: SpAx encoding (bit-exact codes), tier choice (bit-exact lists),
+dense gate/up activations and the three-tier down-projection (within the FFN
+tolerance)."""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from gpu_util import TOL, Guarded, dev, dev_bf16, device_view, rel_err, torch
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def si():
+    import activation_sparse_gb300 as si
+    return si
+
+
+def encoded_buffers(layer):
+    p_wdt, p_codes, p_params = layer.buffers()
+    WdT = device_view(p_wdt, (layer.N, layer.d), "<i2").cpu().numpy().view(np.uint16)
+    codes = device_view(p_codes, (layer.N, layer.d // 2), "|u1").cpu().numpy()
+    params = device_view(p_params, (layer.N, layer.ngp, 2), "<f4").cpu().numpy()
+    return WdT, codes, params
+
+
+@pytest.fixture(scope="module")
+def llama8b_layer():
+    """One Llama-3.1-8B FFN layer (d=4096, d_ff=14336)."""
+    return synth.layer_weights(50, 0, 4096, 14336)
+
+
+@pytest.mark.parametrize("d,N,group", [(256, 64, 128), (4096, 14336, 128), (512, 300, 64), (128, 5, 8)])
+def test_spax_encode_bit_exact(si, d, N, group, llama8b_layer):
+    if (d, N) == (4096, 14336):
+        _, _, Wd = llama8b_layer
+    else:
+        _, _, Wd = synth.layer_weights(51, 0, d, N)
+    layer = si.spax_encode(dev_bf16(Wd), 4, group)
+    WdT, codes, params = encoded_buffers(layer)
+    rc, rp = oracle.spax_encode(Wd, 4, group)
+    assert np.array_equal(WdT, Wd.T)
+    assert np.array_equal(codes, rc)
+    ng = d // group
+    assert np.array_equal(params[:, :ng, :].view(np.uint32), rp.view(np.uint32))
+    assert not params[:, ng:, :].any()
+    layer.close()
+
+
+def signed_acts(seed, N, ties=False):
+    a = synth.normal(seed, 0, synth.T_SPAX_A, N).astype(np.float32)
+    if ties:
+        a = (np.round(a * 2) / 2).astype(np.float32)
+    return a
+
+
+@pytest.mark.parametrize("N,top,mid,ties", [(14336, 0.3, 0.3, False), (14336, 0.3, 0.3, True),
+                                            (1000, 0.0, 0.5, True), (1000, 0.5, 0.0, False),
+                                            (1000, 1.0, 0.0, False), (1000, 0.0, 1.0, True),
+                                            (1000, 0.0, 0.0, False), (77, 0.4, 0.6, True)])
+def test_spax_tiers_and_down(si, N, top, mid, ties):
+    d = 256 if N != 14336 else 4096
+    _, _, Wd = synth.layer_weights(52, 0, d, N)
+    layer = si.spax_encode(dev_bf16(Wd), 4, 128)
+    a = signed_acts(53, N, ties)
+    k_top, k_mid = si.si_count(top, N), si.si_count(mid, N)
+    ti = Guarded((max(k_top, 1),), torch().int32, fill=-1)
+    mi = Guarded((max(k_mid, 1),), torch().int32, fill=-1)
+    y = Guarded((d,), torch().float32, fill=float("nan"))
+    si.spax_tiered_down(layer, dev(a), top, mid, y.t, ti.t if k_top else None, mi.t if k_mid else None)
+    rt, rm = oracle.spax_tiers(a, k_top, k_mid)
+    if k_top:
+        assert np.array_equal(ti.numpy()[:k_top], rt)
+    if k_mid:
+        assert np.array_equal(mi.numpy()[:k_mid], rm)
+    codes, params = oracle.spax_encode(Wd, 4, 128)
+    ref = oracle.spax_down(a, Wd, codes, params, rt, rm)
+    got = y.numpy()
+    if k_top + k_mid == 0:
+        assert np.all(got == 0)
+    else:
+        assert rel_err(got, ref) <= 2e-5
+    layer.close()
+
+
+@pytest.mark.parametrize("d,N", [(4096, 14336), (256, 1000), (1088, 37)])
+def test_spax_dense_act(si, d, N, llama8b_layer):
+    if (d, N) == (4096, 14336):
+        Wg, Wu, _ = llama8b_layer
+    else:
+        Wg, Wu, _ = synth.layer_weights(54, 0, d, N)
+    x = synth.tokens(55, 0, synth.T_DECODE, 1, d)[0]
+    a = Guarded((N,), torch().float32, fill=float("nan"))
+    si.spax_dense_act(dev_bf16(Wg), dev_bf16(Wu), dev_bf16(x), a.t)
+    ref = oracle.dense_act(Wg, Wu, x)
+    assert rel_err(a.numpy(), ref) <= 1e-5
+
+
+def test_spax_ffn_decode_full_token(si, llama8b_layer):
+    """One Llama-3.1-8B layer token: dense gate/up, 30% bf16 / 30% 4-bit / 40% skipped."""
+    Wg, Wu, Wd = llama8b_layer
+    layer = si.spax_encode(dev_bf16(Wd), 4, 128)
+    codes, params = oracle.spax_encode(Wd, 4, 128)
+    N = 14336
+    k_top, k_mid = si.si_count(0.3, N), si.si_count(0.3, N)
+    Wg_d, Wu_d = dev_bf16(Wg), dev_bf16(Wu)
+    for tok in range(2):
+        x = synth.tokens(56, tok, synth.T_DECODE, 1, 4096)[0]
+        y = Guarded((4096,), torch().float32, fill=float("nan"))
+        a_out = Guarded((N,), torch().float32)
+        si.spax_ffn_decode(layer, Wg_d, Wu_d, dev_bf16(x), 0.3, 0.3, y.t, a_out.t)
+        a_ref = oracle.dense_act(Wg, Wu, x).astype(np.float32)
+        rt, rm = oracle.spax_tiers(a_ref, k_top, k_mid)
+        ref = oracle.spax_down(a_ref, Wd, codes, params, rt, rm)
+        assert rel_err(y.numpy(), ref) <= TOL
+        assert rel_err(a_out.numpy(), a_ref) <= 1e-5
+    layer.close()
