@@ -389,7 +389,7 @@ int si_select_dynamic(si_layer* L, const uint16_t* X, int T, int B, int alpha, d
 // ------------------------------------------------------------------ a7
 
 int si_decode_plan(si_layer* L, const int32_t* S, int n_sel, int B, void* stream) {
-    if (!L || !S) return fail(SI_ERR_INVALID_ARG, "NULL pointer");
+    if (!L || (!S && n_sel > 0)) return fail(SI_ERR_INVALID_ARG, "NULL pointer");
     if (B < 1 || B > 8) return fail(SI_ERR_INVALID_ARG, "need 1 <= B <= 8");
     if (n_sel < 0 || n_sel > L->n_loaded) return fail(SI_ERR_INVALID_ARG, "need 0 <= n_sel <= n_loaded");
     cudaStream_t st = (cudaStream_t)stream;
@@ -416,7 +416,7 @@ int si_decode_plan(si_layer* L, const int32_t* S, int n_sel, int B, void* stream
 
 int si_sparse_ffn_decode(si_layer* L, const int32_t* S, int n_sel, int B, const uint16_t* x, float* y,
                          void* stream) {
-    if (!L || !S || !x || !y) return fail(SI_ERR_INVALID_ARG, "NULL pointer");
+    if (!L || (!S && n_sel > 0) || !x || !y) return fail(SI_ERR_INVALID_ARG, "NULL pointer");
     if (B < 1 || B > 8) return fail(SI_ERR_INVALID_ARG, "need 1 <= B <= 8");
     if (n_sel < 0 || n_sel > L->n_loaded) return fail(SI_ERR_INVALID_ARG, "need 0 <= n_sel <= n_loaded");
     if (L->d > 4096) return fail(SI_ERR_UNSUPPORTED, "decode supports d <= 4096");

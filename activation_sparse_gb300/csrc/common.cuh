@@ -4,6 +4,7 @@
 #pragma once
 
 #include <cstdint>
+#include <mutex>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 
@@ -13,16 +14,15 @@ namespace si {
 
 constexpr int kWarp = 32;
 
-// Upper bound on any spin in a kernel (nanoseconds of %globaltimer). A correct
-// kernel never waits this long; when a wait runs out the kernel records
-// SI_DEVERR_WAIT_TIMEOUT in the device error word and goes on without blocking.
-constexpr unsigned long long kWaitLimitNs = 4000000000ull;
+// Upper bound on any spin in a kernel, in SM clock cycles (about 4 s at
+// 2 GHz). A correct kernel never waits this long; when a wait runs out the
+// kernel records SI_DEVERR_WAIT_TIMEOUT in the device error word and goes on
+// without blocking. clock64() is the SM's own monotonic cycle counter (the
+// global nanosecond timer can be stepped by the driver's time sync).
+constexpr long long kWaitLimitCycles = 8000000000ll;
+constexpr long long kDrainLimitCycles = 400000000ll;
 
-__device__ __forceinline__ unsigned long long global_ns() {
-    unsigned long long t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
+__device__ __forceinline__ long long cycles() { return clock64(); }
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -66,15 +66,22 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // Bounded wait for the phase with the given parity to complete. Returns false
 // when the limit runs out (recording SI_DEVERR_WAIT_TIMEOUT), or at once when
 // some wait has already run out, so a faulty launch ends within one limit.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned* err) {
+// Wait sites recorded with a timeout: kernel id in bits 8-15, barrier kind in
+// bits 16-19 (see si.h).
+enum : unsigned {
+    kSiteDecode = 1u << 8, kSiteDenseAct = 2u << 8, kSiteTiered = 3u << 8, kSiteGemm = 4u << 8,
+    kSiteFull = 1u << 16, kSiteEmpty = 2u << 16, kSiteFullB = 3u << 16, kSiteAccum = 4u << 16,
+};
+
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned* err, unsigned site = 0) {
     if (mbar_try_wait(bar, parity)) return true;
-    const unsigned long long t0 = global_ns();
+    const long long t0 = cycles();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((it & 255u) == 0) {
             if (*reinterpret_cast<volatile unsigned*>(err) & SI_DEVERR_WAIT_TIMEOUT) return false;
-            if (global_ns() - t0 > kWaitLimitNs) {
-                atomicOr(err, SI_DEVERR_WAIT_TIMEOUT);
+            if (cycles() - t0 > kWaitLimitCycles) {
+                atomicOr(err, SI_DEVERR_WAIT_TIMEOUT | site);
                 return false;
             }
         }
@@ -166,6 +173,40 @@ __device__ __forceinline__ uint32_t lanemask_lt() {
     uint32_t m;
     asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
     return m;
+}
+
+// ------------------------------------------------------------------ host
+
+// Lets `kernel` use all the dynamic shared memory the device offers (once per
+// kernel and device). Launches then only need their own size to fit, whatever
+// size an earlier launch of the same kernel used.
+template <class K>
+cudaError_t allow_max_smem(K kernel) {
+    static std::mutex mu;
+    static const void* done[64];
+    static int done_dev[64];
+    static int n_done = 0;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const void* fn = reinterpret_cast<const void*>(kernel);
+    std::lock_guard<std::mutex> lk(mu);
+    for (int i = 0; i < n_done; ++i)
+        if (done[i] == fn && done_dev[i] == dev) return cudaSuccess;
+    int optin = 0;
+    e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (e != cudaSuccess) return e;
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, fn);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, optin - (int)fa.sharedSizeBytes);
+    if (e != cudaSuccess) return e;
+    if (n_done < 64) {
+        done[n_done] = fn;
+        done_dev[n_done] = dev;
+        ++n_done;
+    }
+    return cudaSuccess;
 }
 
 }  // namespace si

@@ -131,7 +131,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_sparse_decode(SparseDecodePa
             const uint64_t pol = policy_evict_first();
             for (int i = 0; i < cnt; ++i) {
                 const int s = i % R;
-                if (i >= R) mbar_wait(&empty[s], (uint32_t)((i / R - 1) & 1), P.err);
+                if (i >= R) mbar_wait(&empty[s], (uint32_t)((i / R - 1) & 1), P.err, kSiteDecode | kSiteEmpty);
                 int p = P.pos[lo + i];
                 if (p < 0 || p >= P.n_records) {  // never read outside the packed buffer
                     atomicOr(P.err, SI_DEVERR_COUNT);
@@ -166,7 +166,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_sparse_decode(SparseDecodePa
             const int i = it * kConsWarps + warp;
             if (i < cnt) {
                 const int s = i % R;
-                mbar_wait(&full[s], (uint32_t)((i / R) & 1), P.err);
+                mbar_wait(&full[s], (uint32_t)((i / R) & 1), P.err, kSiteDecode | kSiteFull);
                 const uint4* st = reinterpret_cast<const uint4*>(ring + (size_t)s * L.stage);
                 float g[B], u[B];
 #pragma unroll
@@ -207,7 +207,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_sparse_decode(SparseDecodePa
             for (int w2 = 0; w2 < nb; ++w2) {
                 const int i2 = it * kConsWarps + w2;
                 const int s2 = i2 % R;
-                mbar_wait(&full[s2], (uint32_t)((i2 / R) & 1), P.err);
+                mbar_wait(&full[s2], (uint32_t)((i2 / R) & 1), P.err, kSiteDecode | kSiteFullB);
                 const uint4* dn = reinterpret_cast<const uint4*>(ring + (size_t)s2 * L.stage) + 2 * (d / 8);
                 float av[B];
 #pragma unroll
@@ -282,7 +282,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_dense_act(DenseActParams P) 
             const uint64_t pol = policy_evict_first();
             for (int i = 0; i < cnt; ++i) {
                 const int s = i % R;
-                if (i >= R) mbar_wait(&empty[s], (uint32_t)((i / R - 1) & 1), P.err);
+                if (i >= R) mbar_wait(&empty[s], (uint32_t)((i / R - 1) & 1), P.err, kSiteDenseAct | kSiteEmpty);
                 const size_t n = (size_t)(lo + i);
                 uint8_t* dst = ring + (size_t)s * L.stage;
                 mbar_arrive_expect_tx(&full[s], 2 * row_bytes);
@@ -301,7 +301,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_dense_act(DenseActParams P) 
         }
         for (int i = warp; i < cnt; i += kConsWarps) {
             const int s = i % R;
-            mbar_wait(&full[s], (uint32_t)((i / R) & 1), P.err);
+            mbar_wait(&full[s], (uint32_t)((i / R) & 1), P.err, kSiteDenseAct | kSiteFull);
             const uint4* st = reinterpret_cast<const uint4*>(ring + (size_t)s * L.stage);
             float g = 0.0f, u = 0.0f;
 #pragma unroll
@@ -361,7 +361,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_tiered_down(TieredDownParams
             const uint64_t pol = policy_evict_first();
             for (int i = 0; i < nrec; ++i) {
                 const int s = i % R;
-                if (i >= R) mbar_wait(&empty[s], (uint32_t)((i / R - 1) & 1), P.err);
+                if (i >= R) mbar_wait(&empty[s], (uint32_t)((i / R - 1) & 1), P.err, kSiteTiered | kSiteEmpty);
                 uint8_t* dst = ring + (size_t)s * L.stage;
                 int ci = i < ntop ? P.top[t0 + i] : P.mid[m0 + i - ntop];
                 if (ci < 0 || ci >= P.N) {  // never read outside the encoded buffers
@@ -389,7 +389,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_tiered_down(TieredDownParams
         const int tid = threadIdx.x;
         for (int i = 0; i < nrec; ++i) {
             const int s = i % R;
-            mbar_wait(&full[s], (uint32_t)((i / R) & 1), P.err);
+            mbar_wait(&full[s], (uint32_t)((i / R) & 1), P.err, kSiteTiered | kSiteFull);
             const uint8_t* st = ring + (size_t)s * L.stage;
             const float av = s_av[i];
             if (i < ntop) {
@@ -469,7 +469,7 @@ cudaError_t pick_grid(K kernel, size_t smem, int* grid, int* cluster) {
     if (e != cudaSuccess) return e;
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    e = allow_max_smem(kernel);
     if (e != cudaSuccess) return e;
     int best = 0, bestC = 2;
     for (int C = 8; C >= 2; C /= 2) {
@@ -490,8 +490,10 @@ cudaError_t pick_grid(K kernel, size_t smem, int* grid, int* cluster) {
             (void)cudaGetLastError();
             continue;
         }
-        if (ncl * C > best) {
-            best = ncl * C;
+        // one CTA per SM at most: the partial buffers are sized for that
+        const int ctas = ncl * C < (sms / C) * C ? ncl * C : (sms / C) * C;
+        if (ctas > best) {
+            best = ctas;
             bestC = C;
         }
     }
@@ -599,12 +601,10 @@ cudaError_t launch_dense_act(DenseActParams P, cudaStream_t st) {
     const size_t smem = (size_t)ring_layout(P.R, 4 * P.d, 0, P.d * 2).total;
     const int grid = P.N < sms ? P.N : sms;
     if (P.d > 2048) {
-        e = cudaFuncSetAttribute(k_dense_act<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
+        if ((e = allow_max_smem(k_dense_act<2>)) != cudaSuccess) return e;
         k_dense_act<2><<<grid, kDecThreads, smem, st>>>(P);
     } else {
-        e = cudaFuncSetAttribute(k_dense_act<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
+        if ((e = allow_max_smem(k_dense_act<1>)) != cudaSuccess) return e;
         k_dense_act<1><<<grid, kDecThreads, smem, st>>>(P);
     }
     return cudaGetLastError();

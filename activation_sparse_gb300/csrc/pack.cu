@@ -114,7 +114,7 @@ cudaError_t launch_pack_loaded(const uint16_t* Wg, const uint16_t* Wu, const uin
 cudaError_t launch_spax_encode(const uint16_t* Wd, int d, int N, int group, int ngp, uint16_t* WdT, uint8_t* codes,
                                float* params, cudaStream_t st) {
     const size_t smem = (size_t)group * 33 * 2;
-    cudaError_t e = cudaFuncSetAttribute(k_spax_encode, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = allow_max_smem(k_spax_encode);
     if (e != cudaSuccess) return e;
     dim3 grid((N + 31) / 32, d / group);
     k_spax_encode<<<grid, 256, smem, st>>>(Wd, d, N, group, ngp, WdT, codes, params);

@@ -343,7 +343,7 @@ __global__ void k_merge_scores(MergeArgs args, int N, float* __restrict__ out) {
 cudaError_t launch_topk_alpha(const float* absA, int ld, int n, int T, int B, int alpha, uint32_t* counts,
                               uint32_t* topmask, cudaStream_t st) {
     const size_t smem = (size_t)n * 4;
-    cudaError_t e = cudaFuncSetAttribute(k_topk_alpha, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = allow_max_smem(k_topk_alpha);
     if (e != cudaSuccess) return e;
     k_topk_alpha<<<B * T, kSelNT, smem, st>>>(absA, ld, n, T, alpha, counts, topmask, (n + 31) / 32);
     return cudaGetLastError();
@@ -352,7 +352,7 @@ cudaError_t launch_topk_alpha(const float* absA, int ld, int n, int T, int B, in
 cudaError_t launch_topk_beta(const uint32_t* counts, const uint8_t* is_static, int n, int B, int beta, int n_sel,
                              int32_t* S, unsigned* err, cudaStream_t st) {
     const size_t smem = (size_t)n * 5 + 16;
-    cudaError_t e = cudaFuncSetAttribute(k_topk_beta, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = allow_max_smem(k_topk_beta);
     if (e != cudaSuccess) return e;
     k_topk_beta<<<B, 1024, smem, st>>>(counts, is_static, n, beta, n_sel, S, err);
     return cudaGetLastError();
@@ -361,7 +361,7 @@ cudaError_t launch_topk_beta(const uint32_t* counts, const uint8_t* is_static, i
 cudaError_t launch_rank_loaded(const float* task, const float* model, int N, int n_base, int n_load,
                                int32_t* loaded, uint8_t* is_static, unsigned* err, cudaStream_t st) {
     const size_t smem = (size_t)N * 2 + 16;
-    cudaError_t e = cudaFuncSetAttribute(k_rank_loaded, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = allow_max_smem(k_rank_loaded);
     if (e != cudaSuccess) return e;
     k_rank_loaded<<<1, 1024, smem, st>>>(task, model, N, n_base, n_load, loaded, is_static, err);
     return cudaGetLastError();
@@ -370,7 +370,7 @@ cudaError_t launch_rank_loaded(const float* task, const float* model, int N, int
 cudaError_t launch_decode_plan(const int32_t* S, int n_sel, int B, int n, int32_t* pos, uint32_t* pmask,
                                int* count, unsigned* err, cudaStream_t st) {
     const size_t smem = (size_t)n * 4;
-    cudaError_t e = cudaFuncSetAttribute(k_decode_plan, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = allow_max_smem(k_decode_plan);
     if (e != cudaSuccess) return e;
     k_decode_plan<<<1, 1024, smem, st>>>(S, n_sel, B, n, pos, pmask, count, err);
     return cudaGetLastError();
@@ -379,7 +379,7 @@ cudaError_t launch_decode_plan(const int32_t* S, int n_sel, int B, int n, int32_
 cudaError_t launch_spax_tiers(const float* a, int N, int k_top, int k_mid, int32_t* top, int32_t* mid,
                               unsigned* err, cudaStream_t st) {
     const size_t smem = (size_t)N * 5 + 16;
-    cudaError_t e = cudaFuncSetAttribute(k_spax_tiers, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = allow_max_smem(k_spax_tiers);
     if (e != cudaSuccess) return e;
     k_spax_tiers<<<1, 1024, smem, st>>>(a, N, k_top, k_mid, top, mid, err);
     return cudaGetLastError();

@@ -86,8 +86,12 @@ long long si_packed_bytes(int d, int n_loaded);
 /* Reads (and with clear != 0 resets) the device error word of the current
  * device. *code (host) receives 0 when no kernel reported a failure, else a
  * bit set of SI_DEVERR_* values. Synchronises the device. */
-#define SI_DEVERR_WAIT_TIMEOUT 1u   /* a bounded mbarrier / TMEM wait ran out */
-#define SI_DEVERR_COUNT 2u          /* an internal count check failed */
+#define SI_DEVERR_WAIT_TIMEOUT 1u   /* a bounded mbarrier wait ran out */
+#define SI_DEVERR_COUNT 2u          /* an index or count check failed (bad S / tier list, count mismatch) */
+/* With SI_DEVERR_WAIT_TIMEOUT, bits 8-15 name the kernel whose wait ran out
+ * (1 sparse decode, 2 dense activation pass, 3 tiered down-projection,
+ * 4 activation GEMM) and bits 16-19 the barrier (1 stage full, 2 stage empty,
+ * 3 stage full in the down-projection phase, 4 accumulator ready). */
 int si_device_error(uint32_t *code, int clear);
 
 /* --------------------------------------------------- a1: profiler score */

@@ -66,7 +66,7 @@ TOL = 2e-2  # max relative error of FFN outputs (bf16 weights, fp32 accumulation
 
 class _CAI:
     def __init__(self, ptr, shape, typestr):
-        self.__cuda_array_interface__ = {"shape": tuple(shape), "typestr": typestr, "data": (int(ptr), True),
+        self.__cuda_array_interface__ = {"shape": tuple(shape), "typestr": typestr, "data": (int(ptr), False),
                                          "version": 2, "strides": None}
 
 

@@ -1,0 +1,88 @@
+"""GPU parity of the tcgen05 activation GEMM: the profiler score (Eq. 1) and
+the prefill activation matrix |A| of si_select_dynamic, plus the selection it
+drives. Full-size shapes are checked on sampled neurons / token rows that the
+oracle computes one by one."""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from gpu_util import Guarded, dev, dev_bf16, torch
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def si():
+    import activation_sparse_gb300 as si
+    return si
+
+
+PROFILE_CASES = [
+    # d, N, T (calibration tokens), neurons sampled for the oracle (None = all)
+    (256, 1024, 128, None),       # single-layer workload
+    (256, 1000, 100, None),       # ragged N and T
+    (128, 130, 1, None),          # one token, ragged tile
+    (2048, 8192, 4096, 96),       # Llama3.2-1B layer, 4096 calibration tokens
+    (3072, 8192, 512, 64),        # Llama3.2-3B width
+]
+
+
+@pytest.mark.parametrize("d,N,T,sample", PROFILE_CASES)
+def test_profile_scores(si, d, N, T, sample):
+    Wg, Wu, _ = synth.layer_weights(60, 0, d, N)
+    X = synth.tokens(60, 0, synth.T_CALIB, T, d)
+    scores = Guarded((N,), torch().float32, fill=0.0)
+    si.si_profile_scores(dev_bf16(Wg), dev_bf16(Wu), dev_bf16(X), scores.t)
+    got = scores.numpy().astype(np.float64)
+    idx = np.arange(N) if sample is None else np.sort(np.random.default_rng(0).choice(N, sample, replace=False))
+    ref = oracle.profile_scores(Wg[idx], Wu[idx], X)
+    rel = np.abs(got[idx] - ref) / np.maximum(ref, 1e-30)
+    assert rel.max() < 1e-3, rel.max()
+    # scores accumulate over calls
+    si.si_profile_scores(dev_bf16(Wg), dev_bf16(Wu), dev_bf16(X), scores.t)
+    got2 = scores.numpy().astype(np.float64)
+    assert np.allclose(got2, 2 * got, rtol=1e-5)
+
+
+SELECT_CASES = [
+    # d, N, gamma, delta, phi, alpha, T, B, sampled rows (None = all)
+    (256, 1024, 0.7, 0.2, 0.4, 64, 32, 1, None),          # single-layer workload
+    (2048, 8192, 0.7, 0.2, 0.4, 1024, 512, 1, 12),        # Llama3.2-1B prompt
+    (3072, 8192, 0.7, 0.25, 0.5, 1024, 1024, 1, 8),       # Llama3.2-3B prompt
+    (2048, 11008, 0.8, 0.25, 0.5, 1024, 256, 8, 8),       # Qwen2.5-3B, 8 prompts
+    (512, 700, 0.9, 0.3, 0.5, 40, 77, 2, None),           # ragged M and neurons
+]
+
+
+@pytest.mark.parametrize("d,N,gamma,delta,phi,alpha,T,B,sample", SELECT_CASES)
+def test_select_dynamic(si, d, N, gamma, delta, phi, alpha, T, B, sample):
+    Wg, Wu, Wd = synth.layer_weights(61, 0, d, N, 1.5 if B > 1 else 1.0)
+    s = synth.lognormal_absact(61, 1, N)[0]
+    layer = si.si_pack_loaded(dev_bf16(Wg), dev_bf16(Wu), dev_bf16(Wd), dev(s), dev(s), gamma, delta)
+    loaded, st = oracle.rank_loaded(s, s, gamma, delta)
+    X = synth.tokens(62, 0, synth.T_PROMPT, B * T, d)
+    n_sel = si.si_count(phi, N)
+    S = Guarded((B, n_sel), torch().int32, fill=-1)
+    A = Guarded((B * T, layer.n_pad), torch().float32, fill=float("nan"))
+    si.si_select_dynamic(layer, dev_bf16(X), T, B, alpha, phi, S.t, A.t)
+    got_A = A.numpy()
+    assert not got_A[:, layer.n_loaded:].any()                 # pad neurons give zero
+    rows = np.arange(B * T) if sample is None else np.sort(np.random.default_rng(1).choice(B * T, sample, False))
+    ref_A = oracle.absact(Wg, Wu, loaded, X[rows])
+    err = np.abs(got_A[rows, :layer.n_loaded] - ref_A)
+    assert err.max() <= 1e-3 * ref_A.max() + 1e-6, err.max() / ref_A.max()
+    got_S = S.numpy()
+    # the selection is the exact selection of the |A| the GPU computed
+    S2 = Guarded((B, n_sel), torch().int32, fill=-1)
+    si.si_select_from_absact(layer, A.t, T, B, alpha, phi, S2.t)
+    assert np.array_equal(got_S, S2.numpy())
+    # and agrees with the oracle's selection on its own |A| up to near-ties
+    if sample is None:
+        ref_S = oracle.select(oracle.absact(Wg, Wu, loaded, X).astype(np.float32), T, B, len(loaded), st, alpha, n_sel)
+        for b in range(B):
+            overlap = len(np.intersect1d(got_S[b], ref_S[b])) / n_sel
+            assert overlap >= 0.98, overlap
+    assert np.all(np.diff(got_S, axis=1) > 0)                  # ascending, distinct
+    assert np.all(st[got_S].sum(axis=1) == int(st.sum()))      # every static neuron kept
+    layer.close()
