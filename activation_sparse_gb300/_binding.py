@@ -32,6 +32,7 @@ SIGNATURES = {
     "si_layer_buffers": (_i, [_vp, C.POINTER(_vp), C.POINTER(_vp), C.POINTER(_vp)]),
     "si_layer_destroy": (_i, [_vp]),
     "si_select_dynamic": (_i, [_vp, _vp, _i, _i, _i, _d, _vp, _vp, _vp]),
+    "si_prefill_absact": (_i, [_vp, _vp, _i, _i, _vp, _vp]),
     "si_select_from_absact": (_i, [_vp, _vp, _i, _i, _i, _i, _d, _vp, _vp, _vp, _vp]),
     "si_decode_plan": (_i, [_vp, _vp, _i, _i, _vp]),
     "si_sparse_ffn_decode": (_i, [_vp, _vp, _i, _i, _vp, _vp, _vp]),
@@ -206,6 +207,12 @@ def si_select_dynamic(layer: Layer, X, T, B, alpha, phi, S, absact_out=None, str
                                     _ptr(S, torch.int32, "S"), _ptr(absact_out, torch.float32, "absact_out"),
                                     _stream(stream)))
     return S
+
+
+def si_prefill_absact(layer: Layer, X, T, B, absact_out, stream=None):
+    _check(load().si_prefill_absact(layer.handle, _bf16(X, "X"), int(T), int(B),
+                                    _ptr(absact_out, _torch().float32, "absact_out"), _stream(stream)))
+    return absact_out
 
 
 def si_select_from_absact(layer: Layer, absA, T, B, alpha, phi, S, topmask=None, counts=None, stream=None):

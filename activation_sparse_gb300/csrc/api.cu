@@ -341,6 +341,38 @@ int si_select_from_absact(si_layer* L, const float* absA, int ld, int T, int B, 
     return select_core(L, absA, ld, T, B, alpha, phi, S, topmask, counts, (cudaStream_t)stream);
 }
 
+namespace {
+
+int absact_core(si_layer* L, const uint16_t* X, int M, float* A, cudaStream_t st) {
+    unsigned* err = nullptr;
+    int rc = err_word(&err);
+    if (rc) return rc;
+    si::ActGemmParams P = {};
+    P.X = X;
+    P.M = M;
+    P.K = L->d;
+    P.Wgate = L->packed;
+    P.Wup = L->packed + L->d;
+    P.w_stride = 3LL * L->d;
+    P.Nrows = L->n_pad;
+    P.Nvalid = L->n_pad;
+    P.mode = 0;
+    P.out = A;
+    P.ldo = L->n_pad;
+    P.err = err;
+    SI_CK(si::launch_act_gemm(P, st));
+    return SI_OK;
+}
+
+}  // namespace
+
+int si_prefill_absact(si_layer* L, const uint16_t* X, int T, int B, float* absact_out, void* stream) {
+    if (!L || !X || !absact_out) return fail(SI_ERR_INVALID_ARG, "NULL pointer");
+    if (T < 1 || B < 1) return fail(SI_ERR_INVALID_ARG, "need T, B >= 1");
+    if ((long long)T * B > (1LL << 30) / L->n_pad) return fail(SI_ERR_INVALID_ARG, "T * B too large");
+    return absact_core(L, X, T * B, absact_out, (cudaStream_t)stream);
+}
+
 int si_select_dynamic(si_layer* L, const uint16_t* X, int T, int B, int alpha, double phi, int32_t* S,
                       float* absact_out, void* stream) {
     if (!L || !X || !S) return fail(SI_ERR_INVALID_ARG, "NULL pointer");
@@ -369,20 +401,8 @@ int si_select_dynamic(si_layer* L, const uint16_t* X, int T, int B, int alpha, d
         }
         A = L->absA;
     }
-    si::ActGemmParams P = {};
-    P.X = X;
-    P.M = M;
-    P.K = L->d;
-    P.Wgate = L->packed;
-    P.Wup = L->packed + L->d;
-    P.w_stride = 3LL * L->d;
-    P.Nrows = L->n_pad;
-    P.Nvalid = L->n_pad;
-    P.mode = 0;
-    P.out = A;
-    P.ldo = L->n_pad;
-    P.err = err;
-    SI_CK(si::launch_act_gemm(P, st));
+    rc = absact_core(L, X, M, A, st);
+    if (rc) return rc;
     return select_core(L, A, L->n_pad, T, B, alpha, phi, S, nullptr, nullptr, st);
 }
 
@@ -534,7 +554,7 @@ int spax_dense_act(const uint16_t* Wg, const uint16_t* Wu, int d, int N, const u
     P.a = a;
     P.err = err;
     P.R = si::dense_act_stages(d);
-    if (P.R < 2) return fail(SI_ERR_UNSUPPORTED, "d too large for the activation ring");
+    if (P.R < 8) return fail(SI_ERR_UNSUPPORTED, "d too large for the activation ring");
     SI_CK(si::launch_dense_act(P, (cudaStream_t)stream));
     return SI_OK;
 }

@@ -586,10 +586,16 @@ cudaError_t launch_sparse_decode(SparseDecodeParams P, int B, cudaStream_t st) {
     }
 }
 
+// The dense pass hands neuron i to warp i % 8 and stage i % R. R is kept a
+// multiple of the consumer-warp count so that every stage belongs to one warp:
+// a warp then always consumed the previous fill of a stage before it waits on
+// the next one, and a parity wait can never be two phases behind (which would
+// read as complete).
 int dense_act_stages(int d) {
     const int fixed = ring_layout(0, 4 * d, 0, d * 2).total;
     int R = (kSmemBudget - fixed - 256) / round_up(4 * d, 128);
-    return R > 32 ? 32 : R;
+    if (R > 32) R = 32;
+    return (R / kConsWarps) * kConsWarps;
 }
 
 cudaError_t launch_dense_act(DenseActParams P, cudaStream_t st) {

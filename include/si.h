@@ -164,6 +164,13 @@ int si_layer_destroy(si_layer *layer);
 int si_select_dynamic(si_layer *layer, const uint16_t *X, int T, int B, int alpha, double phi,
                       int32_t *S, float *absact_out, void *stream);
 
+/* Step a3 of si_select_dynamic alone: absact_out fp32 [B*T x n_pad] receives
+ * |A| for every token row and packed position (pad columns zero), computed on
+ * the tcgen05 tensor cores exactly as si_select_dynamic does. Together with
+ * si_select_from_absact(layer, absact_out, n_pad, ...) it gives the same S. */
+int si_prefill_absact(si_layer *layer, const uint16_t *X, int T, int B, float *absact_out,
+                      void *stream);
+
 /* Steps a4..a6 of si_select_dynamic on a given |A| matrix (fp32 [B*T x ld],
  * ld >= n_loaded, finite; only the first n_loaded columns are read, and they
  * are ranked by magnitude). Optional outputs (may be NULL): topmask

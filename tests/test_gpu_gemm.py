@@ -86,3 +86,22 @@ def test_select_dynamic(si, d, N, gamma, delta, phi, alpha, T, B, sample):
     assert np.all(np.diff(got_S, axis=1) > 0)                  # ascending, distinct
     assert np.all(st[got_S].sum(axis=1) == int(st.sum()))      # every static neuron kept
     layer.close()
+
+
+def test_prefill_absact_matches_select_dynamic(si):
+    d, N, T, B = 2048, 8192, 512, 1
+    Wg, Wu, Wd = synth.layer_weights(63, 0, d, N)
+    s = synth.lognormal_absact(63, 1, N)[0]
+    layer = si.si_pack_loaded(dev_bf16(Wg), dev_bf16(Wu), dev_bf16(Wd), dev(s), dev(s), 0.7, 0.2)
+    X = dev_bf16(synth.tokens(64, 0, synth.T_PROMPT, T, d))
+    A1 = Guarded((T, layer.n_pad), torch().float32, fill=float("nan"))
+    A2 = Guarded((T, layer.n_pad), torch().float32, fill=float("nan"))
+    n_sel = si.si_count(0.4, N)
+    S1 = Guarded((1, n_sel), torch().int32)
+    S2 = Guarded((1, n_sel), torch().int32)
+    si.si_prefill_absact(layer, X, T, B, A1.t)
+    si.si_select_from_absact(layer, A1.t, T, B, 1024, 0.4, S1.t)
+    si.si_select_dynamic(layer, X, T, B, 1024, 0.4, S2.t, A2.t)
+    assert np.array_equal(A1.numpy().view(np.uint32), A2.numpy().view(np.uint32))
+    assert np.array_equal(S1.numpy(), S2.numpy())
+    layer.close()

@@ -116,3 +116,19 @@ def test_spax_ffn_decode_full_token(si, llama8b_layer):
         assert rel_err(y.numpy(), ref) <= TOL
         assert rel_err(a_out.numpy(), a_ref) <= 1e-5
     layer.close()
+
+
+def test_spax_dense_act_repeated_calls(si, llama8b_layer):
+    """Many back-to-back dense passes at full size: every stage of the ring
+    belongs to one consumer warp, so no wait can alias a stale phase (the
+    autouse check then finds the device error word clean)."""
+    Wg, Wu, _ = llama8b_layer
+    gWg, gWu = dev_bf16(Wg), dev_bf16(Wu)
+    x = synth.tokens(57, 0, synth.T_DECODE, 1, 4096)[0]
+    ref = oracle.dense_act(Wg, Wu, x)
+    a = Guarded((14336,), torch().float32)
+    xd = dev_bf16(x)
+    for _ in range(40):
+        si.spax_dense_act(gWg, gWu, xd, a.t)
+    assert rel_err(a.numpy(), ref) <= 1e-5
+    assert si.si_device_error() == 0
