@@ -13,7 +13,7 @@ import os
 from . import _build
 
 SI_OK, SI_ERR_INVALID_ARG, SI_ERR_CUDA, SI_ERR_OOM, SI_ERR_UNSUPPORTED, SI_ERR_DEVICE = range(6)
-SI_DEVERR_WAIT_TIMEOUT, SI_DEVERR_COUNT = 1, 2
+SI_DEVERR_WAIT_TIMEOUT, SI_DEVERR_COUNT, SI_DEVERR_RANGE = 1, 2, 4
 
 # every symbol include/si.h declares, with (restype, argtypes)
 _vp, _i, _d, _ll, _u32p = C.c_void_p, C.c_int, C.c_double, C.c_longlong, C.POINTER(C.c_uint32)
@@ -36,6 +36,7 @@ SIGNATURES = {
     "si_select_from_absact": (_i, [_vp, _vp, _i, _i, _i, _i, _d, _vp, _vp, _vp, _vp]),
     "si_decode_plan": (_i, [_vp, _vp, _i, _i, _vp]),
     "si_sparse_ffn_decode": (_i, [_vp, _vp, _i, _i, _vp, _vp, _vp]),
+    "si_sparse_ffn_decode_residual": (_i, [_vp, _vp, _i, _i, _vp, _vp, _vp]),
     "spax_encode": (_i, [_vp, _i, _i, _i, _i, C.POINTER(_vp), _vp]),
     "spax_layer_info": (_i, [_vp, _ip, _ip, _ip, _ip, _ip]),
     "spax_layer_buffers": (_i, [_vp, C.POINTER(_vp), C.POINTER(_vp), C.POINTER(_vp)]),
@@ -233,6 +234,13 @@ def si_sparse_ffn_decode(layer: Layer, S, n_sel, B, x, y, stream=None):
     torch = _torch()
     _check(load().si_sparse_ffn_decode(layer.handle, _ptr(S, torch.int32, "S"), int(n_sel), int(B), _bf16(x, "x"),
                                        _ptr(y, torch.float32, "y"), _stream(stream)))
+    return y
+
+
+def si_sparse_ffn_decode_residual(layer: Layer, S, n_sel, B, x, y, stream=None):
+    torch = _torch()
+    _check(load().si_sparse_ffn_decode_residual(layer.handle, _ptr(S, torch.int32, "S"), int(n_sel), int(B),
+                                                _bf16(x, "x"), _ptr(y, torch.float32, "y"), _stream(stream)))
     return y
 
 

@@ -96,11 +96,19 @@ struct si_layer {
     float* part = nullptr;
     long long part_floats = 0;
     unsigned* tickets = nullptr;
+    unsigned long long* acc = nullptr;  // batch-1 decode accumulator [d] (+ its ticket in tickets[15])
     int32_t* plan_pos = nullptr;
     uint32_t* plan_mask = nullptr;
     int* plan_n = nullptr;
+    uint16_t* plan_Wp = nullptr;  // batch-1 plan: row-major down weights of the selected records [d][np]
+    float* plan_a = nullptr;      // batch-1 plan: activations of the selected records [np]
+    int plan_np = 0;
     const int32_t* plan_S = nullptr;
     int plan_nsel = -1, plan_B = 0;
+    // True from si_decode_plan until the next decode launch on this handle: that
+    // launch may directly follow the plan kernel, so it reads the plan only after
+    // its dependency wait; later launches are ordered after it and may stream early.
+    bool plan_fresh = false;
 };
 
 struct spax_layer {
@@ -140,9 +148,12 @@ void destroy_layer(si_layer* L) {
     dfree(L->absA);
     dfree(L->part);
     dfree(L->tickets);
+    dfree(L->acc);
     dfree(L->plan_pos);
     dfree(L->plan_mask);
     dfree(L->plan_n);
+    dfree(L->plan_Wp);
+    dfree(L->plan_a);
     delete L;
 }
 
@@ -287,11 +298,13 @@ int si_pack_loaded(const uint16_t* Wg, const uint16_t* Wu, const uint16_t* Wd, i
     L->n_pad = round_up(n_loaded, 128);
     if ((rc = dalloc(&L->loaded, n_loaded, "loaded index")) || (rc = dalloc(&L->is_static, n_loaded, "static flags")) ||
         (rc = dalloc(&L->packed, (size_t)L->n_pad * 3 * d, "packed weights")) ||
-        (rc = dalloc(&L->tickets, 16, "tickets")) || (rc = grow_part(&L->part, &L->part_floats, d, 1))) {
+        (rc = dalloc(&L->tickets, 16, "tickets")) || (rc = dalloc(&L->acc, d, "decode accumulator")) ||
+        (rc = grow_part(&L->part, &L->part_floats, d, 1))) {
         destroy_layer(L);
         return rc;
     }
     cudaError_t e = cudaMemsetAsync(L->tickets, 0, 16 * sizeof(unsigned), st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(L->acc, 0, (size_t)d * sizeof(unsigned long long), st);
     if (e == cudaSuccess) e = si::launch_rank_loaded(task_scores, model_scores, N, n_static, n_loaded, L->loaded,
                                                      L->is_static, err, st);
     if (e == cudaSuccess) e = si::launch_pack_loaded(Wg, Wu, Wd, d, N, L->loaded, n_loaded, L->n_pad, L->packed, st);
@@ -427,15 +440,52 @@ int si_decode_plan(si_layer* L, const int32_t* S, int n_sel, int B, void* stream
         rc = grow_part(&L->part, &L->part_floats, L->d, B);
         if (rc) return rc;
     }
-    SI_CK(si::launch_decode_plan(S, n_sel, B, L->n_loaded, L->plan_pos, L->plan_mask, L->plan_n, err, st));
+    if (B == 1) {
+        // batch 1: the plan is S itself plus a row-major copy of the selected
+        // down columns, so decode needs no cross-CTA sum (see si_sparse_ffn_decode)
+        const int np_cap = round_up(L->n_loaded, 8);
+        if (!L->plan_Wp) {
+            if (capturing(st)) return fail(SI_ERR_INVALID_ARG, "plan buffers must be allocated before capture");
+            if ((rc = dalloc(&L->plan_Wp, (size_t)L->d * np_cap, "plan down rows")) ||
+                (rc = dalloc(&L->plan_a, (size_t)np_cap, "plan activations")))
+                return rc;
+        }
+        const int np = round_up(n_sel > 0 ? n_sel : 1, 8);
+        if (n_sel > 0) SI_CK(cudaMemcpyAsync(L->plan_pos, S, (size_t)n_sel * 4, cudaMemcpyDeviceToDevice, st));
+        SI_CK(cudaMemsetAsync(L->plan_a, 0, (size_t)np * sizeof(float), st));
+        SI_CK(si::launch_repack_down(L->packed, L->d, L->plan_pos, n_sel, np, L->plan_Wp, st));
+        L->plan_np = np;
+    } else {
+        SI_CK(si::launch_decode_plan(S, n_sel, B, L->n_loaded, L->plan_pos, L->plan_mask, L->plan_n, err, st));
+    }
+    L->plan_fresh = true;
     L->plan_S = S;
     L->plan_nsel = n_sel;
     L->plan_B = B;
     return SI_OK;
 }
 
+namespace {
+int sparse_decode_impl(si_layer* L, const int32_t* S, int n_sel, int B, const uint16_t* x, float* y,
+                       void* stream, bool accumulate);
+}
+
 int si_sparse_ffn_decode(si_layer* L, const int32_t* S, int n_sel, int B, const uint16_t* x, float* y,
                          void* stream) {
+    return sparse_decode_impl(L, S, n_sel, B, x, y, stream, false);
+}
+
+int si_sparse_ffn_decode_residual(si_layer* L, const int32_t* S, int n_sel, int B, const uint16_t* x, float* y,
+                                  void* stream) {
+    if (B != 1) return fail(SI_ERR_UNSUPPORTED, "the residual form is implemented for B == 1");
+    return sparse_decode_impl(L, S, n_sel, B, x, y, stream, true);
+}
+
+}  // extern "C"
+
+namespace {
+int sparse_decode_impl(si_layer* L, const int32_t* S, int n_sel, int B, const uint16_t* x, float* y,
+                       void* stream, bool accumulate) {
     if (!L || (!S && n_sel > 0) || !x || !y) return fail(SI_ERR_INVALID_ARG, "NULL pointer");
     if (B < 1 || B > 8) return fail(SI_ERR_INVALID_ARG, "need 1 <= B <= 8");
     if (n_sel < 0 || n_sel > L->n_loaded) return fail(SI_ERR_INVALID_ARG, "need 0 <= n_sel <= n_loaded");
@@ -454,23 +504,63 @@ int si_sparse_ffn_decode(si_layer* L, const int32_t* S, int n_sel, int B, const 
     P.part = L->part;
     P.part_floats = L->part_floats;
     P.tickets = L->tickets;
+    P.acc = L->acc;
+    P.acc_ticket = L->tickets + 15;
+    P.accumulate = accumulate ? 1 : 0;
     P.err = err;
     P.R = si::sparse_decode_stages(L->d, B);
     if (P.R < 8) return fail(SI_ERR_UNSUPPORTED, "d too large for the decode ring");
+    const bool have_plan = L->plan_S == S && L->plan_nsel == n_sel && L->plan_B == B;
+    const bool stable = have_plan && !L->plan_fresh;
+    P.stable_plan = stable ? 1 : 0;
+    if (B == 1 && have_plan && !accumulate) {
+        // planned batch 1: gate/up pass over the plan's records writes a, then
+        // each CTA of the down pass owns output rows of the row-major plan copy
+        si::PlanActParams A = {};
+        A.packed = L->packed;
+        A.n_records = L->n_pad;
+        A.d = L->d;
+        A.pos = L->plan_pos;
+        A.n = n_sel;
+        A.x = x;
+        A.a = L->plan_a;
+        A.err = err;
+        A.R = si::plan_act_stages(L->d);
+        A.stable_plan = P.stable_plan;
+        si::PlanDownParams D = {};
+        D.Wp = L->plan_Wp;
+        D.np = L->plan_np;
+        D.d = L->d;
+        D.rows = si::plan_down_rows(L->d, L->plan_np);
+        D.a = L->plan_a;
+        D.y = y;
+        D.err = err;
+        D.stable_plan = P.stable_plan;
+        SI_CK(si::launch_plan_act(A, (cudaStream_t)stream));
+        SI_CK(si::launch_plan_down(D, (cudaStream_t)stream));
+        L->plan_fresh = false;
+        return SI_OK;
+    }
     if (B == 1) {
-        P.pos = S;
+        // a batch-1 plan is a copy of S (n_sel entries); the count is the host's
+        P.pos = stable ? L->plan_pos : S;
         P.pmask = nullptr;
         P.n_dev = nullptr;
         P.n_host = n_sel;
     } else {
         P.pos = L->plan_pos;
-        P.pmask = L->plan_mask;
+        P.pmask = B > 1 ? L->plan_mask : nullptr;
         P.n_dev = L->plan_n;
-        P.n_host = 0;
+        P.n_host = n_sel;
     }
     SI_CK(si::launch_sparse_decode(P, B, (cudaStream_t)stream));
+    if (have_plan) L->plan_fresh = false;
     return SI_OK;
 }
+
+}  // namespace
+
+extern "C" {
 
 // ------------------------------------------------------------------ SpAx
 

@@ -117,6 +117,23 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
     return p;
 }
 
+// L2 prefetch of a global range (a hint: no data dependency, no completion).
+__device__ __forceinline__ void prefetch_l2(const void* src_gmem, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src_gmem), "r"(bytes) : "memory");
+}
+
+// ------------------------------------------------ programmatic dependent launch
+
+// Blocks until the grids this launch depends on have completed and their
+// memory is visible (a no-op when the launch has no programmatic dependency).
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Lets the next launch in the stream (if it was launched with programmatic
+// stream serialization) start scheduling its CTAs before this grid finishes.
+__device__ __forceinline__ void grid_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // -------------------------------------------------------------- named barrier
 
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {

@@ -22,6 +22,39 @@ struct SparseDecodeParams {
     unsigned* tickets;        // [16], zero between launches
     unsigned* err;            // device error word
     int R;                    // ring stages
+    int stable_plan;          // pos / n_dev come from a completed decode plan: records may be
+                              // streamed before this grid's dependency wait
+    unsigned long long* acc;  // [B*d] fixed-point accumulator, zero between launches
+    unsigned* acc_ticket;     // zero between launches
+    int accumulate;           // 1: y += result with float atomics (no cross-CTA ordering)
+};
+
+// Planned batch-1 decode, split in two kernels that need no cross-CTA sum:
+// plan_act computes a[i] for the plan's records (gate/up rows), plan_down
+// computes each output row from the plan's row-major down matrix.
+struct PlanActParams {
+    const uint16_t* packed;   // [n_pad][3][d] bf16 records
+    int n_records;
+    int d;
+    const int32_t* pos;       // plan positions [n]
+    int n;
+    const uint16_t* x;        // [d]
+    float* a;                 // [n] out
+    unsigned* err;
+    int R;
+    int stable_plan;
+};
+
+struct PlanDownParams {
+    const uint16_t* Wp;       // [d][np] bf16, row j = down weights of the plan's records
+    int np;                   // row length (plan count rounded up to 8; pad weights are zero)
+    int d;
+    int rows;                 // rows per CTA
+    const float* a;           // [np] (pad entries zero)
+    float* y;                 // [d]
+    unsigned* err;
+    int stable_plan;
+    int accumulate;           // 1: y += result (each row has one writer, so still deterministic)
 };
 
 struct DenseActParams {
@@ -73,6 +106,12 @@ cudaError_t launch_spax_encode(const uint16_t* Wd, int d, int N, int group, int 
                                float* params, cudaStream_t st);
 
 // decode.cu
+cudaError_t launch_repack_down(const uint16_t* packed, int d, const int32_t* pos, int n, int np, uint16_t* Wp,
+                               cudaStream_t st);
+int plan_act_stages(int d);
+cudaError_t launch_plan_act(PlanActParams P, cudaStream_t st);
+int plan_down_rows(int d, int np);
+cudaError_t launch_plan_down(PlanDownParams P, cudaStream_t st);
 int sparse_decode_stages(int d, int B);
 int decode_max_partial_floats(int d, int B);
 cudaError_t launch_sparse_decode(SparseDecodeParams P, int B, cudaStream_t st);

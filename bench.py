@@ -8,7 +8,8 @@ T=512 tokens and 256 decode tokens at batch 1, on synthetic seeded data.
 One step = one request through the online path:
   prefill  for every layer: |A| on the tensor cores (si_prefill_absact),
            per-token top-alpha + counts + top-beta union (si_select_from_absact);
-  decode   256 tokens x 16 layers of si_sparse_ffn_decode on the selected set.
+  decode   256 tokens x 16 layers of si_sparse_ffn_decode_residual (y += FFN(x))
+           on the selected set, with the decode plan built after prefill.
 Both halves are CUDA graphs replayed on one stream; CUDA events bracket each.
 The offline steps (profiler scores over 4096 calibration tokens, selective
 loading) run once before the timed region and are reported on their own; the
@@ -221,7 +222,7 @@ def run_gpu(args, world, rank, local):
     xdec = gpu_tokens(torch, seed, 300, w.decode_tokens * w.L, w.d, dev).view(w.decode_tokens, w.L, w.d)
     A = torch.empty((M, n_pad), dtype=torch.float32, device=dev)
     S = [torch.empty((w.B, n_sel), dtype=torch.int32, device=dev) for _ in range(w.L)]
-    y = torch.empty((w.decode_tokens, w.L, w.d), dtype=torch.float32, device=dev)
+    y = torch.zeros((w.decode_tokens, w.L, w.d), dtype=torch.float32, device=dev)
 
     stream = torch.cuda.Stream(device=dev)
 
@@ -233,15 +234,18 @@ def run_gpu(args, world, rank, local):
         for l in range(w.L):
             si.si_prefill_absact(layers[l], X[l], w.T, w.B, A)
             si.si_select_from_absact(layers[l], A, w.T, w.B, w.alpha, w.phi, S[l])
+            si.si_decode_plan(layers[l], S[l], n_sel, w.B)
 
+    # decode in the residual form (y += FFN(x)), the way a transformer adds the
+    # FFN output to its residual stream; y holds one residual row per (token, layer)
     def decode():
         for t in range(w.decode_tokens):
             for l in range(w.L):
-                si.si_sparse_ffn_decode(layers[l], S[l], n_sel, w.B, xdec[t, l], y[t, l])
+                si.si_sparse_ffn_decode_residual(layers[l], S[l], n_sel, w.B, xdec[t, l], y[t, l])
 
     def decode_one_pass():
         for l in range(w.L):
-            si.si_sparse_ffn_decode(layers[l], S[l], n_sel, w.B, xdec[0, l], y[0, l])
+            si.si_sparse_ffn_decode_residual(layers[l], S[l], n_sel, w.B, xdec[0, l], y[0, l])
 
     with torch.cuda.stream(stream):
         prefill()
@@ -263,7 +267,7 @@ def run_gpu(args, world, rank, local):
         g_gemm.replay()
     stream.synchronize()
 
-    launches_per_step = w.L * 3 + w.decode_tokens * w.L   # gemm, top-alpha, top-beta per layer; decode
+    launches_per_step = w.L * 4 + w.decode_tokens * w.L   # gemm, top-alpha, top-beta, plan per layer; decode
     pre_ms, dec_ms = [], []
     barrier(world)
     torch.cuda.synchronize()
@@ -373,10 +377,12 @@ def run_e2e(si, torch, dev, stream, layers, S, n_sel, args):
         for l in range(w.L):
             si.si_prefill_absact(layers[l], dX[l], w.T, w.B, A)
             si.si_select_from_absact(layers[l], A, w.T, w.B, w.alpha, w.phi, S[l])
+            si.si_decode_plan(layers[l], S[l], n_sel, w.B)
             hS[l].copy_(S[l], non_blocking=True)
+        dy.zero_()
         for t in range(w.decode_tokens):
             for l in range(w.L):
-                si.si_sparse_ffn_decode(layers[l], S[l], n_sel, w.B, dx[t, l], dy[t, l])
+                si.si_sparse_ffn_decode_residual(layers[l], S[l], n_sel, w.B, dx[t, l], dy[t, l])
         hy.copy_(dy, non_blocking=True)
 
     with torch.cuda.stream(stream):

@@ -88,6 +88,7 @@ long long si_packed_bytes(int d, int n_loaded);
  * bit set of SI_DEVERR_* values. Synchronises the device. */
 #define SI_DEVERR_WAIT_TIMEOUT 1u   /* a bounded mbarrier wait ran out */
 #define SI_DEVERR_COUNT 2u          /* an index or count check failed (bad S / tier list, count mismatch) */
+#define SI_DEVERR_RANGE 4u          /* a decode partial exceeded the fixed-point accumulator's range (|y| >= 2^23) */
 /* With SI_DEVERR_WAIT_TIMEOUT, bits 8-15 name the kernel whose wait ran out
  * (1 sparse decode, 2 dense activation pass, 3 tiered down-projection,
  * 4 activation GEMM) and bits 16-19 the barrier (1 stage full, 2 stage empty,
@@ -182,11 +183,16 @@ int si_select_from_absact(si_layer *layer, const float *absA, int ld, int T, int
 
 /* --------------------------------------------------- a7: sparse decode */
 
-/* Builds, inside the handle, the decode plan for B > 1 sequences that each
- * have their own computed set: the union of the B lists S[b][0..n_sel) with,
- * per union entry, a bit mask of the sequences that selected it, so decode
- * reads each selected neuron once. S must stay unchanged while the plan is
- * used. Not needed for B == 1. Requires 1 <= B <= 8. */
+/* Builds, inside the handle, the decode plan for the computed sets S[b]
+ * (b < B): the union of the B ascending lists S[b][0..n_sel) with, per union
+ * entry, a bit mask of the sequences that selected it, so decode reads each
+ * selected neuron once. Required before decoding with B > 1; optional for
+ * B == 1, where it lets decode start streaming the selected weights while the
+ * previous kernel on the stream is still finishing (from the second decode
+ * call after the plan on; the first one follows the plan kernel and waits for
+ * it). S must stay unchanged while the plan is used; calling si_decode_plan
+ * again replaces it. Plan and decode calls of a handle go on one stream.
+ * Requires 1 <= B <= 8. */
 int si_decode_plan(si_layer *layer, const int32_t *S, int n_sel, int B, void *stream);
 
 /* Sparse decode FFN on the computed set, [SI] section 5 (only the selected
@@ -202,6 +208,18 @@ int si_decode_plan(si_layer *layer, const int32_t *S, int n_sel, int B, void *st
  * the same S pointer, n_sel and B. No allocation: safe to capture. */
 int si_sparse_ffn_decode(si_layer *layer, const int32_t *S, int n_sel, int B,
                          const uint16_t *x, float *y, void *stream);
+
+/* Residual form of si_sparse_ffn_decode for one sequence (B == 1):
+ * y += sum over p in S of a_{loaded[p]}(x) * Wd[:, loaded[p]], the way a
+ * transformer adds the FFN output to its residual stream. The CTAs add their
+ * partial sums into y with float atomics as they finish, so there is no
+ * cross-CTA pass at the end of the kernel; the order of those additions is
+ * not fixed, so repeated calls can differ in the last bits (within fp32
+ * rounding of the si_sparse_ffn_decode result). A plan built with
+ * si_decode_plan lets a call stream its weights while the previous kernel on
+ * the stream finishes. y fp32 [d] (read and written). */
+int si_sparse_ffn_decode_residual(si_layer *layer, const int32_t *S, int n_sel, int B,
+                                  const uint16_t *x, float *y, void *stream);
 
 /* ------------------------------------------------------------- SpAx */
 

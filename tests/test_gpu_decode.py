@@ -49,7 +49,11 @@ def test_sparse_decode_parity(si, d, N, gamma, delta, phi, alpha, T, B, sigma):
     S_dev = dev(c.S)
     if B > 1:
         si.si_decode_plan(c.layer, S_dev, c.n_sel, B)
-    for tok in range(2):
+    # batch 1: two calls without a plan (fused kernel), then three with one
+    # (gate/up pass + row-split down pass; the first waits for the plan)
+    for tok in range(2 if B > 1 else 5):
+        if B == 1 and tok == 2:
+            si.si_decode_plan(c.layer, S_dev, c.n_sel, 1)
         x = synth.tokens(41, tok, synth.T_DECODE, B, d)
         y = Guarded((B, d), torch().float32, fill=float("nan"))
         si.si_sparse_ffn_decode(c.layer, S_dev, c.n_sel, B, dev_bf16(x), y.t)
@@ -96,11 +100,14 @@ def test_sparse_decode_edge_sets(si):
     c.layer.close()
 
 
-def test_sparse_decode_deterministic_and_repeatable(si):
+@pytest.mark.parametrize("planned", [False, True])
+def test_sparse_decode_deterministic_and_repeatable(si, planned):
     d, N = 2048, 8192
     c = Case(si, d, N, 0.7, 0.2, 0.4, 1024, 16, 1)
     x = dev_bf16(synth.tokens(44, 0, synth.T_DECODE, 1, d))
     S = dev(c.S)
+    if planned:
+        si.si_decode_plan(c.layer, S, c.n_sel, 1)
     ys = []
     for _ in range(5):
         y = Guarded((1, d), torch().float32)
@@ -108,6 +115,8 @@ def test_sparse_decode_deterministic_and_repeatable(si):
         ys.append(y.numpy())
     for y in ys[1:]:
         assert np.array_equal(y.view(np.uint32), ys[0].view(np.uint32))
+    ref = oracle.sparse_ffn(c.Wg, c.Wu, c.Wd, c.loaded, c.S[0], synth.tokens(44, 0, synth.T_DECODE, 1, d)[0])
+    assert rel_err(ys[0][0], ref) <= 2e-5
     c.layer.close()
 
 
@@ -118,4 +127,57 @@ def test_decode_plan_required_for_batches(si):
     with pytest.raises(si.SIError) as e:
         si.si_sparse_ffn_decode(c.layer, dev(c.S), c.n_sel, 2, x, y)
     assert e.value.code == si.SI_ERR_INVALID_ARG
+    c.layer.close()
+
+
+def test_planned_b1_decode_pipelined_back_to_back(si):
+    """Batch-1 decode with a plan: from the second call on, a launch streams its
+    records while the previous launch is still finishing (programmatic
+    dependent launch). Alternate two layers without host syncs and check every
+    output against the oracle."""
+    d, N = 2048, 8192
+    cases = [Case(si, d, N, 0.7, 0.2, 0.4, 1024, 16, 1, seed=s) for s in (70, 71)]
+    S_dev = [dev(c.S) for c in cases]
+    for c, S in zip(cases, S_dev):
+        si.si_decode_plan(c.layer, S, c.n_sel, 1)
+    toks = 6
+    xs = [synth.tokens(72, t, synth.T_DECODE, 1, d) for t in range(toks)]
+    xd = [dev_bf16(x) for x in xs]
+    ys = [[Guarded((1, d), torch().float32, fill=float("nan")) for _ in range(toks)] for _ in cases]
+    for t in range(toks):
+        for k, c in enumerate(cases):
+            si.si_sparse_ffn_decode(c.layer, S_dev[k], c.n_sel, 1, xd[t], ys[k][t].t)
+    torch().cuda.synchronize()
+    for k, c in enumerate(cases):
+        for t in range(toks):
+            ref = oracle.sparse_ffn(c.Wg, c.Wu, c.Wd, c.loaded, c.S[0], xs[t][0])
+            assert rel_err(ys[k][t].numpy()[0], ref) <= 2e-5, (k, t)
+    # the unplanned path agrees within fp32 summation-order noise
+    y_plain = Guarded((1, d), torch().float32)
+    c2 = Case(si, d, N, 0.7, 0.2, 0.4, 1024, 16, 1, seed=70)
+    si.si_sparse_ffn_decode(c2.layer, dev(c2.S), c2.n_sel, 1, xd[toks - 1], y_plain.t)
+    assert rel_err(y_plain.numpy()[0], ys[0][toks - 1].numpy()[0]) <= 1e-5
+    for c in cases + [c2]:
+        c.layer.close()
+
+
+@pytest.mark.parametrize("planned", [False, True])
+def test_residual_decode_accumulates(si, planned):
+    """y += FFN(x): the residual form adds the sparse FFN output to y."""
+    d, N = 2048, 8192
+    c = Case(si, d, N, 0.7, 0.2, 0.4, 1024, 16, 1, seed=75)
+    S = dev(c.S)
+    if planned:
+        si.si_decode_plan(c.layer, S, c.n_sel, 1)
+    base = synth.normal(76, 0, synth.T_MISC, d).astype(np.float32)
+    y = Guarded((1, d), torch().float32)
+    y.t.copy_(torch().from_numpy(base[None, :]))
+    xs = [synth.tokens(77, t, synth.T_DECODE, 1, d) for t in range(3)]
+    ref = base.astype(np.float64)
+    for x in xs:
+        si.si_sparse_ffn_decode_residual(c.layer, S, c.n_sel, 1, dev_bf16(x), y.t)
+        ref = ref + oracle.sparse_ffn(c.Wg, c.Wu, c.Wd, c.loaded, c.S[0], x[0])
+    assert rel_err(y.numpy()[0], ref) <= 2e-5
+    with pytest.raises(si.SIError):
+        si.si_sparse_ffn_decode_residual(c.layer, S, c.n_sel, 2, dev_bf16(xs[0]), y.t)
     c.layer.close()
