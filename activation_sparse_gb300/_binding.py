@@ -37,6 +37,7 @@ SIGNATURES = {
     "si_decode_plan": (_i, [_vp, _vp, _i, _i, _vp]),
     "si_sparse_ffn_decode": (_i, [_vp, _vp, _i, _i, _vp, _vp, _vp]),
     "si_sparse_ffn_decode_residual": (_i, [_vp, _vp, _i, _i, _vp, _vp, _vp]),
+    "si_sparse_ffn_decode_noalloc": (_i, [_vp, _i, _i, _vp, _i, _vp, _vp, _vp]),
     "spax_encode": (_i, [_vp, _i, _i, _i, _i, C.POINTER(_vp), _vp]),
     "spax_layer_info": (_i, [_vp, _ip, _ip, _ip, _ip, _ip]),
     "spax_layer_buffers": (_i, [_vp, C.POINTER(_vp), C.POINTER(_vp), C.POINTER(_vp)]),
@@ -241,6 +242,15 @@ def si_sparse_ffn_decode_residual(layer: Layer, S, n_sel, B, x, y, stream=None):
     torch = _torch()
     _check(load().si_sparse_ffn_decode_residual(layer.handle, _ptr(S, torch.int32, "S"), int(n_sel), int(B),
                                                 _bf16(x, "x"), _ptr(y, torch.float32, "y"), _stream(stream)))
+    return y
+
+
+def si_sparse_ffn_decode_noalloc(packed_ptr: int, n_records: int, d: int, S, n_sel, x, y, stream=None):
+    """The no-allocation batch-1 decode; packed_ptr is a device address (int)."""
+    torch = _torch()
+    _check(load().si_sparse_ffn_decode_noalloc(C.c_void_p(packed_ptr), int(n_records), int(d),
+                                               _ptr(S, torch.int32, "S"), int(n_sel), _bf16(x, "x"),
+                                               _ptr(y, torch.float32, "y"), _stream(stream)))
     return y
 
 

@@ -83,6 +83,10 @@ bool ratios_ok(double delta, double phi, double gamma) {
 
 }  // namespace
 
+namespace si {
+void set_error_message(const char* msg) { g_msg = msg; }
+}  // namespace si
+
 struct si_layer {
     int device = 0;
     int d = 0, N = 0, n_loaded = 0, n_static = 0, n_pad = 0;

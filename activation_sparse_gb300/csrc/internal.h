@@ -105,7 +105,11 @@ cudaError_t launch_pack_loaded(const uint16_t* Wg, const uint16_t* Wu, const uin
 cudaError_t launch_spax_encode(const uint16_t* Wd, int d, int N, int group, int ngp, uint16_t* WdT, uint8_t* codes,
                                float* params, cudaStream_t st);
 
+// api.cu: sets the message si_last_error_string() returns on this thread
+void set_error_message(const char* msg);
+
 // decode.cu
+int sparse_decode_b1_stages(int d);
 cudaError_t launch_repack_down(const uint16_t* packed, int d, const int32_t* pos, int n, int np, uint16_t* Wp,
                                cudaStream_t st);
 int plan_act_stages(int d);

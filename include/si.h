@@ -221,6 +221,29 @@ int si_sparse_ffn_decode(si_layer *layer, const int32_t *S, int n_sel, int B,
 int si_sparse_ffn_decode_residual(si_layer *layer, const int32_t *S, int n_sel, int B,
                                   const uint16_t *x, float *y, void *stream);
 
+/* Batch-1 sparse decode that allocates no memory: the same computation as
+ * si_sparse_ffn_decode with B == 1 (y = sum over p in S of a_p(x) * down_p,
+ * overwritten, deterministic), for callers that must not call cudaMalloc
+ * while they run -- a server that owns all device memory through its own
+ * pool, code inside a stream capture, or a process under a hard memory cap.
+ * The methods this library implements have no counterpart of it.
+ *   packed bf16 [n_records][3][d] neuron records (gate row, up row, down
+ *   column), e.g. the buffer si_layer_buffers() returns with n_records =
+ *   n_pad; S int32 [n_sel] positions in [0, n_records); x bf16 [d]; y fp32 [d].
+ * Its scratch (a 64-bit fixed-point accumulator of d words, a ticket and an
+ * error word) lives in one fixed device array of 4096 + 2 words that every
+ * GPU loading the library keeps until the process exits, so d is limited to
+ * 4096 (larger d fails with SI_ERR_INVALID_ARG); also 256 <= d, d % 64 == 0.
+ * The first call on a device looks up that array's device address
+ * (cudaGetSymbolAddress); make that first call before any stream capture.
+ * All calls share the array: calls that overlap on the GPU (other streams,
+ * other threads) race and give wrong results; order them on one stream.
+ * Each call leaves the accumulator and ticket at zero for the next one.
+ * Device-side failures go to the array's error word, which this entry point
+ * does not report. */
+int si_sparse_ffn_decode_noalloc(const uint16_t *packed, int n_records, int d, const int32_t *S,
+                                 int n_sel, const uint16_t *x, float *y, void *stream);
+
 /* ------------------------------------------------------------- SpAx */
 
 /* SpAx offline encoding, [SPAX] Fig. 2 / Fig. 3: for each column n of Wd and
