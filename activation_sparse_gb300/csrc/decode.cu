@@ -57,6 +57,36 @@ __host__ __device__ inline RingLayout ring_layout(int R, int stage_bytes, int au
 
 // Cluster-level then grid-level reduction of the per-CTA partials ypart[BD]
 // (shared memory) into y[BD]. Must be called by every thread of every CTA.
+// Producer loop of the ring kernels whose records are picked by an index
+// list (idx[0, cnt), each in [0, limit)): the warp loads the indices 32 at a
+// time, with the next block's load in flight while this block is issued, and
+// lane 0 issues record i into stage i % R once that stage's previous fill has
+// been released. An index out of range is flagged and replaced by 0. Called
+// by the whole producer warp.
+template <class IssueF>
+__device__ __forceinline__ void produce_by_index(const int32_t* __restrict__ idx, int cnt, int limit, int R,
+                                                 uint64_t* empty, unsigned* err, unsigned site, IssueF issue) {
+    const int lane = threadIdx.x & 31;
+    int pn = lane < cnt ? __ldcg(idx + lane) : 0;
+    for (int base = 0; base < cnt; base += 32) {
+        int p = pn;
+        pn = base + 32 + lane < cnt ? __ldcg(idx + base + 32 + lane) : 0;
+        const bool bad = base + lane < cnt && (p < 0 || p >= limit);
+        if (bad) p = 0;
+        if (__any_sync(0xFFFFFFFFu, bad) && lane == 0) atomicOr(err, SI_DEVERR_COUNT);
+        const int m = cnt - base < 32 ? cnt - base : 32;
+        for (int k = 0; k < m; ++k) {
+            const int pk = __shfl_sync(0xFFFFFFFFu, p, k);
+            if (lane == 0) {
+                const int i = base + k, s = i % R;
+                if (i >= R) mbar_wait(&empty[s], (uint32_t)((i / R - 1) & 1), err, site);
+                issue(i, s, pk);
+            }
+        }
+    }
+    __syncwarp();
+}
+
 __device__ void cluster_ticket_reduce(float* ypart, int BD, float* __restrict__ part, unsigned* tickets,
                                       float* __restrict__ y) {
     __shared__ unsigned s_last;
@@ -268,21 +298,13 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_sparse_decode(SparseDecodePa
     __syncthreads();
 
     if (warp == kConsWarps) {
-        if (lane == 0) {
-            const uint64_t pol = policy_evict_first();
-            for (int i = 0; i < cnt; ++i) {
-                const int s = i % R;
-                if (i >= R) mbar_wait(&empty[s], (uint32_t)((i / R - 1) & 1), P.err, kSiteDecode | kSiteEmpty);
-                int p = P.pos[lo + i];
-                if (p < 0 || p >= P.n_records) {  // never read outside the packed buffer
-                    atomicOr(P.err, SI_DEVERR_COUNT);
-                    p = 0;
-                }
-                mbar_arrive_expect_tx(&full[s], rec_bytes);
-                bulk_g2s_hint(ring + (size_t)s * L.stage, P.packed + (size_t)p * 3 * d, rec_bytes, &full[s], pol);
-            }
-        }
-        __syncwarp();
+        const uint64_t pol = policy_evict_first();
+        produce_by_index(P.pos + lo, cnt, P.n_records, R, empty, P.err, kSiteDecode | kSiteEmpty,
+                         [&](int, int s, int p) {
+                             mbar_arrive_expect_tx(&full[s], rec_bytes);
+                             bulk_g2s_hint(ring + (size_t)s * L.stage, P.packed + (size_t)p * 3 * d, rec_bytes,
+                                           &full[s], pol);
+                         });
     } else {
         float acc[MAXC][8][B];
 #pragma unroll
@@ -447,29 +469,19 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_sparse_decode_b1(SparseDecod
         // grid finishes. Otherwise the index list may be that grid's output:
         // only an L2 prefetch hint is issued before the dependency wait.
         if (!P.stable_plan) {
-            if (lane == 0) {
-                for (int i = 0; i < cnt && i < R; ++i) {
-                    const int p = P.pos[lo + i];
-                    if (p >= 0 && p < P.n_records) prefetch_l2(P.packed + (size_t)p * 3 * d, rec_bytes);
-                }
+            for (int i = lane; i < cnt && i < R; i += 32) {
+                const int p = P.pos[lo + i];
+                if (p >= 0 && p < P.n_records) prefetch_l2(P.packed + (size_t)p * 3 * d, rec_bytes);
             }
             grid_dependency_wait();
         }
-        if (lane == 0) {
-            const uint64_t pol = policy_evict_first();
-            for (int i = 0; i < cnt; ++i) {
-                const int s = i % R;
-                if (i >= R) mbar_wait(&empty[s], (uint32_t)((i / R - 1) & 1), P.err, kSiteDecode | kSiteEmpty);
-                int p = P.pos[lo + i];
-                if (p < 0 || p >= P.n_records) {  // never read outside the packed buffer
-                    atomicOr(P.err, SI_DEVERR_COUNT);
-                    p = 0;
-                }
-                mbar_arrive_expect_tx(&full[s], rec_bytes);
-                bulk_g2s_hint(ring + (size_t)s * L.stage, P.packed + (size_t)p * 3 * d, rec_bytes, &full[s], pol);
-            }
-        }
-        __syncwarp();
+        const uint64_t pol = policy_evict_first();
+        produce_by_index(P.pos + lo, cnt, P.n_records, R, empty, P.err, kSiteDecode | kSiteEmpty,
+                         [&](int, int s, int p) {
+                             mbar_arrive_expect_tx(&full[s], rec_bytes);
+                             bulk_g2s_hint(ring + (size_t)s * L.stage, P.packed + (size_t)p * 3 * d, rec_bytes,
+                                           &full[s], pol);
+                         });
         if (P.stable_plan) grid_dependency_wait();  // before the tail touches y and the partials
     } else {
         grid_dependency_wait();  // x may be the previous grid's output
@@ -760,6 +772,16 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_dense_act(DenseActParams P) 
         }
         fence_mbar_init();
     }
+    grid_launch_dependents();
+    // The weights belong to the caller and may be the previous grid's output,
+    // so before the dependency wait they are only prefetched into L2; x and a
+    // are touched after it.
+    if (warp == kConsWarps)
+        for (int i = lane; i < cnt && i < R; i += 32) {
+            prefetch_l2(P.Wg + (size_t)(lo + i) * d, row_bytes);
+            prefetch_l2(P.Wu + (size_t)(lo + i) * d, row_bytes);
+        }
+    grid_dependency_wait();
     for (int i = threadIdx.x; i < d / 8; i += blockDim.x)
         reinterpret_cast<uint4*>(s_x)[i] = reinterpret_cast<const uint4*>(P.x)[i];
     __syncthreads();
@@ -841,9 +863,15 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_tiered_down(TieredDownParams
         }
         fence_mbar_init();
     }
+    // the tier lists and a are the previous grids' output
+    grid_launch_dependents();
+    grid_dependency_wait();
+    int* s_col = reinterpret_cast<int*>(s_av + P.aux_floats / 2);
     for (int i = threadIdx.x; i < nrec; i += blockDim.x) {
         const int col = i < ntop ? P.top[t0 + i] : P.mid[m0 + i - ntop];
-        s_av[i] = (col >= 0 && col < P.N) ? P.a[col] : 0.0f;
+        const bool ok = col >= 0 && col < P.N;
+        s_col[i] = ok ? col : -1;
+        s_av[i] = ok ? P.a[col] : 0.0f;
     }
     __syncthreads();
 
@@ -854,8 +882,8 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_tiered_down(TieredDownParams
                 const int s = i % R;
                 if (i >= R) mbar_wait(&empty[s], (uint32_t)((i / R - 1) & 1), P.err, kSiteTiered | kSiteEmpty);
                 uint8_t* dst = ring + (size_t)s * L.stage;
-                int ci = i < ntop ? P.top[t0 + i] : P.mid[m0 + i - ntop];
-                if (ci < 0 || ci >= P.N) {  // never read outside the encoded buffers
+                int ci = s_col[i];
+                if (ci < 0) {  // never read outside the encoded buffers
                     atomicOr(P.err, SI_DEVERR_COUNT);
                     ci = 0;
                 }
@@ -1204,14 +1232,13 @@ cudaError_t launch_dense_act(DenseActParams P, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     const size_t smem = (size_t)ring_layout(P.R, 4 * P.d, 0, P.d * 2).total;
     const int grid = P.N < sms ? P.N : sms;
+    void* args[] = {&P};
     if (P.d > 2048) {
         if ((e = allow_max_smem(k_dense_act<2>)) != cudaSuccess) return e;
-        k_dense_act<2><<<grid, kDecThreads, smem, st>>>(P);
-    } else {
-        if ((e = allow_max_smem(k_dense_act<1>)) != cudaSuccess) return e;
-        k_dense_act<1><<<grid, kDecThreads, smem, st>>>(P);
+        return launch_clustered(k_dense_act<2>, grid, 1, smem, st, args, /*pdl=*/true);
     }
-    return cudaGetLastError();
+    if ((e = allow_max_smem(k_dense_act<1>)) != cudaSuccess) return e;
+    return launch_clustered(k_dense_act<1>, grid, 1, smem, st, args, /*pdl=*/true);
 }
 
 int tiered_down_stages(int d, int aux_floats) {
@@ -1232,11 +1259,12 @@ cudaError_t launch_tiered_down(TieredDownParams P, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     if (P.part_floats < (long long)(grid / cluster) * P.d) return cudaErrorInvalidValue;
     // per-CTA record counts must fit the activation buffer
+    // (activations in the first half of the buffer, columns in the second)
     const long long per = (long long)(P.k_top + grid - 1) / grid + (P.k_mid + grid - 1) / grid;
-    if (per > P.aux_floats) return cudaErrorInvalidValue;
+    if (2 * per > P.aux_floats) return cudaErrorInvalidValue;
     void* args[] = {&P};
-    if (P.d > 2048) return launch_clustered(k_tiered_down<2>, grid, cluster, smem, st, args);
-    return launch_clustered(k_tiered_down<1>, grid, cluster, smem, st, args);
+    if (P.d > 2048) return launch_clustered(k_tiered_down<2>, grid, cluster, smem, st, args, /*pdl=*/true);
+    return launch_clustered(k_tiered_down<1>, grid, cluster, smem, st, args, /*pdl=*/true);
 }
 
 int streaming_grid_upper_bound() {

@@ -82,7 +82,7 @@ struct TieredDownParams {
     unsigned* tickets;
     unsigned* err;
     int R;
-    int aux_floats;           // capacity of the per-CTA activation buffer
+    int aux_floats;           // per-CTA buffer: activations in the first half, columns in the second
 };
 
 // select.cu

@@ -331,7 +331,7 @@ def run_gpu(args, world, rank, local):
         "prefill_select_ms": round(statistics.mean(pre_ms), 4),
         "prefill_gemm_ms": round(gemm_s * 1e3, 4),
         "offline_ms": {"profile_16_layers_4096_tokens": round(t_prof * 1e3, 3), "pack_16_layers": round(t_pack * 1e3, 3)},
-        "roofline": {"kernel": "k_sparse_decode", "bound": "hbm", "achieved": round(achieved_gbs, 1),
+        "roofline": {"kernel": "k_sparse_decode_b1", "bound": "hbm", "achieved": round(achieved_gbs, 1),
                      "peak": hbm_peak, "unit": "GB/s", "frac": round(achieved_gbs / hbm_peak, 4),
                      "peak_source": peak_kind, "traffic": args.traffic,
                      "bytes_per_launch": launch_bytes, "launch_us": round(launch_s * 1e6, 3)},
@@ -538,7 +538,8 @@ def run_reference(args, world, rank):
 
 def run_profile_case(args):
     """A few launches of one kernel on one full-size layer, for ncu captures:
-    decode (k_sparse_decode, Llama3.2-1B layer), prefill (k_act_gemm,
+    decode (k_sparse_decode_b1 in the residual form with a decode plan, as
+    the timed step runs it, Llama3.2-1B layer), prefill (k_act_gemm,
     512-token prompt), dense (k_dense_act) and tiered (k_tiered_down) on a
     Llama-3.1-8B layer. Prints one JSON line with the CUDA-event time."""
     import torch
@@ -558,7 +559,9 @@ def run_profile_case(args):
         si.si_select_dynamic(layer, X, w.T, 1, w.alpha, w.phi, S, A)
         x = gpu_tokens(torch, 7, 2, 1, w.d, dev)
         y = torch.empty((1, w.d), dtype=torch.float32, device=dev)
-        fn = (lambda: si.si_sparse_ffn_decode(layer, S, n_sel, 1, x, y)) if case == "decode" else \
+        si.si_decode_plan(layer, S, n_sel, 1)
+        y.zero_()
+        fn = (lambda: si.si_sparse_ffn_decode_residual(layer, S, n_sel, 1, x, y)) if case == "decode" else \
              (lambda: si.si_prefill_absact(layer, X, w.T, 1, A))
     else:
         w = SPAX_WL
@@ -593,7 +596,7 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU oracle time budget")
     ap.add_argument("--traffic", type=float, default=None,
-                    help="DRAM bytes per k_sparse_decode launch from an ncu capture (null when unknown)")
+                    help="DRAM bytes per k_sparse_decode_b1 launch from an ncu capture (null when unknown)")
     ap.add_argument("--out-dir", default=None, help="directory for the clock samples (optional)")
     ap.add_argument("--profile-case", choices=["decode", "prefill", "dense", "tiered"], default=None,
                     help="run only a few launches of one kernel (for ncu captures)")
