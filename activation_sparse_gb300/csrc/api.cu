@@ -104,9 +104,6 @@ struct si_layer {
     int32_t* plan_pos = nullptr;
     uint32_t* plan_mask = nullptr;
     int* plan_n = nullptr;
-    uint16_t* plan_Wp = nullptr;  // batch-1 plan: row-major down weights of the selected records [d][np]
-    float* plan_a = nullptr;      // batch-1 plan: activations of the selected records [np]
-    int plan_np = 0;
     const int32_t* plan_S = nullptr;
     int plan_nsel = -1, plan_B = 0;
     // True from si_decode_plan until the next decode launch on this handle: that
@@ -121,8 +118,7 @@ struct spax_layer {
     uint16_t* WdT = nullptr;
     uint8_t* codes = nullptr;
     float* params = nullptr;
-    int32_t* top = nullptr;
-    int32_t* mid = nullptr;
+    unsigned* hist = nullptr;  // tier histogram of the current a (zero between calls) + its ticket
     float* a = nullptr;
     float* part = nullptr;
     long long part_floats = 0;
@@ -156,8 +152,6 @@ void destroy_layer(si_layer* L) {
     dfree(L->plan_pos);
     dfree(L->plan_mask);
     dfree(L->plan_n);
-    dfree(L->plan_Wp);
-    dfree(L->plan_a);
     delete L;
 }
 
@@ -166,8 +160,7 @@ void destroy_spax(spax_layer* L) {
     dfree(L->WdT);
     dfree(L->codes);
     dfree(L->params);
-    dfree(L->top);
-    dfree(L->mid);
+    dfree(L->hist);
     dfree(L->a);
     dfree(L->part);
     dfree(L->tickets);
@@ -445,20 +438,9 @@ int si_decode_plan(si_layer* L, const int32_t* S, int n_sel, int B, void* stream
         if (rc) return rc;
     }
     if (B == 1) {
-        // batch 1: the plan is S itself plus a row-major copy of the selected
-        // down columns, so decode needs no cross-CTA sum (see si_sparse_ffn_decode)
-        const int np_cap = round_up(L->n_loaded, 8);
-        if (!L->plan_Wp) {
-            if (capturing(st)) return fail(SI_ERR_INVALID_ARG, "plan buffers must be allocated before capture");
-            if ((rc = dalloc(&L->plan_Wp, (size_t)L->d * np_cap, "plan down rows")) ||
-                (rc = dalloc(&L->plan_a, (size_t)np_cap, "plan activations")))
-                return rc;
-        }
-        const int np = round_up(n_sel > 0 ? n_sel : 1, 8);
+        // batch 1: the plan is a copy of S that later calls may read before
+        // their dependency wait (nothing but si_decode_plan writes it)
         if (n_sel > 0) SI_CK(cudaMemcpyAsync(L->plan_pos, S, (size_t)n_sel * 4, cudaMemcpyDeviceToDevice, st));
-        SI_CK(cudaMemsetAsync(L->plan_a, 0, (size_t)np * sizeof(float), st));
-        SI_CK(si::launch_repack_down(L->packed, L->d, L->plan_pos, n_sel, np, L->plan_Wp, st));
-        L->plan_np = np;
     } else {
         SI_CK(si::launch_decode_plan(S, n_sel, B, L->n_loaded, L->plan_pos, L->plan_mask, L->plan_n, err, st));
     }
@@ -517,34 +499,6 @@ int sparse_decode_impl(si_layer* L, const int32_t* S, int n_sel, int B, const ui
     const bool have_plan = L->plan_S == S && L->plan_nsel == n_sel && L->plan_B == B;
     const bool stable = have_plan && !L->plan_fresh;
     P.stable_plan = stable ? 1 : 0;
-    if (B == 1 && have_plan && !accumulate) {
-        // planned batch 1: gate/up pass over the plan's records writes a, then
-        // each CTA of the down pass owns output rows of the row-major plan copy
-        si::PlanActParams A = {};
-        A.packed = L->packed;
-        A.n_records = L->n_pad;
-        A.d = L->d;
-        A.pos = L->plan_pos;
-        A.n = n_sel;
-        A.x = x;
-        A.a = L->plan_a;
-        A.err = err;
-        A.R = si::plan_act_stages(L->d);
-        A.stable_plan = P.stable_plan;
-        si::PlanDownParams D = {};
-        D.Wp = L->plan_Wp;
-        D.np = L->plan_np;
-        D.d = L->d;
-        D.rows = si::plan_down_rows(L->d, L->plan_np);
-        D.a = L->plan_a;
-        D.y = y;
-        D.err = err;
-        D.stable_plan = P.stable_plan;
-        SI_CK(si::launch_plan_act(A, (cudaStream_t)stream));
-        SI_CK(si::launch_plan_down(D, (cudaStream_t)stream));
-        L->plan_fresh = false;
-        return SI_OK;
-    }
     if (B == 1) {
         // a batch-1 plan is a copy of S (n_sel entries); the count is the host's
         P.pos = stable ? L->plan_pos : S;
@@ -573,8 +527,8 @@ int spax_encode(const uint16_t* Wd, int d, int N, int bits, int group, spax_laye
     *out = nullptr;
     if (!Wd) return fail(SI_ERR_INVALID_ARG, "NULL pointer");
     if (bits != 4) return fail(SI_ERR_UNSUPPORTED, "only 4-bit codes are implemented");
-    if (group < 8 || group % 8 || d < 64 || d % 64 || d % group)
-        return fail(SI_ERR_INVALID_ARG, "need group % 8 == 0, d % 64 == 0, d % group == 0");
+    if (group < 8 || (group & (group - 1)) || d < 64 || d % 64 || d % group)
+        return fail(SI_ERR_INVALID_ARG, "need group a power of two >= 8, d % 64 == 0, d % group == 0");
     if (d > 4096) return fail(SI_ERR_UNSUPPORTED, "tiered decode supports d <= 4096");
     if (N < 1 || N > 32768) return fail(SI_ERR_INVALID_ARG, "need 1 <= N <= 32768");
     cudaStream_t st = (cudaStream_t)stream;
@@ -589,13 +543,14 @@ int spax_encode(const uint16_t* Wd, int d, int N, int bits, int group, spax_laye
     int rc;
     if ((rc = dalloc(&L->WdT, (size_t)N * d, "column-major Wd")) ||
         (rc = dalloc(&L->codes, (size_t)N * d / 2, "codes")) ||
-        (rc = dalloc(&L->params, (size_t)N * L->ngp * 2, "code params")) || (rc = dalloc(&L->top, N, "top tier")) ||
-        (rc = dalloc(&L->mid, N, "mid tier")) || (rc = dalloc(&L->a, N, "activations")) ||
+        (rc = dalloc(&L->params, (size_t)N * L->ngp * 2, "code params")) ||
+        (rc = dalloc(&L->hist, si::kTierBins + 1, "tier histogram")) || (rc = dalloc(&L->a, N, "activations")) ||
         (rc = dalloc(&L->tickets, 16, "tickets")) || (rc = grow_part(&L->part, &L->part_floats, d, 1))) {
         destroy_spax(L);
         return rc;
     }
     cudaError_t e = cudaMemsetAsync(L->tickets, 0, 16 * sizeof(unsigned), st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(L->hist, 0, (si::kTierBins + 1) * sizeof(unsigned), st);
     if (e == cudaSuccess) e = cudaMemsetAsync(L->params, 0, (size_t)N * L->ngp * 2 * sizeof(float), st);
     if (e == cudaSuccess) e = si::launch_spax_encode(Wd, d, N, group, L->ngp, L->WdT, L->codes, L->params, st);
     if (e == cudaSuccess) e = cudaStreamSynchronize(st);
@@ -632,7 +587,12 @@ int spax_layer_destroy(spax_layer* L) {
     return SI_OK;
 }
 
-int spax_dense_act(const uint16_t* Wg, const uint16_t* Wu, int d, int N, const uint16_t* x, float* a, void* stream) {
+}  // extern "C"
+
+namespace {
+
+int dense_act_core(const uint16_t* Wg, const uint16_t* Wu, int d, int N, const uint16_t* x, float* a, unsigned* hist,
+                   cudaStream_t stream) {
     if (!Wg || !Wu || !x || !a) return fail(SI_ERR_INVALID_ARG, "NULL pointer");
     if (d < 8 || d % 8 || N < 1) return fail(SI_ERR_INVALID_ARG, "need d % 8 == 0, N >= 1");
     if (d > 4096) return fail(SI_ERR_UNSUPPORTED, "dense activation pass supports d <= 4096");
@@ -646,34 +606,38 @@ int spax_dense_act(const uint16_t* Wg, const uint16_t* Wu, int d, int N, const u
     P.N = N;
     P.x = x;
     P.a = a;
+    P.hist = hist;
     P.err = err;
     P.R = si::dense_act_stages(d);
     if (P.R < 8) return fail(SI_ERR_UNSUPPORTED, "d too large for the activation ring");
-    SI_CK(si::launch_dense_act(P, (cudaStream_t)stream));
+    SI_CK(si::launch_dense_act(P, stream));
     return SI_OK;
 }
 
-int spax_tiered_down(spax_layer* L, const float* a, double top_frac, double mid_frac, float* y, int32_t* top_idx,
-                     int32_t* mid_idx, void* stream) {
-    if (!L || !a || !y) return fail(SI_ERR_INVALID_ARG, "NULL pointer");
+int tier_counts(const spax_layer* L, double top_frac, double mid_frac, long long* k_top, long long* k_mid) {
     if (!(top_frac >= 0.0 && mid_frac >= 0.0 && top_frac <= 1.0 && mid_frac <= 1.0))
         return fail(SI_ERR_INVALID_ARG, "tier fractions must be in [0, 1]");
-    const long long k_top = count_of(top_frac, L->N), k_mid = count_of(mid_frac, L->N);
-    if (k_top + k_mid > L->N) return fail(SI_ERR_INVALID_ARG, "top + mid tiers exceed N");
-    cudaStream_t st = (cudaStream_t)stream;
+    *k_top = count_of(top_frac, L->N);
+    *k_mid = count_of(mid_frac, L->N);
+    if (*k_top + *k_mid > L->N) return fail(SI_ERR_INVALID_ARG, "top + mid tiers exceed N");
+    return SI_OK;
+}
+
+// The tiered down-projection with the tier choice inside the kernel; L->hist
+// must hold the tier histogram of a (the kernel re-zeroes it).
+int tiered_core(spax_layer* L, const float* a, long long k_top, long long k_mid, float* y, int32_t* top_out,
+                int32_t* mid_out, cudaStream_t st) {
     unsigned* err = nullptr;
     int rc = err_word(&err);
     if (rc) return rc;
-    int32_t* top = top_idx ? top_idx : L->top;
-    int32_t* mid = mid_idx ? mid_idx : L->mid;
-    SI_CK(si::launch_spax_tiers(a, L->N, (int)k_top, (int)k_mid, top, mid, err, st));
     si::TieredDownParams P = {};
     P.WdT = L->WdT;
     P.codes = L->codes;
     P.params = L->params;
     P.a = a;
-    P.top = top;
-    P.mid = mid;
+    P.hist = L->hist;
+    P.top_out = top_out;
+    P.mid_out = mid_out;
     P.d = L->d;
     P.group = L->group;
     P.ngp = L->ngp;
@@ -688,18 +652,45 @@ int spax_tiered_down(spax_layer* L, const float* a, double top_frac, double mid_
     const int gmin = si::streaming_grid_upper_bound() / 4;  // grids are at least a quarter of the SMs
     P.aux_floats = round_up((int)(L->N / (gmin > 0 ? gmin : 1)) * 2 + 8, 32);
     P.R = si::tiered_down_stages(L->d, P.aux_floats);
-    if (P.R < 2) return fail(SI_ERR_UNSUPPORTED, "d too large for the tier ring");
+    if (P.R < 8) return fail(SI_ERR_UNSUPPORTED, "d too large for the tier ring");
     SI_CK(si::launch_tiered_down(P, st));
     return SI_OK;
 }
 
+}  // namespace
+
+extern "C" {
+
+int spax_dense_act(const uint16_t* Wg, const uint16_t* Wu, int d, int N, const uint16_t* x, float* a, void* stream) {
+    return dense_act_core(Wg, Wu, d, N, x, a, nullptr, (cudaStream_t)stream);
+}
+
+int spax_tiered_down(spax_layer* L, const float* a, double top_frac, double mid_frac, float* y, int32_t* top_idx,
+                     int32_t* mid_idx, void* stream) {
+    if (!L || !a || !y) return fail(SI_ERR_INVALID_ARG, "NULL pointer");
+    long long k_top = 0, k_mid = 0;
+    int rc = tier_counts(L, top_frac, mid_frac, &k_top, &k_mid);
+    if (rc) return rc;
+    cudaStream_t st = (cudaStream_t)stream;
+    SI_CK(si::launch_abs_hist(a, L->N, L->hist, st));
+    return tiered_core(L, a, k_top, k_mid, y, top_idx, mid_idx, st);
+}
+
 int spax_ffn_decode(spax_layer* L, const uint16_t* Wg, const uint16_t* Wu, const uint16_t* x, double top_frac,
                     double mid_frac, float* y, float* a_out, void* stream) {
-    if (!L) return fail(SI_ERR_INVALID_ARG, "layer is NULL");
-    float* a = a_out ? a_out : L->a;
-    int rc = spax_dense_act(Wg, Wu, L->d, L->N, x, a, stream);
+    if (!L || !y) return fail(SI_ERR_INVALID_ARG, "NULL pointer");
+    long long k_top = 0, k_mid = 0;
+    int rc = tier_counts(L, top_frac, mid_frac, &k_top, &k_mid);
     if (rc) return rc;
-    return spax_tiered_down(L, a, top_frac, mid_frac, y, nullptr, nullptr, stream);
+    cudaStream_t st = (cudaStream_t)stream;
+    float* a = a_out ? a_out : L->a;
+    // the dense pass builds the tier histogram of a as it writes it
+    if ((rc = dense_act_core(Wg, Wu, L->d, L->N, x, a, L->hist, st))) return rc;
+    if ((rc = tiered_core(L, a, k_top, k_mid, y, nullptr, nullptr, st))) {
+        cudaMemsetAsync(L->hist, 0, (si::kTierBins + 1) * sizeof(unsigned), st);  // leave it clean
+        return rc;
+    }
+    return SI_OK;
 }
 
 }  // extern "C"

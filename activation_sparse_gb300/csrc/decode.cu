@@ -1,27 +1,30 @@
 // decode.cu -- HBM-streaming decode kernels (one token per sequence).
 //
-//  k_sparse_decode  SelectInfer sparse decode FFN (section 5: only the
-//                   selected neurons are computed): for each selected packed
-//                   record [gate row | up row | down column] it forms
-//                   a = silu(g.x) * (u.x) and accumulates a * down into a
-//                   per-CTA partial of y.
-//  k_dense_act      SpAx dense gate/up pass: a[n] for every neuron.
-//  k_tiered_down    SpAx three-tier down-projection (abstract, Fig. 2/3):
-//                   top columns in bf16, middle columns rebuilt from 4-bit
-//                   codes (min + q * scale), the rest never read.
+//  k_sparse_decode_b1  SelectInfer sparse decode FFN for one sequence
+//                      (section 5: only the selected neurons are computed):
+//                      for each selected packed record [gate row | up row |
+//                      down column] it forms a = silu(g.x) * (u.x) and adds
+//                      a * down into a per-warp partial of y.
+//  k_sparse_decode     the same for B <= 8 sequences over the union of their
+//                      selections (each record carries a mask of the
+//                      sequences that selected it).
+//  k_dense_act         SpAx dense gate/up pass: a[n] for every neuron.
+//  k_tiered_down       SpAx three-tier down-projection (abstract, Fig. 2/3):
+//                      top columns in bf16, middle columns rebuilt from 4-bit
+//                      codes (min + q * scale), the rest never read.
 //
 // Common structure (warp-specialised, one CTA per SM):
-//   * warp 8, lane 0 streams whole records into a ring of shared-memory
+//   * the producer warp streams whole records into a ring of shared-memory
 //     stages with 1-D bulk copies (cp.async.bulk, completion counted in bytes
-//     on a per-stage "full" mbarrier); consumer warps release a stage through
-//     its "empty" mbarrier. Every wait is bounded.
+//     on a per-stage "full" mbarrier); consumers release a stage through its
+//     "empty" mbarrier. Every wait is bounded.
 //   * records are split evenly over the CTAs of the grid (split-K over
-//     neurons / columns), each CTA keeps its partial y in registers;
-//   * reduction: the CTAs of a thread-block cluster sum their partials
-//     through distributed shared memory (each CTA owns a slice of y), write
-//     one partial per cluster, and the last cluster to finish a slice (an
-//     atomic ticket, no waiting) sums the cluster partials in fixed order.
-//     The result is deterministic run to run.
+//     neurons / columns); partial sums of y stay in registers.
+//   * cross-CTA sum of y: 64-bit fixed-point atomics with a ticketed final
+//     conversion (batch-1 overwrite; deterministic), float atomics into y
+//     (batch-1 residual form), or cluster reduction through distributed
+//     shared memory plus a ticketed fixed-order final pass (batch B and
+//     tiered down; deterministic).
 #include <cooperative_groups.h>
 
 #include "common.cuh"
@@ -55,8 +58,6 @@ __host__ __device__ inline RingLayout ring_layout(int R, int stage_bytes, int au
     return L;
 }
 
-// Cluster-level then grid-level reduction of the per-CTA partials ypart[BD]
-// (shared memory) into y[BD]. Must be called by every thread of every CTA.
 // Producer loop of the ring kernels whose records are picked by an index
 // list (idx[0, cnt), each in [0, limit)): the warp loads the indices 32 at a
 // time, with the next block's load in flight while this block is issued, and
@@ -87,6 +88,8 @@ __device__ __forceinline__ void produce_by_index(const int32_t* __restrict__ idx
     __syncwarp();
 }
 
+// Cluster-level then grid-level reduction of the per-CTA partials ypart[BD]
+// (shared memory) into y[BD]. Must be called by every thread of every CTA.
 __device__ void cluster_ticket_reduce(float* ypart, int BD, float* __restrict__ part, unsigned* tickets,
                                       float* __restrict__ y) {
     __shared__ unsigned s_last;
@@ -580,168 +583,6 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_sparse_decode_b1(SparseDecod
 
 // ------------------------------------------------------ planned batch-1 decode
 
-// Plan repack: Wp[j][i] = down column of record pos[i], element j, so that a
-// CTA that owns output rows reads them contiguously. Pad columns i >= n are
-// zero. 32 x 32 tiles through shared memory.
-__global__ void __launch_bounds__(256) k_repack_down(const uint16_t* __restrict__ packed, int d,
-                                                    const int32_t* __restrict__ pos, int n, int np,
-                                                    uint16_t* __restrict__ Wp) {
-    __shared__ uint16_t tile[32][34];
-    __shared__ int s_p[32];
-    const int i0 = blockIdx.x * 32, j0 = blockIdx.y * 32;
-    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
-    if (threadIdx.x < 32) s_p[threadIdx.x] = (i0 + threadIdx.x < n) ? pos[i0 + threadIdx.x] : -1;
-    __syncthreads();
-    for (int ii = ty; ii < 32; ii += 8) {
-        const int p = s_p[ii];
-        tile[ii][tx] = (p >= 0 && j0 + tx < d) ? packed[((size_t)p * 3 + 2) * d + j0 + tx] : (uint16_t)0;
-    }
-    __syncthreads();
-    for (int jj = ty; jj < 32; jj += 8)
-        if (j0 + jj < d && i0 + tx < np) Wp[(size_t)(j0 + jj) * np + i0 + tx] = tile[tx][jj];
-}
-
-// K5a: a[i] = silu(gate[pos[i]] . x) * (up[pos[i]] . x). Warp w owns records
-// i = w, w + 8, ... of its CTA's range and ring stages i % R (R a multiple of
-// 8); only the gate and up rows (the first 4d bytes of a record) are read.
-// With a stable plan the ring fills before the dependency wait; x is read
-// after it.
-template <int MAXC>
-__global__ void __launch_bounds__(kDecThreads, 1) k_plan_act(PlanActParams P) {
-    extern __shared__ __align__(1024) uint8_t smem[];
-    const int d = P.d;
-    const RingLayout L = ring_layout(P.R, 4 * d, 0, 0);
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.off_full);
-    uint64_t* empty = reinterpret_cast<uint64_t*>(smem + L.off_empty);
-    uint8_t* ring = smem + L.off_ring;
-    const int R = L.R;
-    if (R < 1) {  // the host never launches without stages; refuse rather than divide by zero
-        if (threadIdx.x == 0) atomicOr(P.err, SI_DEVERR_COUNT);
-        return;
-    }
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int lo = (int)((long long)P.n * blockIdx.x / gridDim.x);
-    const int hi = (int)((long long)P.n * (blockIdx.x + 1) / gridDim.x);
-    const int cnt = hi - lo;
-    const uint32_t row2 = (uint32_t)(4 * d);
-    constexpr int XJ = 8 * MAXC;
-    const int nch = d / 8;
-
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < R; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1);
-        }
-        fence_mbar_init();
-    }
-    __syncthreads();
-    grid_launch_dependents();
-
-    if (warp == kConsWarps) {
-        if (!P.stable_plan) grid_dependency_wait();
-        if (lane == 0) {
-            const uint64_t pol = policy_evict_first();
-            for (int i = 0; i < cnt; ++i) {
-                const int s = i % R;
-                if (i >= R) mbar_wait(&empty[s], (uint32_t)((i / R - 1) & 1), P.err, kSiteDecode | kSiteEmpty);
-                int p = P.pos[lo + i];
-                if (p < 0 || p >= P.n_records) {
-                    atomicOr(P.err, SI_DEVERR_COUNT);
-                    p = 0;
-                }
-                mbar_arrive_expect_tx(&full[s], row2);
-                bulk_g2s_hint(ring + (size_t)s * L.stage, P.packed + (size_t)p * 3 * d, row2, &full[s], pol);
-            }
-        }
-        __syncwarp();
-    } else {
-        grid_dependency_wait();  // x may be the previous grid's output; a may still be read by it
-        uint4 xr[XJ];
-#pragma unroll
-        for (int j = 0; j < XJ; ++j) {
-            const int c = lane + 32 * j;
-            xr[j] = (c < nch) ? __ldg(reinterpret_cast<const uint4*>(P.x) + c) : make_uint4(0u, 0u, 0u, 0u);
-        }
-        for (int i = warp; i < cnt; i += kConsWarps) {
-            const int s = i % R;
-            mbar_wait(&full[s], (uint32_t)((i / R) & 1), P.err, kSiteDecode | kSiteFull);
-            const uint4* st = reinterpret_cast<const uint4*>(ring + (size_t)s * L.stage);
-            float ga[4] = {0.f, 0.f, 0.f, 0.f}, ua[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int j = 0; j < XJ; ++j) {
-                const int c = lane + 32 * j;
-                if (c < nch) {
-                    ga[j & 3] = dot8(st[c], xr[j], ga[j & 3]);
-                    ua[j & 3] = dot8(st[nch + c], xr[j], ua[j & 3]);
-                }
-            }
-            const float g = warp_sum((ga[0] + ga[1]) + (ga[2] + ga[3]));
-            const float u = warp_sum((ua[0] + ua[1]) + (ua[2] + ua[3]));
-            __syncwarp();
-            if (lane == 0) {
-                P.a[lo + i] = swiglu(g, u);
-                mbar_arrive(&empty[s]);
-            }
-        }
-    }
-}
-
-// K5b: y[j] = sum_i a[i] * Wp[j][i] for the CTA's rows. The rows (plan data)
-// stream into shared memory before the dependency wait when the plan is
-// stable; a is read after it. Warp w handles rows w, w + 8, ...; lanes stride
-// over 8-column chunks with four accumulators, summed in a fixed order.
-__global__ void __launch_bounds__(256, 2) k_plan_down(PlanDownParams P) {
-    extern __shared__ __align__(1024) uint8_t smem[];
-    uint64_t* bar = reinterpret_cast<uint64_t*>(smem);
-    float* s_a = reinterpret_cast<float*>(smem + 128);
-    uint16_t* s_w = reinterpret_cast<uint16_t*>(smem + 128 + round_up(P.np * 4, 128));
-    const int r0 = blockIdx.x * P.rows;
-    const int nr = min(P.rows, P.d - r0);
-    const uint32_t row_bytes = (uint32_t)(P.np * 2);
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (threadIdx.x == 0) {
-        mbar_init(bar, 1);
-        fence_mbar_init();
-    }
-    __syncthreads();
-    grid_launch_dependents();
-    if (!P.stable_plan) grid_dependency_wait();
-    if (threadIdx.x == 0 && nr > 0) {
-        mbar_arrive_expect_tx(bar, row_bytes * (uint32_t)nr);
-        const uint64_t pol = policy_evict_first();
-        for (int r = 0; r < nr; ++r)
-            bulk_g2s_hint(s_w + (size_t)r * P.np, P.Wp + (size_t)(r0 + r) * P.np, row_bytes, bar, pol);
-    }
-    grid_dependency_wait();  // a is the previous grid's output
-    for (int k = threadIdx.x; k < P.np / 4; k += blockDim.x)
-        reinterpret_cast<float4*>(s_a)[k] = __ldcg(reinterpret_cast<const float4*>(P.a) + k);
-    __syncthreads();
-    if (nr > 0) mbar_wait(bar, 0u, P.err, kSiteDecode | kSiteFullB);
-    const int nch = P.np / 8;
-    for (int r = warp; r < nr; r += 8) {
-        const uint4* w = reinterpret_cast<const uint4*>(s_w + (size_t)r * P.np);
-        const float4* av = reinterpret_cast<const float4*>(s_a);
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
-        int q = 0;
-        for (int c = lane; c < nch; c += 32, ++q) {
-            float f[8];
-            unpack8(w[c], f);
-            const float4 a0 = av[2 * c], a1 = av[2 * c + 1];
-            float t = acc[q & 3];
-            t = fmaf(f[0], a0.x, t);
-            t = fmaf(f[1], a0.y, t);
-            t = fmaf(f[2], a0.z, t);
-            t = fmaf(f[3], a0.w, t);
-            t = fmaf(f[4], a1.x, t);
-            t = fmaf(f[5], a1.y, t);
-            t = fmaf(f[6], a1.z, t);
-            t = fmaf(f[7], a1.w, t);
-            acc[q & 3] = t;
-        }
-        const float v = warp_sum((acc[0] + acc[1]) + (acc[2] + acc[3]));
-        if (lane == 0) P.y[r0 + r] = P.accumulate ? P.y[r0 + r] + v : v;
-    }
-}
 
 // --------------------------------------------------------------- dense act
 
@@ -825,15 +666,429 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_dense_act(DenseActParams P) 
             const float u = warp_sum((ua[0] + ua[1]) + (ua[2] + ua[3]));
             __syncwarp();
             if (lane == 0) {
-                P.a[lo + i] = swiglu(g, u);
+                const float av = swiglu(g, u);
+                P.a[lo + i] = av;
+                if (P.hist) atomicAdd(P.hist + (abs_key(av) >> kTierShift), 1u);
                 mbar_arrive(&empty[s]);
             }
         }
     }
 }
 
+// Tier histogram of a given activation vector, for a tiered call whose a
+// did not come from the dense pass (which builds the same histogram).
+__global__ void __launch_bounds__(256) k_abs_hist(const float* __restrict__ a, int N, unsigned* __restrict__ hist) {
+    __shared__ unsigned h[kTierBins];
+    grid_launch_dependents();
+    grid_dependency_wait();  // a may be the previous grid's output
+    for (int i = threadIdx.x; i < kTierBins; i += blockDim.x) h[i] = 0u;
+    __syncthreads();
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < N; i += gridDim.x * blockDim.x)
+        atomicAdd(&h[abs_key(__ldcg(a + i)) >> kTierShift], 1u);
+    __syncthreads();
+    for (int i = threadIdx.x; i < kTierBins; i += blockDim.x)
+        if (h[i]) atomicAdd(hist + i, h[i]);
+}
+
 // ---------------------------------------------------------- tiered down
 
+// Tier choice inside the tiered kernel (abstract, Fig. 2: Top = the k_top
+// largest |a|, Mid = the next k_mid, ties to the lower index). Every CTA
+// derives the same two rank boundaries, K0 = k_top and K1 = k_top + k_mid:
+// the tier histogram (bits 30..20 of the |a| key) gives each boundary's
+// top digit, two passes over the keys of that bin (bits 19..9, then 8..0)
+// give the exact key `thr` and how many keys equal to it are taken. The
+// CTA then counts the members of each tier in index order and takes its
+// window of ranks of both tiers (balanced over the CTAs).
+constexpr int kTDW = kDecThreads / 32;  // warps of the tiered kernel
+
+// Exclusive scan over the CTA's warps of two per-warp counts (the same value
+// in every lane of a warp); gives the warp's offsets and the CTA totals.
+__device__ __forceinline__ void cta_scan2(uint32_t c0, uint32_t c1, uint2* s_w, uint32_t& o0, uint32_t& o1,
+                                          uint32_t& n0, uint32_t& n1) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (lane == 0) s_w[warp] = make_uint2(c0, c1);
+    __syncthreads();
+    uint32_t a0 = 0u, a1 = 0u, t0 = 0u, t1 = 0u;
+#pragma unroll
+    for (int w = 0; w < kTDW; ++w) {
+        const uint2 v = s_w[w];
+        if (w < warp) {
+            a0 += v.x;
+            a1 += v.y;
+        }
+        t0 += v.x;
+        t1 += v.y;
+    }
+    o0 = a0;
+    o1 = a1;
+    n0 = t0;
+    n1 = t1;
+    __syncthreads();  // s_w may be reused
+}
+
+// For each active boundary t: the bin of h[t] (nb bins, a power of two >= 256,
+// counted from the highest bin down) holding its kk[t]-th largest key.
+// Updates kk[t] to the rank left inside that bin and returns the bin and its
+// count; `total` is the sum of h[0]. Threads 0..255 own nb/256 bins each.
+__device__ void find_bins2(const unsigned* h0, const unsigned* h1, int nb, const bool* act, uint32_t* kk,
+                           uint32_t* bin, uint32_t* cnt, uint32_t* total, uint2* s_w, uint32_t* s_state) {
+    const int tid = threadIdx.x, lane = tid & 31;
+    const int per = nb / 256;
+    const bool own = tid < 256;
+    uint32_t c[2] = {0u, 0u};
+    if (own)
+        for (int j = 0; j < per; ++j) {
+            c[0] += h0[nb - 1 - per * tid - j];
+            c[1] += h1[nb - 1 - per * tid - j];
+        }
+    uint32_t w0 = c[0], w1 = c[1];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t a0 = __shfl_up_sync(0xFFFFFFFFu, w0, o), a1 = __shfl_up_sync(0xFFFFFFFFu, w1, o);
+        if (lane >= o) {
+            w0 += a0;
+            w1 += a1;
+        }
+    }
+    uint32_t o0, o1, n0, n1;
+    cta_scan2(__shfl_sync(0xFFFFFFFFu, w0, 31), __shfl_sync(0xFFFFFFFFu, w1, 31), s_w, o0, o1, n0, n1);
+    const uint32_t e[2] = {o0 + w0 - c[0], o1 + w1 - c[1]};  // keys in higher bins
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+        if (own && act[t] && e[t] < kk[t] && kk[t] <= e[t] + c[t]) {
+            const unsigned* h = t ? h1 : h0;
+            uint32_t run = e[t];
+            for (int j = 0; j < per; ++j) {
+                const int b = nb - 1 - per * tid - j;
+                if (run + h[b] >= kk[t]) {
+                    s_state[3 * t] = (uint32_t)b;
+                    s_state[3 * t + 1] = kk[t] - run;
+                    s_state[3 * t + 2] = h[b];
+                    break;
+                }
+                run += h[b];
+            }
+        }
+    }
+    *total = n0;
+    __syncthreads();
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+        if (act[t]) {
+            bin[t] = s_state[3 * t];
+            kk[t] = s_state[3 * t + 1];
+            cnt[t] = s_state[3 * t + 2];
+        }
+    }
+    __syncthreads();
+}
+
+
+// Tier choice of one CTA (the scheme above): both boundaries from the tier
+// histogram (already in s_hist[0]) and two passes over the keys, then this
+// CTA's windows [t0, t1) of the top ranks and [m0, m1) of the middle ranks
+// into s_col / s_av (top first), and the optional global lists for exactly
+// those windows. aval(i) reads a[i]. Called by every thread of the CTA.
+template <class ValF>
+__device__ __forceinline__ void tier_windows(const TieredDownParams& P, ValF aval, int t0, int t1, int m0, int m1,
+                                               int* s_col, float* s_av, unsigned (*s_hist)[kTierBins], uint2* s_w,
+                                               uint32_t* s_state) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int N = P.N, ntop = t1 - t0;
+    auto key = [&](int i) -> uint32_t { return abs_key(aval(i)); };
+    // --- the two boundaries: digits 30..20 (histogram), 19..9, 8..0
+    const int K[2] = {P.k_top, P.k_top + P.k_mid};
+    bool act[2] = {K[0] > 0 && K[0] < N, K[1] > 0 && K[1] < N};
+    uint32_t kk[2] = {(uint32_t)K[0], (uint32_t)K[1]}, d0[2] = {0u, 0u}, d1[2] = {0u, 0u}, d2[2] = {0u, 0u};
+    uint32_t eqn[2] = {0u, 0u}, total = 0u, unused = 0u;
+    find_bins2(s_hist[0], s_hist[0], kTierBins, act, kk, d0, eqn, &total, s_w, s_state);
+    const bool bad = total != (uint32_t)N;  // a histogram that does not describe a
+    if (bad) act[0] = act[1] = false;
+    const bool same1 = act[0] && act[1] && d0[0] == d0[1];
+    for (int i = tid; i < 2 * kTierBins; i += blockDim.x) (&s_hist[0][0])[i] = 0u;
+    __syncthreads();
+    // keys are read eight at a time ahead of the atomics (which the compiler
+    // cannot move loads across); 0xFFFFFFFF pads past the end and matches no bin
+    if (act[0] || act[1])
+        for (int i0 = tid; i0 < N; i0 += 8 * kDecThreads) {
+            uint32_t kv[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) kv[u] = i0 + u * kDecThreads < N ? key(i0 + u * kDecThreads) : 0xFFFFFFFFu;
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const uint32_t top = kv[u] >> kTierShift, b = (kv[u] >> 9) & 2047u;
+                if (act[0] && top == d0[0]) atomicAdd(&s_hist[0][b], 1u);
+                if (act[1] && !same1 && top == d0[1]) atomicAdd(&s_hist[1][b], 1u);
+            }
+        }
+    __syncthreads();
+    find_bins2(s_hist[0], same1 ? s_hist[0] : s_hist[1], 2048, act, kk, d1, eqn, &unused, s_w, s_state);
+    const uint32_t pre[2] = {(d0[0] << 11) | d1[0], (d0[1] << 11) | d1[1]};
+    const bool same2 = same1 && pre[0] == pre[1];
+    for (int i = tid; i < 2 * kTierBins; i += blockDim.x) (&s_hist[0][0])[i] = 0u;
+    __syncthreads();
+    if (act[0] || act[1])
+        for (int i0 = tid; i0 < N; i0 += 8 * kDecThreads) {
+            uint32_t kv[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) kv[u] = i0 + u * kDecThreads < N ? key(i0 + u * kDecThreads) : 0xFFFFFFFFu;
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const uint32_t b = kv[u] & 511u;
+                if (act[0] && (kv[u] >> 9) == pre[0]) atomicAdd(&s_hist[0][b], 1u);
+                if (act[1] && !same2 && (kv[u] >> 9) == pre[1]) atomicAdd(&s_hist[1][b], 1u);
+            }
+        }
+    __syncthreads();
+    find_bins2(s_hist[0], same2 ? s_hist[0] : s_hist[1], 512, act, kk, d2, eqn, &unused, s_w, s_state);
+    // Boundary t takes every key > thr[t] and the first take[t] keys == thr[t]
+    // in index order; K == 0 (or a bad histogram) takes nothing, K == N all.
+    uint32_t thr[2], take[2];
+    bool split = false;
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+        if (act[t]) {
+            thr[t] = (d0[t] << kTierShift) | (d1[t] << 9) | d2[t];
+            take[t] = kk[t];
+            split |= kk[t] < eqn[t];
+        } else if (K[t] <= 0 || bad) {
+            thr[t] = 0xFFFFFFFFu;  // keys are below 2^31: nothing is greater or equal
+            take[t] = 0u;
+        } else {
+            thr[t] = 0u;
+            take[t] = 0xFFFFFFFFu;
+        }
+    }
+
+    // --- members in index order; this CTA takes ranks [t0, t1) and [m0, m1).
+    // Warp w covers indices [w * SEG, (w + 1) * SEG), 32 at a time.
+    const int SEG = ((N + kTDW * 32 - 1) / (kTDW * 32)) * 32;
+    const int lo = warp * SEG, hi = min(N, lo + SEG);
+    const uint32_t lt = lanemask_lt();
+    uint32_t eqb0 = 0u, eqb1 = 0u;
+    if (split) {  // ranks among equal keys need the equal keys before each warp
+        uint32_t q0 = 0u, q1 = 0u, u0, u1;
+        for (int i0 = lo; i0 < hi; i0 += 128) {
+            uint32_t kv[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) kv[u] = i0 + 32 * u + lane < hi ? key(i0 + 32 * u + lane) : 0xFFFFFFFFu;
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const bool in = i0 + 32 * u + lane < hi;
+                q0 += __popc(__ballot_sync(0xFFFFFFFFu, in && kv[u] == thr[0]));
+                q1 += __popc(__ballot_sync(0xFFFFFFFFu, in && kv[u] == thr[1]));
+            }
+        }
+        cta_scan2(q0, q1, s_w, eqb0, eqb1, u0, u1);
+    }
+    uint32_t base0 = 0u, base1 = 0u, n0 = 0u, n1 = 0u, w0 = 0u, w1 = 0u;
+    for (int pass = 0; pass < 2; ++pass) {
+        // pass 0 counts the warp's members, pass 1 places those in this CTA's windows
+        if (pass == 1 && !(base0 < (uint32_t)t1 && base0 + w0 > (uint32_t)t0) &&
+            !(base1 < (uint32_t)m1 && base1 + w1 > (uint32_t)m0) && !(P.top_out || P.mid_out))
+            break;
+        uint32_t r0 = eqb0, r1 = eqb1, c0 = 0u, c1 = 0u;
+        for (int i4 = lo; i4 < hi; i4 += 128) {
+            uint32_t kv[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) kv[u] = i4 + 32 * u + lane < hi ? key(i4 + 32 * u + lane) : 0u;
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int i = i4 + 32 * u + lane;
+                const bool in = i < hi;
+                const uint32_t k = kv[u];
+                const uint32_t e0 = __ballot_sync(0xFFFFFFFFu, in && k == thr[0]);
+                const uint32_t e1 = __ballot_sync(0xFFFFFFFFu, in && k == thr[1]);
+                const bool sel0 = in && (k > thr[0] || (k == thr[0] && r0 + __popc(e0 & lt) < take[0]));
+                const bool sel1 = in && (k > thr[1] || (k == thr[1] && r1 + __popc(e1 & lt) < take[1]));
+                r0 += __popc(e0);
+                r1 += __popc(e1);
+                const bool is_mid = sel1 && !sel0;
+                const uint32_t bt = __ballot_sync(0xFFFFFFFFu, sel0), bm = __ballot_sync(0xFFFFFFFFu, is_mid);
+                if (pass == 1) {
+                    if (sel0) {
+                        const uint32_t r = base0 + c0 + __popc(bt & lt);
+                        if (r >= (uint32_t)t0 && r < (uint32_t)t1) {
+                            s_col[r - t0] = i;
+                            s_av[r - t0] = aval(i);
+                            if (P.top_out) P.top_out[r] = i;
+                        }
+                    }
+                    if (is_mid) {
+                        const uint32_t r = base1 + c1 + __popc(bm & lt);
+                        if (r >= (uint32_t)m0 && r < (uint32_t)m1) {
+                            s_col[ntop + r - m0] = i;
+                            s_av[ntop + r - m0] = aval(i);
+                            if (P.mid_out) P.mid_out[r] = i;
+                        }
+                    }
+                }
+                c0 += __popc(bt);
+                c1 += __popc(bm);
+            }
+        }
+        if (pass == 0) {
+            w0 = c0;
+            w1 = c1;
+            cta_scan2(c0, c1, s_w, base0, base1, n0, n1);
+        }
+    }
+    if (tid == 0 && !bad && (n0 != (uint32_t)P.k_top || n1 != (uint32_t)P.k_mid)) atomicOr(P.err, SI_DEVERR_COUNT);
+    if (tid == 0 && bad) atomicOr(P.err, SI_DEVERR_COUNT);
+}
+
+// Thresholds of both boundaries from the candidates: pass `p` (1: bits
+// 19..9, 2: bits 8..0) over the keys in cand[0, C) that share the prefix
+// found so far. Every thread of the CTA calls it.
+template <class KeyF>
+__device__ __forceinline__ void tier_refine(KeyF key, const int* cand, int C, int p, const bool* act,
+                                            const uint32_t* pre, unsigned (*s_hist)[kTierBins], uint32_t* kk,
+                                            uint32_t* dig, uint32_t* eqn, uint2* s_w, uint32_t* s_state) {
+    const int shift = p == 1 ? kTierShift : 9;   // bits above the digit: the prefix
+    const int dshift = p == 1 ? 9 : 0;
+    const uint32_t dmask = p == 1 ? 2047u : 511u;
+    const bool same = act[0] && act[1] && pre[0] == pre[1];
+    for (int i = threadIdx.x; i < 2 * kTierBins; i += blockDim.x) (&s_hist[0][0])[i] = 0u;
+    __syncthreads();
+    for (int c = threadIdx.x; c < C; c += blockDim.x) {
+        const uint32_t k = key(cand[c]), hi = k >> shift, b = (k >> dshift) & dmask;
+        if (act[0] && hi == pre[0]) atomicAdd(&s_hist[0][b], 1u);
+        if (act[1] && !same && hi == pre[1]) atomicAdd(&s_hist[1][b], 1u);
+    }
+    __syncthreads();
+    uint32_t unused;
+    find_bins2(s_hist[0], same ? s_hist[0] : s_hist[1], (int)dmask + 1, act, kk, dig, eqn, &unused, s_w, s_state);
+}
+
+// Tier choice of one CTA when a is staged in shared memory (s_a) and no
+// global lists are wanted: the CTA owns the contiguous index range
+// [n0, n1) and takes the tier members in it, top ones first, then middle
+// ones, each in index order, into s_col / s_av, with their counts in s_n.
+// Only the keys in the two boundary bins of the histogram (the candidates,
+// gathered once into cand) are needed to finish both thresholds and to
+// count the keys equal to a threshold before n0. Returns false (before
+// touching the histogram in s_hist[0]) when the candidates exceed cap; the
+// caller then takes the rank windows instead. Every thread calls it.
+__device__ bool tier_own_range(const TieredDownParams& P, const float* s_a, int* cand, int cap, int n0, int n1,
+                               int* s_col, float* s_av, unsigned (*s_hist)[kTierBins], uint2* s_w,
+                               uint32_t* s_state, int* s_n, unsigned* s_cnt) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int N = P.N;
+    auto key = [&](int i) -> uint32_t { return abs_key(s_a[i]); };
+    const int K[2] = {P.k_top, P.k_top + P.k_mid};
+    bool act[2] = {K[0] > 0 && K[0] < N, K[1] > 0 && K[1] < N};
+    uint32_t kk[2] = {(uint32_t)K[0], (uint32_t)K[1]}, d0[2] = {0u, 0u}, d1[2] = {0u, 0u}, d2[2] = {0u, 0u};
+    uint32_t eqn[2] = {0u, 0u}, total = 0u;
+    // the top digit of each boundary from the histogram (read only)
+    find_bins2(s_hist[0], s_hist[0], kTierBins, act, kk, d0, eqn, &total, s_w, s_state);
+    const bool bad = total != (uint32_t)N;  // a histogram that does not describe a
+    if (bad) act[0] = act[1] = false;
+
+    // candidates: indices of the keys in either boundary bin (any order)
+    if (tid == 0) *s_cnt = 0u;
+    __syncthreads();
+    const uint32_t lt = lanemask_lt();
+    if (act[0] || act[1])
+        for (int i4 = warp * 128; i4 < N; i4 += kTDW * 128) {
+            uint32_t tv[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) tv[u] = i4 + 32 * u + lane < N ? key(i4 + 32 * u + lane) >> kTierShift : ~0u;
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const bool m = (act[0] && tv[u] == d0[0]) || (act[1] && tv[u] == d0[1]);
+                const uint32_t bm = __ballot_sync(0xFFFFFFFFu, m);
+                if (bm) {
+                    uint32_t base = 0u;
+                    if (lane == 0) base = atomicAdd(s_cnt, (unsigned)__popc(bm));
+                    base = __shfl_sync(0xFFFFFFFFu, base, 0);
+                    const uint32_t pos = base + __popc(bm & lt);
+                    if (m && pos < (uint32_t)cap) cand[pos] = i4 + 32 * u + lane;
+                }
+            }
+        }
+    __syncthreads();
+    const int C = (int)*s_cnt;
+    if (C > cap) return false;
+
+    // both thresholds: bits 19..9, then 8..0, over the candidates
+    const uint32_t pre1[2] = {d0[0], d0[1]};
+    tier_refine(key, cand, C, 1, act, pre1, s_hist, kk, d1, eqn, s_w, s_state);
+    const uint32_t pre2[2] = {(d0[0] << 11) | d1[0], (d0[1] << 11) | d1[1]};
+    tier_refine(key, cand, C, 2, act, pre2, s_hist, kk, d2, eqn, s_w, s_state);
+    uint32_t thr[2], take[2];
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+        if (act[t]) {
+            thr[t] = (d0[t] << kTierShift) | (d1[t] << 9) | d2[t];
+            take[t] = kk[t];
+        } else if (K[t] <= 0 || bad) {
+            thr[t] = 0xFFFFFFFFu;  // keys are below 2^31: nothing is greater or equal
+            take[t] = 0u;
+        } else {
+            thr[t] = 0u;
+            take[t] = 0xFFFFFFFFu;
+        }
+    }
+
+    // keys equal to a threshold before n0: all of them are candidates
+    uint32_t e0 = 0u, e1 = 0u;
+    for (int c = tid; c < C; c += blockDim.x) {
+        const int i = cand[c];
+        if (i < n0) {
+            const uint32_t k = key(i);
+            e0 += k == thr[0];
+            e1 += k == thr[1];
+        }
+    }
+    uint32_t o0, o1, E0, E1;
+    cta_scan2(__reduce_add_sync(0xFFFFFFFFu, e0), __reduce_add_sync(0xFFFFFFFFu, e1), s_w, o0, o1, E0, E1);
+
+    // the CTA's own range, in index order: top members, then middle members
+    if (warp == 0) {
+        int ntop = 0;
+        for (int part = 0; part < 2; ++part) {
+            uint32_t r0 = E0, r1 = E1;
+            int c = 0;
+            for (int i0 = n0; i0 < n1; i0 += 32) {
+                const int i = i0 + lane;
+                const bool in = i < n1;
+                const uint32_t k = in ? key(i) : 0u;
+                const uint32_t q0 = __ballot_sync(0xFFFFFFFFu, in && k == thr[0]);
+                const uint32_t q1 = __ballot_sync(0xFFFFFFFFu, in && k == thr[1]);
+                const bool sel0 = in && (k > thr[0] || (k == thr[0] && r0 + __popc(q0 & lt) < take[0]));
+                const bool sel1 = in && (k > thr[1] || (k == thr[1] && r1 + __popc(q1 & lt) < take[1]));
+                r0 += __popc(q0);
+                r1 += __popc(q1);
+                const bool want = part == 0 ? sel0 : (sel1 && !sel0);
+                const uint32_t bw = __ballot_sync(0xFFFFFFFFu, want);
+                if (want) {
+                    const int pos = (part == 0 ? 0 : ntop) + c + __popc(bw & lt);
+                    s_col[pos] = i;
+                    s_av[pos] = s_a[i];
+                }
+                c += __popc(bw);
+            }
+            if (part == 0) ntop = c;
+            else if (lane == 0) {
+                s_n[0] = ntop;
+                s_n[1] = c;
+            }
+        }
+    }
+    if (tid == 0 && bad) atomicOr(P.err, SI_DEVERR_COUNT);
+    return true;
+}
+
+// SpAx tiered down-projection (abstract, Fig. 2; middle columns rebuilt from
+// their codes as in Fig. 3): y = sum over Top of a_n Wd[:, n] + sum over Mid
+// of a_n (min_g + q * scale_g). Each CTA takes an even share of both tier
+// lists. Record i of the CTA (its top columns first, then its middle ones)
+// goes to consumer warp i % 8 and ring stage i % R, R a multiple of 8, so a
+// stage always belongs to one warp; each warp keeps its own partial of y in
+// registers (lane l holds chunks l + 32 j of 8 columns). The partials meet
+// in shared memory at the end and the CTAs' sums are reduced through the
+// cluster and a fixed-order final pass (deterministic).
 template <int MAXC>
 __global__ void __launch_bounds__(kDecThreads, 1) k_tiered_down(TieredDownParams P) {
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -845,35 +1100,94 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_tiered_down(TieredDownParams
     float* s_av = reinterpret_cast<float*>(smem + L.off_aux);
     uint8_t* ring = smem + L.off_ring;
     const int R = L.R;
-    if (R < 1) {  // the host never launches without stages; refuse rather than divide by zero
+    // the host never launches a ring without warp-owned stages or without room
+    // for the eight warp partials and the CTA sum; refuse one
+    if (R < kConsWarps || R % kConsWarps ||
+        (long long)R * L.stage < (long long)kConsWarps * ((d + 255) / 256) * 1024 + 4LL * d) {
         if (threadIdx.x == 0) atomicOr(P.err, SI_DEVERR_COUNT);
         return;
     }
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // rank windows of the two tiers (fallback) and own index range (fast path)
     const int t0 = (int)((long long)P.k_top * blockIdx.x / gridDim.x);
     const int t1 = (int)((long long)P.k_top * (blockIdx.x + 1) / gridDim.x);
     const int m0 = (int)((long long)P.k_mid * blockIdx.x / gridDim.x);
     const int m1 = (int)((long long)P.k_mid * (blockIdx.x + 1) / gridDim.x);
-    const int ntop = t1 - t0, nrec = ntop + (m1 - m0);
+    const int n0 = (int)((long long)P.N * blockIdx.x / gridDim.x);
+    const int n1 = (int)((long long)P.N * (blockIdx.x + 1) / gridDim.x);
+    constexpr int XJ = 8 * MAXC;  // 16-byte chunks of a bf16 column per lane
+    const int nch = d / 8;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < R; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], kConsWarps);
+            mbar_init(&empty[s], 1);
         }
         fence_mbar_init();
     }
-    // the tier lists and a are the previous grids' output
+    __shared__ unsigned s_hist[2][kTierBins];
+    __shared__ uint2 s_w[kTDW];
+    __shared__ uint32_t s_state[6];
+    __shared__ unsigned s_last;
+    __shared__ __align__(8) uint64_t s_stage_bar;
+    __shared__ int s_n[2];
+    __shared__ unsigned s_cnt;
     grid_launch_dependents();
-    grid_dependency_wait();
+    grid_dependency_wait();  // a and its tier histogram are the previous grids' output
+    const int tid = threadIdx.x;
+    const int N = P.N;
     int* s_col = reinterpret_cast<int*>(s_av + P.aux_floats / 2);
-    for (int i = threadIdx.x; i < nrec; i += blockDim.x) {
-        const int col = i < ntop ? P.top[t0 + i] : P.mid[m0 + i - ntop];
-        const bool ok = col >= 0 && col < P.N;
-        s_col[i] = ok ? col : -1;
-        s_av[i] = ok ? P.a[col] : 0.0f;
+    // a is staged in the ring when it fits (the ring is idle until streaming):
+    // one bulk copy when a is 16-byte aligned and sized, else vector loads
+    float* s_a = reinterpret_cast<float*>(ring);
+    const bool staged = (long long)N * 4 <= (long long)R * L.stage;
+    const bool bulk = staged && (N % 4) == 0 && (reinterpret_cast<uintptr_t>(P.a) & 15) == 0;
+    if (bulk && tid == 0) {
+        mbar_init(&s_stage_bar, 1);
+        fence_mbar_init();
+        mbar_arrive_expect_tx(&s_stage_bar, (uint32_t)(N * 4));
+        bulk_g2s(s_a, P.a, (uint32_t)(N * 4), &s_stage_bar);
+    } else if (staged && !bulk) {
+        for (int i = tid; i < N; i += blockDim.x) s_a[i] = __ldcg(P.a + i);
     }
+    for (int i = tid; i < kTierBins; i += blockDim.x) s_hist[0][i] = __ldcg(P.hist + i);
     __syncthreads();
+    if (bulk) mbar_wait(&s_stage_bar, 0u, P.err, kSiteTiered | kSiteFullB);
+    if (tid == 0) {  // the last CTA to have read the histogram re-zeroes it at its end
+        __threadfence();
+        s_last = (atomicAdd(P.hist + kTierBins, 1u) == gridDim.x - 1) ? 1u : 0u;
+    }
+
+    // Fast path: own index range, candidates in the ring after the staged a.
+    int ntop = 0, nrec = 0;
+    bool own = false;
+    if (staged && !P.top_out && !P.mid_out) {
+        const long long off = ((long long)N * 4 + 15) / 16 * 16;
+        const long long cap = ((long long)R * L.stage - off) / 4;
+        own = tier_own_range(P, s_a, reinterpret_cast<int*>(ring + off), (int)(cap < N ? cap : N), n0, n1, s_col,
+                             s_av, s_hist, s_w, s_state, s_n, &s_cnt);
+        __syncthreads();
+        if (own) {
+            ntop = s_n[0];
+            nrec = s_n[0] + s_n[1];
+        }
+    }
+    if (!own) {
+        // Rank windows: balanced, and exact global lists; every CTA counts
+        // the members over all N. The selection reads a through one path
+        // only (a generic "shared or global" load would make the compiler
+        // issue the global load every time).
+        ntop = t1 - t0;
+        nrec = ntop + (m1 - m0);
+        for (int i = tid; i < nrec; i += blockDim.x) s_col[i] = -1;
+        if (staged)
+            tier_windows(P, [&](int i) -> float { return s_a[i]; }, t0, t1, m0, m1, s_col, s_av, s_hist, s_w,
+                         s_state);
+        else
+            tier_windows(P, [&](int i) -> float { return __ldcg(P.a + i); }, t0, t1, m0, m1, s_col, s_av, s_hist,
+                         s_w, s_state);
+    }
+    __syncthreads();  // the records are in place and the staged keys are no longer read
 
     if (warp == kConsWarps) {
         if (lane == 0) {
@@ -883,7 +1197,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_tiered_down(TieredDownParams
                 if (i >= R) mbar_wait(&empty[s], (uint32_t)((i / R - 1) & 1), P.err, kSiteTiered | kSiteEmpty);
                 uint8_t* dst = ring + (size_t)s * L.stage;
                 int ci = s_col[i];
-                if (ci < 0) {  // never read outside the encoded buffers
+                if (ci < 0 || ci >= P.N) {  // never read outside the encoded buffers
                     atomicOr(P.err, SI_DEVERR_COUNT);
                     ci = 0;
                 }
@@ -900,22 +1214,27 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_tiered_down(TieredDownParams
         }
         __syncwarp();
     } else {
-        float acc[MAXC][8];
+        // amin: the middle columns' a * min terms, equal over a chunk; kept apart
+        // only where registers allow (nine warps leave 168 per thread)
+        constexpr bool kSepMin = (MAXC == 1);
+        float acc[XJ][8], amin[XJ];
 #pragma unroll
-        for (int j = 0; j < MAXC; ++j)
+        for (int j = 0; j < XJ; ++j) {
+            amin[j] = 0.0f;
 #pragma unroll
             for (int e = 0; e < 8; ++e) acc[j][e] = 0.0f;
-        const int tid = threadIdx.x;
-        for (int i = 0; i < nrec; ++i) {
+        }
+        const int gshift = 31 - __clz(P.group);  // group is a power of two (checked by the host)
+        for (int i = warp; i < nrec; i += kConsWarps) {
             const int s = i % R;
             mbar_wait(&full[s], (uint32_t)((i / R) & 1), P.err, kSiteTiered | kSiteFull);
             const uint8_t* st = ring + (size_t)s * L.stage;
             const float av = s_av[i];
             if (i < ntop) {
 #pragma unroll
-                for (int j = 0; j < MAXC; ++j) {
-                    const int c = tid + kConsThreads * j;
-                    if (c < d / 8) {
+                for (int j = 0; j < XJ; ++j) {
+                    const int c = lane + 32 * j;
+                    if (c < nch) {
                         float f[8];
                         unpack8(reinterpret_cast<const uint4*>(st)[c], f);
 #pragma unroll
@@ -925,35 +1244,86 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_tiered_down(TieredDownParams
             } else {
                 const float2* prm = reinterpret_cast<const float2*>(st + d / 2);
 #pragma unroll
-                for (int j = 0; j < MAXC; ++j) {
-                    const int c = tid + kConsThreads * j;
-                    if (c < d / 8) {
+                for (int j = 0; j < XJ; ++j) {
+                    const int c = lane + 32 * j;
+                    if (c < nch) {
                         const uint32_t q = reinterpret_cast<const uint32_t*>(st)[c];
-                        const float2 sm = prm[(8 * c) / P.group];  // (scale, min)
+                        const float2 sm = prm[(8 * c) >> gshift];  // (scale, min)
                         const float c1 = av * sm.x, c0 = av * sm.y;
-#pragma unroll
-                        for (int e = 0; e < 8; ++e)
-                            acc[j][e] += fmaf(c1, (float)((q >> (4 * e)) & 15u), c0);
+                        if constexpr (kSepMin) amin[j] += c0;
+                        // acc += c1 * code (+ c0 unless it is kept apart)
+                        auto mac = [&](float& acc_e, uint32_t word) {
+                            const float qf = __uint_as_float(word) - 8388608.0f;
+                            if constexpr (kSepMin) acc_e = fmaf(c1, qf, acc_e);
+                            else acc_e = fmaf(c1, qf, acc_e + c0);
+                        };
+                        // codes of elements 0,2,4,6 (low nibbles) and 1,3,5,7 (high
+                        // nibbles) as bytes; byte -> float exactly as the float
+                        // 2^23 + code minus 2^23
+                        const uint32_t lo = q & 0x0F0F0F0Fu, hi = (q >> 4) & 0x0F0F0F0Fu;
+                        mac(acc[j][0], __byte_perm(lo, 0x4B000000u, 0x7440));
+                        mac(acc[j][1], __byte_perm(hi, 0x4B000000u, 0x7440));
+                        mac(acc[j][2], __byte_perm(lo, 0x4B000000u, 0x7441));
+                        mac(acc[j][3], __byte_perm(hi, 0x4B000000u, 0x7441));
+                        mac(acc[j][4], __byte_perm(lo, 0x4B000000u, 0x7442));
+                        mac(acc[j][5], __byte_perm(hi, 0x4B000000u, 0x7442));
+                        mac(acc[j][6], __byte_perm(lo, 0x4B000000u, 0x7443));
+                        mac(acc[j][7], __byte_perm(hi, 0x4B000000u, 0x7443));
                     }
                 }
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[s]);
         }
+        // All records consumed: warp w's partial goes to ring region w
+        // (round_up(d, 256) floats; for chunk j the lanes' first halves, then
+        // their second halves, so the stores are bank-conflict free), then
+        // each thread sums the eight partials of its float4 columns.
+        const int wstride = ((d + 255) / 256) * 64;  // float4s per warp region
         named_bar_sync(1, kConsThreads);
-        float* ypart = reinterpret_cast<float*>(ring);
+        float4* wst = reinterpret_cast<float4*>(ring) + (size_t)warp * wstride;
 #pragma unroll
-        for (int j = 0; j < MAXC; ++j) {
-            const int c = tid + kConsThreads * j;
-            if (c < d / 8) {
-                float4* dst = reinterpret_cast<float4*>(ypart + c * 8);
-                dst[0] = make_float4(acc[j][0], acc[j][1], acc[j][2], acc[j][3]);
-                dst[1] = make_float4(acc[j][4], acc[j][5], acc[j][6], acc[j][7]);
+        for (int j = 0; j < XJ; ++j) {
+            if constexpr (kSepMin)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc[j][e] += amin[j];
+            if (32 * j < nch) {
+                wst[j * 64 + lane] = make_float4(acc[j][0], acc[j][1], acc[j][2], acc[j][3]);
+                wst[j * 64 + 32 + lane] = make_float4(acc[j][4], acc[j][5], acc[j][6], acc[j][7]);
             }
+        }
+        named_bar_sync(1, kConsThreads);
+        float4* part4 = reinterpret_cast<float4*>(ring);
+        float4 v[2 * MAXC];
+        constexpr int KV = 2 * MAXC;  // float4 columns per consumer thread
+#pragma unroll
+        for (int t = 0; t < KV; ++t) {
+            const int k = threadIdx.x + t * kConsThreads;
+            v[t] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (k < d / 4) {
+                const int c = k >> 1, off = (c >> 5) * 64 + (k & 1) * 32 + (c & 31);
+#pragma unroll
+                for (int w = 0; w < kConsWarps; ++w) {
+                    const float4 u = part4[(size_t)w * wstride + off];
+                    v[t].x += u.x; v[t].y += u.y; v[t].z += u.z; v[t].w += u.w;
+                }
+            }
+        }
+        // the CTA sum goes to the tail of the ring, past the eight regions
+        float4* ysum = reinterpret_cast<float4*>(ring + (size_t)R * L.stage) - d / 4;
+#pragma unroll
+        for (int t = 0; t < KV; ++t) {
+            const int k = threadIdx.x + t * kConsThreads;
+            if (k < d / 4) ysum[k] = v[t];
         }
     }
     __syncthreads();
-    cluster_ticket_reduce4(reinterpret_cast<float*>(ring), d, P.part, P.tickets, P.y);
+    const float* ycta = reinterpret_cast<const float*>(ring + (size_t)R * L.stage) - d;
+    cluster_ticket_reduce4(ycta, d, P.part, P.tickets, P.y);
+    if (s_last) {
+        for (int i = threadIdx.x; i < kTierBins; i += blockDim.x) P.hist[i] = 0u;
+        if (threadIdx.x == 0) P.hist[kTierBins] = 0u;
+    }
 }
 
 // ------------------------------------------------------------------ launch
@@ -1101,62 +1471,6 @@ cudaError_t launch_sd1(SparseDecodeParams& P, cudaStream_t st) {
 
 }  // namespace
 
-cudaError_t launch_repack_down(const uint16_t* packed, int d, const int32_t* pos, int n, int np, uint16_t* Wp,
-                               cudaStream_t st) {
-    dim3 grid((np + 31) / 32, (d + 31) / 32);
-    k_repack_down<<<grid, 256, 0, st>>>(packed, d, pos, n, np, Wp);
-    return cudaGetLastError();
-}
-
-// Small rings so that the down kernel's CTAs fit beside this kernel's on an SM.
-int plan_act_stages(int d) {
-    const int stage = round_up(4 * d, 128);
-    int R = (80 * 1024) / stage;
-    R = (R / kConsWarps) * kConsWarps;
-    return R < kConsWarps ? kConsWarps : R;
-}
-
-cudaError_t launch_plan_act(PlanActParams P, cudaStream_t st) {
-    int dev = 0, sms = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-    const size_t smem = (size_t)ring_layout(P.R, 4 * P.d, 0, 0).total;
-    const int grid = P.n < sms ? (P.n > 0 ? P.n : 1) : sms;
-    void* args[] = {&P};
-    if (P.d > 2048) {
-        if ((e = allow_max_smem(k_plan_act<2>)) != cudaSuccess) return e;
-        return launch_clustered(k_plan_act<2>, grid, 1, smem, st, args, true);
-    }
-    if ((e = allow_max_smem(k_plan_act<1>)) != cudaSuccess) return e;
-    return launch_clustered(k_plan_act<1>, grid, 1, smem, st, args, true);
-}
-
-int plan_down_rows(int d, int np) {
-    // rows per CTA: enough CTAs to cover the SMs about twice, rows buffer <= 96 KB
-    int rows = 8;
-    while (rows > 1 && (size_t)rows * np * 2 > 96 * 1024) rows /= 2;
-    (void)d;
-    return rows;
-}
-
-cudaError_t launch_plan_down(PlanDownParams P, cudaStream_t st) {
-    cudaError_t e = allow_max_smem(k_plan_down);
-    if (e != cudaSuccess) return e;
-    const size_t smem = 128 + (size_t)round_up(P.np * 4, 128) + (size_t)P.rows * P.np * 2;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((P.d + P.rows - 1) / P.rows, 1, 1);
-    cfg.blockDim = dim3(256, 1, 1);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    void* args[] = {&P};
-    return cudaLaunchKernelExC(&cfg, reinterpret_cast<const void*>(k_plan_down), args);
-}
 
 int sparse_decode_stages(int d, int B) {
     const int fixed = ring_layout(0, 6 * d, 2 * kConsWarps * B * 4, B * d * 2).total;
@@ -1241,10 +1555,20 @@ cudaError_t launch_dense_act(DenseActParams P, cudaStream_t st) {
     return launch_clustered(k_dense_act<1>, grid, 1, smem, st, args, /*pdl=*/true);
 }
 
+// Stages of the tiered ring: a multiple of the consumer-warp count (each
+// stage belongs to one warp), and enough ring for the eight warp partials
+// (round_up(d, 256) floats each) plus the CTA sum (d floats) at its tail.
 int tiered_down_stages(int d, int aux_floats) {
-    const int fixed = ring_layout(0, 2 * d, aux_floats * 4, 0).total;
-    int R = (kSmemBudget - fixed - 256) / round_up(2 * d, 128);
-    return R > 32 ? 32 : R;
+    // the kernel's static shared memory (tier histograms, reduction scratch)
+    // takes about 21 KB of the 227 KB
+    constexpr int kTieredBudget = 227 * 1024 - 24 * 1024;
+    const int stage = round_up(2 * d, 128);
+    const long long need = (long long)kConsWarps * round_up(d, 256) * 4 + 4LL * d;
+    int R = (int)((need + stage - 1) / stage);  // at least the tail's bytes
+    if (R < 32) R = 32;                           // up to 32 stages of look-ahead
+    R = ((R + kConsWarps - 1) / kConsWarps) * kConsWarps;
+    while (R >= kConsWarps && ring_layout(R, 2 * d, aux_floats * 4, 0).total > kTieredBudget) R -= kConsWarps;
+    return (R >= kConsWarps && (long long)R * stage >= need) ? R : 0;
 }
 
 cudaError_t launch_tiered_down(TieredDownParams P, cudaStream_t st) {
@@ -1258,13 +1582,36 @@ cudaError_t launch_tiered_down(TieredDownParams P, cudaStream_t st) {
     }
     if (e != cudaSuccess) return e;
     if (P.part_floats < (long long)(grid / cluster) * P.d) return cudaErrorInvalidValue;
-    // per-CTA record counts must fit the activation buffer
-    // (activations in the first half of the buffer, columns in the second)
-    const long long per = (long long)(P.k_top + grid - 1) / grid + (P.k_mid + grid - 1) / grid;
+    // per-CTA record counts (rank windows, or an own range of N / grid
+    // columns) must fit the activation buffer (activations in the first half
+    // of the buffer, columns in the second)
+    long long per = (long long)(P.k_top + grid - 1) / grid + (P.k_mid + grid - 1) / grid;
+    const long long own = ((long long)P.N + grid - 1) / grid;
+    if (own > per) per = own;
     if (2 * per > P.aux_floats) return cudaErrorInvalidValue;
     void* args[] = {&P};
     if (P.d > 2048) return launch_clustered(k_tiered_down<2>, grid, cluster, smem, st, args, /*pdl=*/true);
     return launch_clustered(k_tiered_down<1>, grid, cluster, smem, st, args, /*pdl=*/true);
+}
+
+cudaError_t launch_abs_hist(const float* a, int N, unsigned* hist, cudaStream_t st) {
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    int grid = (N + 2047) / 2048;
+    if (grid > sms) grid = sms;
+    if (grid < 1) grid = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.blockDim = dim3(256, 1, 1);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k_abs_hist, a, N, hist);
 }
 
 int streaming_grid_upper_bound() {

@@ -29,33 +29,12 @@ struct SparseDecodeParams {
     int accumulate;           // 1: y += result with float atomics (no cross-CTA ordering)
 };
 
-// Planned batch-1 decode, split in two kernels that need no cross-CTA sum:
-// plan_act computes a[i] for the plan's records (gate/up rows), plan_down
-// computes each output row from the plan's row-major down matrix.
-struct PlanActParams {
-    const uint16_t* packed;   // [n_pad][3][d] bf16 records
-    int n_records;
-    int d;
-    const int32_t* pos;       // plan positions [n]
-    int n;
-    const uint16_t* x;        // [d]
-    float* a;                 // [n] out
-    unsigned* err;
-    int R;
-    int stable_plan;
-};
 
-struct PlanDownParams {
-    const uint16_t* Wp;       // [d][np] bf16, row j = down weights of the plan's records
-    int np;                   // row length (plan count rounded up to 8; pad weights are zero)
-    int d;
-    int rows;                 // rows per CTA
-    const float* a;           // [np] (pad entries zero)
-    float* y;                 // [d]
-    unsigned* err;
-    int stable_plan;
-    int accumulate;           // 1: y += result (each row has one writer, so still deterministic)
-};
+// Tier histogram: bin b counts the neurons whose |a| key (the float's bits
+// with the sign cleared) has bits 30..20 equal to b; word kTierBins is the
+// ticket of the CTAs that have read it (the last one re-zeroes everything).
+constexpr int kTierBins = 2048;
+constexpr int kTierShift = 20;
 
 struct DenseActParams {
     const uint16_t* Wg;
@@ -63,6 +42,7 @@ struct DenseActParams {
     int d, N;
     const uint16_t* x;
     float* a;
+    unsigned* hist;           // optional tier histogram of a (kTierBins + 1 words, zero on entry)
     unsigned* err;
     int R;
 };
@@ -72,10 +52,11 @@ struct TieredDownParams {
     const uint8_t* codes;     // [N][d/2]
     const float* params;      // [N][ngp][2]
     const float* a;           // [N]
-    const int32_t* top;       // [k_top]
-    const int32_t* mid;       // [k_mid]
+    unsigned* hist;           // tier histogram of a (kTierBins + 1 words), re-zeroed by the kernel
+    int32_t* top_out;         // optional [k_top]: the top tier, ascending
+    int32_t* mid_out;         // optional [k_mid]: the middle tier, ascending
     int d, group, ngp, k_top, k_mid;
-    int N;                    // columns (indices must be below it)
+    int N;                    // columns
     float* y;                 // [d]
     float* part;
     long long part_floats;
@@ -94,8 +75,6 @@ cudaError_t launch_rank_loaded(const float* task, const float* model, int N, int
                                int32_t* loaded, uint8_t* is_static, unsigned* err, cudaStream_t st);
 cudaError_t launch_decode_plan(const int32_t* S, int n_sel, int B, int n, int32_t* pos, uint32_t* pmask,
                                int* count, unsigned* err, cudaStream_t st);
-cudaError_t launch_spax_tiers(const float* a, int N, int k_top, int k_mid, int32_t* top, int32_t* mid,
-                              unsigned* err, cudaStream_t st);
 cudaError_t launch_merge_scores(const float* const* s, const float* tok, int nfiles, int N, float* out,
                                 cudaStream_t st);
 
@@ -110,17 +89,12 @@ void set_error_message(const char* msg);
 
 // decode.cu
 int sparse_decode_b1_stages(int d);
-cudaError_t launch_repack_down(const uint16_t* packed, int d, const int32_t* pos, int n, int np, uint16_t* Wp,
-                               cudaStream_t st);
-int plan_act_stages(int d);
-cudaError_t launch_plan_act(PlanActParams P, cudaStream_t st);
-int plan_down_rows(int d, int np);
-cudaError_t launch_plan_down(PlanDownParams P, cudaStream_t st);
 int sparse_decode_stages(int d, int B);
 int decode_max_partial_floats(int d, int B);
 cudaError_t launch_sparse_decode(SparseDecodeParams P, int B, cudaStream_t st);
 int dense_act_stages(int d);
 cudaError_t launch_dense_act(DenseActParams P, cudaStream_t st);
+cudaError_t launch_abs_hist(const float* a, int N, unsigned* hist, cudaStream_t st);
 int tiered_down_stages(int d, int aux_floats);
 cudaError_t launch_tiered_down(TieredDownParams P, cudaStream_t st);
 int streaming_grid_upper_bound();

@@ -2,9 +2,9 @@
 //
 // Every ranking of the method is "the k largest by a key, ties to the lower
 // index": per-token top-alpha of |a| and top-beta of counts (SelectInfer
-// section 5, Fig. 7), base/secondary neurons by profiler score (section 4,
-// Fig. 6), and the SpAx tiers by |a| (abstract, Fig. 2). All of them use one
-// block-wide primitive:
+// section 5, Fig. 7) and base/secondary neurons by profiler score (section 4,
+// Fig. 6). All of them use one block-wide primitive (the SpAx tiers are
+// selected inside the tiered down-projection kernel, decode.cu):
 //   block_topk_cut   4 passes of an 8-bit radix histogram over 32-bit
 //                    order-preserving keys find the k-th largest key `thr`
 //                    and how many elements equal to it are still needed;
@@ -291,202 +291,6 @@ __global__ void __launch_bounds__(1024) k_decode_plan(const int32_t* __restrict_
     if (threadIdx.x == 0) *count = total;
 }
 
-// a9: the SpAx tiers of one token (abstract, Fig. 2): Top = the k_top
-// largest |a|, Mid = the next k_mid, ties to the lower index; both lists in
-// ascending index order. Both rank boundaries (k_top and k_top + k_mid) are
-// found in one joint radix select: three passes over the 31-bit |a| key
-// (digits of 11, 11 and 9 bits), each pass building one histogram per
-// boundary with shared-memory atomics. A warp-segmented, index-ordered
-// compaction then writes the lists; the rank among equal keys is counted
-// only when a boundary splits a run of equal keys.
-constexpr int kTierNT = 1024;
-constexpr int kTierNW = kTierNT / 32;
-
-// Exclusive scan over the warps of the block of two counts per warp (given by
-// lane 0 of each warp); returns the warp's offsets and the block totals.
-__device__ __forceinline__ void warp_offsets2(uint32_t c0, uint32_t c1, uint2* s_w, uint32_t* off0,
-                                              uint32_t* off1, uint32_t* tot0, uint32_t* tot1) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    if (lane == 0) s_w[warp] = make_uint2(c0, c1);
-    __syncthreads();
-    const uint2 v = lane < kTierNW ? s_w[lane] : make_uint2(0u, 0u);
-    uint32_t i0 = v.x, i1 = v.y;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t a0 = __shfl_up_sync(0xFFFFFFFFu, i0, o), a1 = __shfl_up_sync(0xFFFFFFFFu, i1, o);
-        if (lane >= o) {
-            i0 += a0;
-            i1 += a1;
-        }
-    }
-    *off0 = __shfl_sync(0xFFFFFFFFu, i0 - v.x, warp);
-    *off1 = __shfl_sync(0xFFFFFFFFu, i1 - v.y, warp);
-    *tot0 = __shfl_sync(0xFFFFFFFFu, i0, 31);
-    *tot1 = __shfl_sync(0xFFFFFFFFu, i1, 31);
-    __syncthreads();  // s_w may be reused
-}
-
-__global__ void __launch_bounds__(kTierNT) k_spax_tiers(const float* __restrict__ a, int N, int k_top, int k_mid,
-                                                       int32_t* __restrict__ top, int32_t* __restrict__ mid,
-                                                       unsigned* err) {
-    extern __shared__ __align__(16) uint32_t s_keys[];  // N keys
-    __shared__ uint32_t hist[2][2048];
-    __shared__ uint32_t s_state[2][3];                 // per boundary: digit, rank left, bin count
-    __shared__ uint2 s_w[kTierNW];
-    grid_launch_dependents();
-    grid_dependency_wait();  // a is written by the previous kernel in the stream
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    if ((N & 3) == 0 && (reinterpret_cast<uintptr_t>(a) & 15) == 0) {
-        const float4* a4 = reinterpret_cast<const float4*>(a);
-        uint4* k4 = reinterpret_cast<uint4*>(s_keys);
-        for (int i = tid; i < N / 4; i += kTierNT) {
-            const float4 v = __ldcg(a4 + i);
-            k4[i] = make_uint4(abs_key(v.x), abs_key(v.y), abs_key(v.z), abs_key(v.w));
-        }
-    } else {
-        for (int i = tid; i < N; i += kTierNT) s_keys[i] = abs_key(__ldcg(a + i));
-    }
-    // boundary t selects the K[t] largest keys; K[1] >= K[0]
-    const int K[2] = {k_top, k_top + k_mid};
-    uint32_t prefix[2] = {0u, 0u}, pmask[2] = {0u, 0u}, kk[2] = {(uint32_t)K[0], (uint32_t)K[1]};
-    uint32_t eqn[2] = {0u, 0u};
-    const bool act[2] = {K[0] > 0 && K[0] < N, K[1] > 0 && K[1] < N};
-    constexpr int kShift[3] = {20, 9, 0}, kBits[3] = {11, 11, 9};
-#pragma unroll
-    for (int p = 0; p < 3; ++p) {
-        const int shift = kShift[p], nb = 1 << kBits[p];
-        for (int i = tid; i < 2 * 2048; i += kTierNT) (&hist[0][0])[i] = 0u;
-        __syncthreads();
-        for (int i = tid; i < N; i += kTierNT) {
-            const uint32_t k = s_keys[i];
-            const uint32_t bin = (k >> shift) & (uint32_t)(nb - 1);
-            if (act[0] && (k & pmask[0]) == prefix[0]) atomicAdd(&hist[0][bin], 1u);
-            if (act[1] && (k & pmask[1]) == prefix[1]) atomicAdd(&hist[1][bin], 1u);
-        }
-        __syncthreads();
-        // thread t owns `per` bins, highest first: bins nb-1-per*t ... nb-per*(t+1)
-        const int per = nb >= kTierNT ? nb / kTierNT : 1;
-        const bool owner = tid * per < nb;
-        uint32_t c0 = 0u, c1 = 0u;
-        if (owner)
-            for (int j = 0; j < per; ++j) {
-                c0 += hist[0][nb - 1 - per * tid - j];
-                c1 += hist[1][nb - 1 - per * tid - j];
-            }
-        // per-warp sums, then offsets across warps: counts in higher bins
-        uint32_t w0 = c0, w1 = c1;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const uint32_t a0 = __shfl_up_sync(0xFFFFFFFFu, w0, o), a1 = __shfl_up_sync(0xFFFFFFFFu, w1, o);
-            if (lane >= o) {
-                w0 += a0;
-                w1 += a1;
-            }
-        }
-        uint32_t o0, o1, t0, t1;
-        warp_offsets2(__shfl_sync(0xFFFFFFFFu, w0, 31), __shfl_sync(0xFFFFFFFFu, w1, 31), s_w, &o0, &o1, &t0, &t1);
-        const uint32_t e[2] = {o0 + w0 - c0, o1 + w1 - c1};  // keys of this prefix in higher bins
-        const uint32_t c[2] = {c0, c1};
-#pragma unroll
-        for (int t = 0; t < 2; ++t) {
-            if (owner && act[t] && e[t] < kk[t] && kk[t] <= e[t] + c[t]) {
-                uint32_t run = e[t];
-                for (int j = 0; j < per; ++j) {
-                    const int b = nb - 1 - per * tid - j;
-                    const uint32_t h = hist[t][b];
-                    if (run + h >= kk[t]) {
-                        s_state[t][0] = (uint32_t)b;
-                        s_state[t][1] = kk[t] - run;
-                        s_state[t][2] = h;
-                        break;
-                    }
-                    run += h;
-                }
-            }
-        }
-        __syncthreads();
-#pragma unroll
-        for (int t = 0; t < 2; ++t) {
-            if (act[t]) {
-                prefix[t] |= s_state[t][0] << shift;
-                pmask[t] |= (uint32_t)(nb - 1) << shift;
-                kk[t] = s_state[t][1];
-                eqn[t] = s_state[t][2];
-            }
-        }
-        __syncthreads();
-    }
-    // Boundary t takes every key > thr[t] and the first take[t] keys == thr[t]
-    // in index order. K == 0 takes nothing; K == N takes everything.
-    uint32_t thr[2];
-    int take[2];
-    bool split[2];
-#pragma unroll
-    for (int t = 0; t < 2; ++t) {
-        if (act[t]) {
-            thr[t] = prefix[t];
-            take[t] = (int)kk[t];
-            split[t] = kk[t] < eqn[t];
-        } else if (K[t] <= 0) {
-            thr[t] = 0xFFFFFFFFu;  // keys are below 2^31: nothing is greater or equal
-            take[t] = 0;
-            split[t] = false;
-        } else {
-            thr[t] = 0u;
-            take[t] = INT_MAX;
-            split[t] = false;
-        }
-    }
-    // Warp w covers indices [w*SEG, (w+1)*SEG), read 32 at a time in index order.
-    const int SEG = ((N + kTierNW * 32 - 1) / (kTierNW * 32)) * 32;
-    const int lo = warp * SEG, hi = min(N, lo + SEG);
-    uint32_t eqb0 = 0u, eqb1 = 0u;
-    if (split[0] || split[1]) {
-        uint32_t q0 = 0u, q1 = 0u;
-        for (int i0 = lo; i0 < hi; i0 += 32) {
-            const int i = i0 + lane;
-            const uint32_t k = i < hi ? s_keys[i] : 0xFFFFFFFFu;
-            q0 += __popc(__ballot_sync(0xFFFFFFFFu, i < hi && k == thr[0]));
-            q1 += __popc(__ballot_sync(0xFFFFFFFFu, i < hi && k == thr[1]));
-        }
-        uint32_t d0, d1;
-        warp_offsets2(q0, q1, s_w, &eqb0, &eqb1, &d0, &d1);
-    }
-    const uint32_t lt = lanemask_lt();
-    // pass 1 counts the warp's top and mid members, pass 2 writes them
-    uint32_t base0 = 0u, base1 = 0u, n0 = 0u, n1 = 0u;
-    for (int pass = 0; pass < 2; ++pass) {
-        uint32_t r0 = eqb0, r1 = eqb1, s0 = 0u, s1 = 0u;
-        for (int i0 = lo; i0 < hi; i0 += 32) {
-            const int i = i0 + lane;
-            const bool in = i < hi;
-            const uint32_t k = in ? s_keys[i] : 0u;
-            const uint32_t m0 = __ballot_sync(0xFFFFFFFFu, in && k == thr[0]);
-            const uint32_t m1 = __ballot_sync(0xFFFFFFFFu, in && k == thr[1]);
-            const bool sel0 = in && (k > thr[0] || (k == thr[0] && (int)(r0 + __popc(m0 & lt)) < take[0]));
-            const bool sel1 = in && (k > thr[1] || (k == thr[1] && (int)(r1 + __popc(m1 & lt)) < take[1]));
-            r0 += __popc(m0);
-            r1 += __popc(m1);
-            const bool is_mid = sel1 && !sel0;
-            const uint32_t b0 = __ballot_sync(0xFFFFFFFFu, sel0), b1 = __ballot_sync(0xFFFFFFFFu, is_mid);
-            if (pass == 1) {
-                if (sel0) {
-                    const uint32_t r = base0 + s0 + __popc(b0 & lt);
-                    if (r < (uint32_t)k_top) top[r] = i;
-                }
-                if (is_mid) {
-                    const uint32_t r = base1 + s1 + __popc(b1 & lt);
-                    if (r < (uint32_t)k_mid) mid[r] = i;
-                }
-            }
-            s0 += __popc(b0);
-            s1 += __popc(b1);
-        }
-        if (pass == 0) warp_offsets2(s0, s1, s_w, &base0, &base1, &n0, &n1);
-    }
-    if (tid == 0 && (n0 != (uint32_t)k_top || n1 != (uint32_t)k_mid)) atomicOr(err, SI_DEVERR_COUNT);
-}
-
 // Score-file merge (SelectInfer section 3): out[n] = sum_f s_f[n] / T_f in
 // float32, files in order, each step rounded (no contraction).
 struct MergeArgs {
@@ -539,24 +343,6 @@ cudaError_t launch_decode_plan(const int32_t* S, int n_sel, int B, int n, int32_
     if (e != cudaSuccess) return e;
     k_decode_plan<<<1, 1024, smem, st>>>(S, n_sel, B, n, pos, pmask, count, err);
     return cudaGetLastError();
-}
-
-cudaError_t launch_spax_tiers(const float* a, int N, int k_top, int k_mid, int32_t* top, int32_t* mid,
-                              unsigned* err, cudaStream_t st) {
-    const size_t smem = (size_t)((N + 3) & ~3) * 4;
-    cudaError_t e = allow_max_smem(k_spax_tiers);
-    if (e != cudaSuccess) return e;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(1, 1, 1);
-    cfg.blockDim = dim3(kTierNT, 1, 1);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, k_spax_tiers, a, N, k_top, k_mid, top, mid, err);
 }
 
 cudaError_t launch_merge_scores(const float* const* s, const float* tok, int nfiles, int N, float* out,

@@ -199,9 +199,10 @@ int si_decode_plan(si_layer *layer, const int32_t *S, int n_sel, int B, void *st
  * neurons are computed at decode):
  *   y[b, :] = sum over p in S[b] of a_{loaded[p]}(x_b) * Wd[:, loaded[p]].
  * Reads only the selected packed records (gate row, up row, down column) with
- * bulk copies, reduces over neurons inside the kernel (split over neurons
- * across the SMs, cluster shared-memory reduction, then a fixed-order
- * cross-cluster sum, so results are deterministic).
+ * bulk copies and reduces over neurons inside the kernel, split over neurons
+ * across the SMs. For B == 1 the CTA partials are summed exactly in 64-bit
+ * fixed point (2^-32 resolution); for B > 1 through cluster shared memory and
+ * then in a fixed cross-cluster order. Either way results are deterministic.
  *   S int32 [B x n_sel] ascending positions (as written by the selection
  *   calls); x bf16 [B x d]; y fp32 [B x d] (overwritten).
  * For B > 1, si_decode_plan(layer, S, n_sel, B) must have been called with
@@ -255,7 +256,8 @@ int si_sparse_ffn_decode_noalloc(const uint16_t *packed, int n_records, int d, c
  * 2i in the low nibble for bits = 4) and fp32 (scale, min) pairs
  * [N][ng_pad][2], ng_pad = d/group rounded up to even.
  *   Wd bf16 [d x N]. Synchronous (allocates, enqueues, waits).
- * Requires bits == 4, group % 8 == 0, d % group == 0, d % 64 == 0. */
+ * Requires bits == 4, group a power of two >= 8 dividing d, d % 64 == 0,
+ * d <= 4096. */
 int spax_encode(const uint16_t *Wd, int d, int N, int bits, int group, spax_layer **out,
                 void *stream);
 
@@ -281,13 +283,17 @@ int spax_dense_act(const uint16_t *Wg, const uint16_t *Wu, int d, int N, const u
  * bf16, the next k_mid = si_count(mid_frac, N) are rebuilt from their codes,
  * the rest skipped (ranking by |a| descending, ties to the lower index):
  *   y = sum_{n in top} a[n] Wd[:, n] + sum_{n in mid} a[n] w^_n.
- *   a fp32 [N] (finite); y fp32 [d] (overwritten); top_idx / mid_idx
- *   (optional, may be NULL) int32 [k_top] / [k_mid] receive the tier lists in
- *   ascending column order. Requires top_frac + mid_frac <= 1. */
+ *   a fp32 [N] (finite); y fp32 [d] (overwritten, deterministic); top_idx /
+ *   mid_idx (optional, may be NULL) int32 [k_top] / [k_mid] receive the tier
+ *   lists in ascending column order. Requires top_frac + mid_frac <= 1.
+ * The tiers are chosen inside the down-projection kernel from a histogram of
+ * |a| that this call builds first; spax_ffn_decode gets that histogram from
+ * its dense pass instead. Calls on one handle go on one stream. */
 int spax_tiered_down(spax_layer *layer, const float *a, double top_frac, double mid_frac,
                      float *y, int32_t *top_idx, int32_t *mid_idx, void *stream);
 
-/* One SpAx decode token: spax_dense_act, then spax_tiered_down on its a.
+/* One SpAx decode token: spax_dense_act, then spax_tiered_down on its a
+ * (two kernels: the dense pass also counts the tier histogram).
  * a_out (optional) fp32 [N] receives the activations. */
 int spax_ffn_decode(spax_layer *layer, const uint16_t *Wg, const uint16_t *Wu,
                     const uint16_t *x, double top_frac, double mid_frac, float *y,

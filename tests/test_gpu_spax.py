@@ -77,10 +77,35 @@ def test_spax_tiers_and_down(si, N, top, mid, ties):
     codes, params = oracle.spax_encode(Wd, 4, 128)
     ref = oracle.spax_down(a, Wd, codes, params, rt, rm)
     got = y.numpy()
+    # without the lists each CTA takes the tier members of its own index range
+    y2 = Guarded((d,), torch().float32, fill=float("nan"))
+    si.spax_tiered_down(layer, dev(a), top, mid, y2.t)
+    got2 = y2.numpy()
     if k_top + k_mid == 0:
-        assert np.all(got == 0)
+        assert np.all(got == 0) and np.all(got2 == 0)
     else:
         assert rel_err(got, ref) <= 2e-5
+        assert rel_err(got2, ref) <= 2e-5
+    layer.close()
+
+
+@pytest.mark.parametrize("d,N,equal", [(256, 8192, False), (2048, 32768, True)])
+def test_spax_tiered_down_fallbacks(si, d, N, equal):
+    """a too long to stage beside a small ring (d = 256), and more keys in the
+    boundary bins than the candidate space (all |a| equal): the per-CTA rank
+    windows give the same tiers."""
+    _, _, Wd = synth.layer_weights(56, 0, d, N)
+    layer = si.spax_encode(dev_bf16(Wd), 4, 128)
+    a = signed_acts(57, N, True)
+    if equal:
+        a = np.where(a < 0, -1.0, 1.0).astype(np.float32)
+    k_top, k_mid = si.si_count(0.3, N), si.si_count(0.3, N)
+    rt, rm = oracle.spax_tiers(a, k_top, k_mid)
+    codes, params = oracle.spax_encode(Wd, 4, 128)
+    ref = oracle.spax_down(a, Wd, codes, params, rt, rm)
+    y = Guarded((d,), torch().float32, fill=float("nan"))
+    si.spax_tiered_down(layer, dev(a), 0.3, 0.3, y.t)
+    assert rel_err(y.numpy(), ref) <= 2e-5
     layer.close()
 
 
