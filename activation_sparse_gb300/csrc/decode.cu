@@ -972,7 +972,7 @@ __device__ __forceinline__ void tier_refine(KeyF key, const int* cand, int C, in
 // caller then takes the rank windows instead. Every thread calls it.
 __device__ bool tier_own_range(const TieredDownParams& P, const float* s_a, int* cand, int cap, int n0, int n1,
                                int* s_col, float* s_av, unsigned (*s_hist)[kTierBins], uint2* s_w,
-                               uint32_t* s_state, int* s_n, unsigned* s_cnt) {
+                               uint32_t* s_state, int* s_n) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int N = P.N;
     auto key = [&](int i) -> uint32_t { return abs_key(s_a[i]); };
@@ -985,37 +985,55 @@ __device__ bool tier_own_range(const TieredDownParams& P, const float* s_a, int*
     const bool bad = total != (uint32_t)N;  // a histogram that does not describe a
     if (bad) act[0] = act[1] = false;
 
-    // candidates: indices of the keys in either boundary bin (any order)
-    if (tid == 0) *s_cnt = 0u;
-    __syncthreads();
+    // candidates: indices of the keys in either boundary bin, in index order.
+    // Each lane owns a contiguous run of LQ quads (four consecutive keys, one
+    // 16-byte read each); the lanes' runs tile the warps' runs in order. Pass
+    // 0 counts per lane (no cross-lane work in the loop), one scan gives each
+    // lane its first slot, pass 1 writes.
     const uint32_t lt = lanemask_lt();
-    if (act[0] || act[1])
-        for (int i4 = warp * 128; i4 < N; i4 += kTDW * 128) {
-            uint32_t tv[4];
+    const int NQ = (N + 3) / 4;
+    const int LQ = ((NQ + kTDW * 32 - 1) / (kTDW * 32)) | 1;  // odd: spreads the lanes over the banks
+    const int q_lo = (warp * 32 + lane) * LQ, q_hi = min(NQ, q_lo + LQ);
+    const float4* s_a4 = reinterpret_cast<const float4*>(s_a);
+    auto quad_matches = [&](int q) -> uint32_t {  // bit u: key 4q + u is a candidate
+        const float4 v = s_a4[q];
+        const float f[4] = {v.x, v.y, v.z, v.w};
+        uint32_t m = 0u;
 #pragma unroll
-            for (int u = 0; u < 4; ++u) tv[u] = i4 + 32 * u + lane < N ? key(i4 + 32 * u + lane) >> kTierShift : ~0u;
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const bool m = (act[0] && tv[u] == d0[0]) || (act[1] && tv[u] == d0[1]);
-                const uint32_t bm = __ballot_sync(0xFFFFFFFFu, m);
-                if (bm) {
-                    uint32_t base = 0u;
-                    if (lane == 0) base = atomicAdd(s_cnt, (unsigned)__popc(bm));
-                    base = __shfl_sync(0xFFFFFFFFu, base, 0);
-                    const uint32_t pos = base + __popc(bm & lt);
-                    if (m && pos < (uint32_t)cap) cand[pos] = i4 + 32 * u + lane;
-                }
-            }
+        for (int u = 0; u < 4; ++u) {
+            const uint32_t t = abs_key(f[u]) >> kTierShift;
+            if (4 * q + u < N && ((act[0] && t == d0[0]) || (act[1] && t == d0[1]))) m |= 1u << u;
         }
+        return m;
+    };
+    uint32_t n = 0u;
+    if (act[0] || act[1])
+        for (int q = q_lo; q < q_hi; ++q) n += __popc(quad_matches(q));
+    uint32_t incl = n;  // lanes' counts, inclusive scan
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += v;
+    }
+    uint32_t wbase, unused0, C, unused1;
+    cta_scan2(__shfl_sync(0xFFFFFFFFu, incl, 31), 0u, s_w, wbase, unused0, C, unused1);
+    if (C > (uint32_t)cap) return false;  // the same decision in every thread
+    if (n) {
+        uint32_t pos = wbase + incl - n;
+        for (int q = q_lo; q < q_hi; ++q) {
+            const uint32_t m = quad_matches(q);
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                if (m & (1u << u)) cand[pos++] = 4 * q + u;
+        }
+    }
     __syncthreads();
-    const int C = (int)*s_cnt;
-    if (C > cap) return false;
 
     // both thresholds: bits 19..9, then 8..0, over the candidates
     const uint32_t pre1[2] = {d0[0], d0[1]};
-    tier_refine(key, cand, C, 1, act, pre1, s_hist, kk, d1, eqn, s_w, s_state);
+    tier_refine(key, cand, (int)C, 1, act, pre1, s_hist, kk, d1, eqn, s_w, s_state);
     const uint32_t pre2[2] = {(d0[0] << 11) | d1[0], (d0[1] << 11) | d1[1]};
-    tier_refine(key, cand, C, 2, act, pre2, s_hist, kk, d2, eqn, s_w, s_state);
+    tier_refine(key, cand, (int)C, 2, act, pre2, s_hist, kk, d2, eqn, s_w, s_state);
     uint32_t thr[2], take[2];
 #pragma unroll
     for (int t = 0; t < 2; ++t) {
@@ -1033,7 +1051,7 @@ __device__ bool tier_own_range(const TieredDownParams& P, const float* s_a, int*
 
     // keys equal to a threshold before n0: all of them are candidates
     uint32_t e0 = 0u, e1 = 0u;
-    for (int c = tid; c < C; c += blockDim.x) {
+    for (int c = tid; c < (int)C; c += blockDim.x) {
         const int i = cand[c];
         if (i < n0) {
             const uint32_t k = key(i);
@@ -1131,7 +1149,6 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_tiered_down(TieredDownParams
     __shared__ unsigned s_last;
     __shared__ __align__(8) uint64_t s_stage_bar;
     __shared__ int s_n[2];
-    __shared__ unsigned s_cnt;
     grid_launch_dependents();
     grid_dependency_wait();  // a and its tier histogram are the previous grids' output
     const int tid = threadIdx.x;
@@ -1153,10 +1170,6 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_tiered_down(TieredDownParams
     for (int i = tid; i < kTierBins; i += blockDim.x) s_hist[0][i] = __ldcg(P.hist + i);
     __syncthreads();
     if (bulk) mbar_wait(&s_stage_bar, 0u, P.err, kSiteTiered | kSiteFullB);
-    if (tid == 0) {  // the last CTA to have read the histogram re-zeroes it at its end
-        __threadfence();
-        s_last = (atomicAdd(P.hist + kTierBins, 1u) == gridDim.x - 1) ? 1u : 0u;
-    }
 
     // Fast path: own index range, candidates in the ring after the staged a.
     int ntop = 0, nrec = 0;
@@ -1165,7 +1178,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_tiered_down(TieredDownParams
         const long long off = ((long long)N * 4 + 15) / 16 * 16;
         const long long cap = ((long long)R * L.stage - off) / 4;
         own = tier_own_range(P, s_a, reinterpret_cast<int*>(ring + off), (int)(cap < N ? cap : N), n0, n1, s_col,
-                             s_av, s_hist, s_w, s_state, s_n, &s_cnt);
+                             s_av, s_hist, s_w, s_state, s_n);
         __syncthreads();
         if (own) {
             ntop = s_n[0];
@@ -1320,6 +1333,13 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_tiered_down(TieredDownParams
     __syncthreads();
     const float* ycta = reinterpret_cast<const float*>(ring + (size_t)R * L.stage) - d;
     cluster_ticket_reduce4(ycta, d, P.part, P.tickets, P.y);
+    // every CTA read the histogram at its start; the last one to finish
+    // re-zeroes it for the next token
+    if (threadIdx.x == 0) {
+        __threadfence();
+        s_last = (atomicAdd(P.hist + kTierBins, 1u) == gridDim.x - 1) ? 1u : 0u;
+    }
+    __syncthreads();
     if (s_last) {
         for (int i = threadIdx.x; i < kTierBins; i += blockDim.x) P.hist[i] = 0u;
         if (threadIdx.x == 0) P.hist[kTierBins] = 0u;
