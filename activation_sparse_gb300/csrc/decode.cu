@@ -424,15 +424,15 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_sparse_decode(SparseDecodePa
 // of its own stages). Each warp computes a = silu(g.x) * (u.x) for its neuron
 // and accumulates a * down into its own register partial of y; there is no
 // CTA-wide barrier in the main loop, so a slow record stalls one warp only.
-// x is read straight into registers; the producer starts streaming as soon as
-// the barriers exist.
+// x is staged once per CTA in shared memory after the dependency wait; the
+// producer starts streaming as soon as the barriers exist.
 template <int MAXC>
 __global__ void __launch_bounds__(kDecThreads, 1) k_sparse_decode_b1(SparseDecodeParams P) {
     extern __shared__ __align__(1024) uint8_t smem[];
     const int d = P.d;
-    // x stays in registers when it fits (d <= 2048); wider rows read it from shared memory
-    constexpr bool kXReg = (MAXC == 1);
-    const RingLayout L = ring_layout(P.R, 6 * d, 0, kXReg ? 0 : 2 * d);
+    // x is staged once per CTA in shared memory (one L2 read of x per CTA
+    // rather than one per warp)
+    const RingLayout L = ring_layout(P.R, 6 * d, 0, 2 * d);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.off_full);
     uint64_t* empty = reinterpret_cast<uint64_t*>(smem + L.off_empty);
     const uint4* s_x = reinterpret_cast<const uint4*>(smem + L.off_x);
@@ -488,21 +488,14 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_sparse_decode_b1(SparseDecod
         if (P.stable_plan) grid_dependency_wait();  // before the tail touches y and the partials
     } else {
         grid_dependency_wait();  // x may be the previous grid's output
-        uint4 xr[kXReg ? XJ : 1];
         float acc[XJ][8];
-        if constexpr (!kXReg) {
-            for (int c = threadIdx.x; c < nch; c += kConsThreads)
-                const_cast<uint4*>(s_x)[c] = __ldg(reinterpret_cast<const uint4*>(P.x) + c);
-            named_bar_sync(1, kConsThreads);
-        }
+        for (int c = threadIdx.x; c < nch; c += kConsThreads)
+            const_cast<uint4*>(s_x)[c] = __ldg(reinterpret_cast<const uint4*>(P.x) + c);
+        named_bar_sync(1, kConsThreads);
 #pragma unroll
-        for (int j = 0; j < XJ; ++j) {
-            const int c = lane + 32 * j;
-            if constexpr (kXReg)
-                xr[j] = (c < nch) ? __ldg(reinterpret_cast<const uint4*>(P.x) + c) : make_uint4(0u, 0u, 0u, 0u);
+        for (int j = 0; j < XJ; ++j)
 #pragma unroll
             for (int e = 0; e < 8; ++e) acc[j][e] = 0.0f;
-        }
         for (int i = warp; i < cnt; i += kConsWarps) {
             const int s = i % R;
             mbar_wait(&full[s], (uint32_t)((i / R) & 1), P.err, kSiteDecode | kSiteFull);
@@ -512,9 +505,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_sparse_decode_b1(SparseDecod
             for (int j = 0; j < XJ; ++j) {
                 const int c = lane + 32 * j;
                 if (c < nch) {
-                    uint4 xv;
-                    if constexpr (kXReg) xv = xr[j];
-                    else xv = s_x[c];
+                    const uint4 xv = s_x[c];
                     ga[j & 3] = dot8(st[c], xv, ga[j & 3]);
                     ua[j & 3] = dot8(st[nch + c], xv, ua[j & 3]);
                 }
@@ -1484,7 +1475,7 @@ cudaError_t launch_sd1(SparseDecodeParams& P, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
     if ((e = allow_max_smem(kern)) != cudaSuccess) return e;
-    const size_t smem = (size_t)ring_layout(P.R, 6 * P.d, 0, MAXC == 1 ? 0 : 2 * P.d).total;
+    const size_t smem = (size_t)ring_layout(P.R, 6 * P.d, 0, 2 * P.d).total;
     void* args[] = {&P};
     return launch_clustered(kern, sms > 2 * kSpareSms ? sms - kSpareSms : sms, 1, smem, st, args, /*pdl=*/true);
 }
@@ -1509,7 +1500,7 @@ int decode_max_partial_floats(int d, int B) {
 
 int sparse_decode_b1_stages(int d) {
     const int stage = round_up(6 * d, 128);
-    int R = (kSmemBudget - 512 - (d > 2048 ? round_up(2 * d, 128) : 0)) / stage;
+    int R = (kSmemBudget - 512 - round_up(2 * d, 128)) / stage;
     if (R > 32) R = 32;
     R = (R / kConsWarps) * kConsWarps;
     // warp w's partial (blocks of 32 chunks: round_up(d, 256) floats) reuses
