@@ -196,31 +196,134 @@ __global__ void __launch_bounds__(kSelNT) k_topk_alpha(const float* __restrict__
 // a6: one CTA per sequence. Top-beta of the counts among non-static positions
 // (ties to the lower position), united with the static positions, written as
 // an ascending list of n_sel positions.
+// Counts are small integers (at most the prompt length), so one 2048-bin
+// histogram of min(count, 2047) finds the threshold count and how many
+// neurons equal to it are taken (in index order). One blocked pass with two
+// CTA scans (ranks among equal counts, then output slots) writes S. Only a
+// threshold in the saturated top bin (counts >= 2047) falls back to the
+// general radix selection.
+constexpr int kBetaBins = 2048;
+
+// Exclusive scan of one value per thread over a 1024-thread CTA; *total gets
+// the sum. s_w: 32 words of shared scratch.
+__device__ __forceinline__ uint32_t cta_excl_scan_1024(uint32_t v, uint32_t* s_w, uint32_t* total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    uint32_t incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += t;
+    }
+    if (lane == 31) s_w[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        const uint32_t w = s_w[lane];
+        uint32_t wi = w;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t t = __shfl_up_sync(0xFFFFFFFFu, wi, o);
+            if (lane >= o) wi += t;
+        }
+        s_w[lane] = wi - w;  // exclusive prefix of the warp totals
+        if (lane == 31) s_w[32] = wi;
+    }
+    __syncthreads();
+    const uint32_t r = s_w[warp] + incl - v;
+    *total = s_w[32];
+    __syncthreads();  // s_w may be reused
+    return r;
+}
+
 __global__ void __launch_bounds__(1024) k_topk_beta(const uint32_t* __restrict__ counts,
                                                    const uint8_t* __restrict__ is_static, int n, int beta,
                                                    int n_sel, int32_t* __restrict__ S, unsigned* err) {
     extern __shared__ __align__(16) uint32_t s_keys[];  // n keys, then n flag bytes
     uint8_t* s_take = reinterpret_cast<uint8_t*>(s_keys + n);
-    __shared__ uint32_t hist[257], state[2], scnt[2 * 1024 / 32];
-    const int b = blockIdx.x;
-    for (int i = threadIdx.x; i < n; i += 1024) {
+    __shared__ uint32_t hist[kBetaBins];
+    __shared__ uint32_t s_w[33];
+    __shared__ uint32_t s_cut[2];  // threshold count, equal counts taken
+    const int b = blockIdx.x, tid = threadIdx.x;
+    for (int i = tid; i < n; i += 1024) {
         s_keys[i] = counts[(size_t)b * n + i];
         s_take[i] = is_static[i] ? 1 : 0;
     }
+    for (int i = tid; i < kBetaBins; i += 1024) hist[i] = 0u;
+    if (tid == 0) {
+        s_cut[0] = 0xFFFFFFFFu;  // beta == 0: no count is above or at it
+        s_cut[1] = 0u;
+    }
     __syncthreads();
-    auto key = [&](int i) -> uint32_t { return s_keys[i]; };
-    auto elig = [&](int i) { return is_static[i] == 0; };
-    const TopkCut cut = block_topk_cut<1024>(n, beta, key, elig, hist, state);
-    auto mark = [&](int i, int) { s_take[i] = 1; };
-    block_topk_emit<1024, false>(n, cut, key, elig, mark, NoWord(), scnt);
+    for (int i = tid; i < n; i += 1024)
+        if (!s_take[i]) atomicAdd(&hist[min(s_keys[i], (uint32_t)(kBetaBins - 1))], 1u);
     __syncthreads();
+    // thread t owns bins 2047 - 2t and 2046 - 2t (counting from the top)
+    const uint32_t h0 = hist[kBetaBins - 1 - 2 * tid], h1 = hist[kBetaBins - 2 - 2 * tid];
+    uint32_t eligible;
+    const uint32_t above = cta_excl_scan_1024(h0 + h1, s_w, &eligible);
+    if (beta > 0 && above < (uint32_t)beta && (uint32_t)beta <= above + h0 + h1) {
+        if ((uint32_t)beta <= above + h0) {
+            s_cut[0] = (uint32_t)(kBetaBins - 1 - 2 * tid);
+            s_cut[1] = (uint32_t)beta - above;
+        } else {
+            s_cut[0] = (uint32_t)(kBetaBins - 2 - 2 * tid);
+            s_cut[1] = (uint32_t)beta - above - h0;
+        }
+    }
+    __syncthreads();
+    const uint32_t thr = s_cut[0], take = s_cut[1];
     int32_t* dst = S + (size_t)b * n_sel;
-    auto pred = [&](int i) { return s_take[i] != 0; };
-    auto put = [&](int i, int r) {
-        if (r < n_sel) dst[r] = i;
-    };
-    const int total = block_compact<1024>(n, pred, put, scnt);
-    if (threadIdx.x == 0 && total != n_sel) atomicOr(err, SI_DEVERR_COUNT);
+    if (beta > 0 && (eligible < (uint32_t)beta || thr == (uint32_t)(kBetaBins - 1))) {
+        // fewer eligible neurons than beta, or a threshold among saturated
+        // counts: the general radix selection decides
+        __syncthreads();
+        __shared__ uint32_t rhist[257], rstate[2], scnt[2 * 1024 / 32];
+        auto key = [&](int i) -> uint32_t { return s_keys[i]; };
+        auto elig = [&](int i) { return is_static[i] == 0; };
+        const TopkCut cut = block_topk_cut<1024>(n, beta, key, elig, rhist, rstate);
+        auto mark = [&](int i, int) { s_take[i] = 1; };
+        block_topk_emit<1024, false>(n, cut, key, elig, mark, NoWord(), scnt);
+        __syncthreads();
+        auto pred = [&](int i) { return s_take[i] != 0; };
+        auto put = [&](int i, int r) {
+            if (r < n_sel) dst[r] = i;
+        };
+        const int total = block_compact<1024>(n, pred, put, scnt);
+        if (tid == 0 && total != n_sel) atomicOr(err, SI_DEVERR_COUNT);
+        return;
+    }
+    // each thread takes a contiguous run of positions, in index order
+    const int CH = (n + 1023) / 1024;
+    const int lo = tid * CH, hi = min(n, lo + CH);
+    uint32_t q = 0u;
+    for (int i = lo; i < hi; ++i) q += (!s_take[i] && s_keys[i] == thr) ? 1u : 0u;
+    uint32_t unused;
+    const uint32_t r0 = cta_excl_scan_1024(q, s_w, &unused);  // equal counts before this run
+    uint32_t r = r0, c = 0u;
+    for (int i = lo; i < hi; ++i) {
+        const uint32_t k = s_keys[i];
+        bool sel = s_take[i] != 0;
+        if (!sel) {
+            sel = k > thr || (k == thr && r < take);
+            r += (k == thr) ? 1u : 0u;
+        }
+        c += sel ? 1u : 0u;
+    }
+    uint32_t total;
+    uint32_t pos = cta_excl_scan_1024(c, s_w, &total);
+    r = r0;
+    for (int i = lo; i < hi; ++i) {
+        const uint32_t k = s_keys[i];
+        bool sel = s_take[i] != 0;
+        if (!sel) {
+            sel = k > thr || (k == thr && r < take);
+            r += (k == thr) ? 1u : 0u;
+        }
+        if (sel) {
+            if (pos < (uint32_t)n_sel) dst[pos] = i;
+            ++pos;
+        }
+    }
+    if (tid == 0 && total != (uint32_t)n_sel) atomicOr(err, SI_DEVERR_COUNT);
 }
 
 // a2: selective loading ranking (SelectInfer section 4, Fig. 6), one CTA.

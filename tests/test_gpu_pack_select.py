@@ -111,6 +111,7 @@ SEL_CASES = [
     (1024, 0.7, 0.0, 0.4, 64, 16, 1, "ties"),             # no static neurons
     (1000, 1.0, 0.3, 0.4, 50, 8, 1, "zeros"),             # all |A| equal (zero)
     (33, 1.0, 0.1, 0.5, 7, 9, 2, "ties"),                 # tiny, ragged word
+    (256, 1.0, 0.1, 0.5, 200, 2100, 1, "lognormal"),      # counts above 2047: top-beta's general path
 ]
 
 
