@@ -166,47 +166,11 @@ __device__ int block_compact(int n, PredF pred, OutF out, uint32_t* scnt) {
 
 // ------------------------------------------------------------------- kernels
 
-constexpr int kSelNT = 512;
-
-// a4 + a5: one CTA per token row. Per-token top-alpha over the loaded
-// positions by |A| (SelectInfer section 5); every selected position adds 1 to
-// its sequence's count. Optional bit mask of the selection per row.
-__global__ void __launch_bounds__(kSelNT) k_topk_alpha(const float* __restrict__ absA, int ld, int n, int T,
-                                                      int alpha, uint32_t* __restrict__ counts,
-                                                      uint32_t* __restrict__ topmask, int words) {
-    extern __shared__ __align__(16) uint32_t s_keys[];
-    __shared__ uint32_t hist[257], state[2], scnt[2 * kSelNT / 32];
-    const int row = blockIdx.x;
-    const int b = row / T;
-    const float* src = absA + (size_t)row * ld;
-    for (int i = threadIdx.x; i < n; i += kSelNT) s_keys[i] = abs_key(__ldg(src + i));
-    __syncthreads();
-    auto key = [&](int i) -> uint32_t { return s_keys[i]; };
-    auto elig = [](int) { return true; };
-    const TopkCut cut = block_topk_cut<kSelNT>(n, alpha, key, elig, hist, state);
-    uint32_t* cnt = counts + (size_t)b * n;
-    uint32_t* tm = topmask ? topmask + (size_t)row * words : nullptr;
-    auto out = [&](int i, int) { atomicAdd(cnt + i, 1u); };
-    auto word = [&](int wi, uint32_t bits) {
-        if (tm) tm[wi] = bits;
-    };
-    block_topk_emit<kSelNT, true>(n, cut, key, elig, out, word, scnt);
-}
-
-// a6: one CTA per sequence. Top-beta of the counts among non-static positions
-// (ties to the lower position), united with the static positions, written as
-// an ascending list of n_sel positions.
-// Counts are small integers (at most the prompt length), so one 2048-bin
-// histogram of min(count, 2047) finds the threshold count and how many
-// neurons equal to it are taken (in index order). One blocked pass with two
-// CTA scans (ranks among equal counts, then output slots) writes S. Only a
-// threshold in the saturated top bin (counts >= 2047) falls back to the
-// general radix selection.
-constexpr int kBetaBins = 2048;
-
-// Exclusive scan of one value per thread over a 1024-thread CTA; *total gets
-// the sum. s_w: 32 words of shared scratch.
-__device__ __forceinline__ uint32_t cta_excl_scan_1024(uint32_t v, uint32_t* s_w, uint32_t* total) {
+// Exclusive scan of one value per thread over an NT-thread CTA (NT a
+// multiple of 32, at most 1024); *total gets the sum. s_w: 33 words of shared
+// scratch. Every thread of the CTA calls it.
+template <int NT>
+__device__ __forceinline__ uint32_t cta_excl_scan(uint32_t v, uint32_t* s_w, uint32_t* total) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     uint32_t incl = v;
 #pragma unroll
@@ -217,7 +181,7 @@ __device__ __forceinline__ uint32_t cta_excl_scan_1024(uint32_t v, uint32_t* s_w
     if (lane == 31) s_w[warp] = incl;
     __syncthreads();
     if (warp == 0) {
-        const uint32_t w = s_w[lane];
+        const uint32_t w = lane < NT / 32 ? s_w[lane] : 0u;
         uint32_t wi = w;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -233,6 +197,115 @@ __device__ __forceinline__ uint32_t cta_excl_scan_1024(uint32_t v, uint32_t* s_w
     __syncthreads();  // s_w may be reused
     return r;
 }
+
+constexpr int kSelNT = 512;
+
+// a4 + a5: one CTA per token row. Per-token top-alpha over the loaded
+// positions by |A| (SelectInfer section 5); every selected position adds 1 to
+// its sequence's count. Optional bit mask of the selection per row.
+// The threshold comes from three radix passes over the 31-bit |A| key
+// (digits of 11, 11 and 9 bits, shared-memory histograms); the emit walks
+// word-aligned runs of 32 positions per warp, so a selection ballot is the
+// row's mask word. Ranks among equal keys are counted only when the
+// threshold splits a run of them.
+constexpr int kAlphaBins = 2048;
+
+__global__ void __launch_bounds__(kSelNT) k_topk_alpha(const float* __restrict__ absA, int ld, int n, int T,
+                                                      int alpha, uint32_t* __restrict__ counts,
+                                                      uint32_t* __restrict__ topmask, int words) {
+    extern __shared__ __align__(16) uint32_t s_keys[];
+    __shared__ uint32_t hist[kAlphaBins];
+    __shared__ uint32_t s_w[33];
+    __shared__ uint32_t s_state[3];  // bin, rank left inside it, its count
+    const int row = blockIdx.x, b = row / T;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const float* src = absA + (size_t)row * ld;
+    for (int i = tid; i < n; i += kSelNT) s_keys[i] = abs_key(__ldg(src + i));
+    const bool act = alpha > 0 && alpha < n;
+    uint32_t prefix = 0u, pmask = 0u, kk = (uint32_t)alpha, eqn = 0u;
+    if (act) {
+        constexpr int kShift[3] = {20, 9, 0}, kBits[3] = {11, 11, 9};
+#pragma unroll
+        for (int p = 0; p < 3; ++p) {
+            const int shift = kShift[p], nb = 1 << kBits[p], per = nb / kSelNT;
+            for (int i = tid; i < kAlphaBins; i += kSelNT) hist[i] = 0u;
+            __syncthreads();
+            for (int i = tid; i < n; i += kSelNT) {
+                const uint32_t k = s_keys[i];
+                if ((k & pmask) == prefix) atomicAdd(&hist[(k >> shift) & (uint32_t)(nb - 1)], 1u);
+            }
+            __syncthreads();
+            // thread t owns bins nb-1-per*t ... nb-per*(t+1), highest first
+            uint32_t c = 0u;
+            for (int j = 0; j < per; ++j) c += hist[nb - 1 - per * tid - j];
+            uint32_t tot;
+            const uint32_t e = cta_excl_scan<kSelNT>(c, s_w, &tot);  // keys in higher bins
+            if (e < kk && kk <= e + c) {
+                uint32_t run = e;
+                for (int j = 0; j < per; ++j) {
+                    const int bin = nb - 1 - per * tid - j;
+                    if (run + hist[bin] >= kk) {
+                        s_state[0] = (uint32_t)bin;
+                        s_state[1] = kk - run;
+                        s_state[2] = hist[bin];
+                        break;
+                    }
+                    run += hist[bin];
+                }
+            }
+            __syncthreads();
+            prefix |= s_state[0] << shift;
+            pmask |= (uint32_t)(nb - 1) << shift;
+            kk = s_state[1];
+            eqn = s_state[2];
+        }
+    } else {
+        __syncthreads();  // the keys are in place
+    }
+    // every key > thr and the first `take` keys == thr, in index order
+    const uint32_t thr = act ? prefix : (alpha <= 0 ? 0xFFFFFFFFu : 0u);
+    const uint32_t take = act ? kk : (alpha <= 0 ? 0u : 0xFFFFFFFFu);
+    const bool split = act && kk < eqn;
+    // warp w owns positions [w * SEG, (w + 1) * SEG), SEG a multiple of 32
+    const int SEG = ((n + kSelNT - 1) / kSelNT) * 32;
+    const int lo = warp * SEG, hi = min(n, lo + SEG);
+    const uint32_t lt = lanemask_lt();
+    uint32_t r = 0u;  // keys equal to thr before the current position
+    if (split) {
+        uint32_t q = 0u;
+        for (int i0 = lo; i0 < hi; i0 += 32) {
+            const int i = i0 + lane;
+            q += __popc(__ballot_sync(0xFFFFFFFFu, i < hi && s_keys[i] == thr));
+        }
+        uint32_t tot;
+        const uint32_t ex = cta_excl_scan<kSelNT>(lane == 0 ? q : 0u, s_w, &tot);
+        r = __shfl_sync(0xFFFFFFFFu, ex, 0);
+    }
+    uint32_t* cnt = counts + (size_t)b * n;
+    uint32_t* tm = topmask ? topmask + (size_t)row * words : nullptr;
+    for (int i0 = lo; i0 < hi; i0 += 32) {
+        const int i = i0 + lane;
+        const bool in = i < hi;
+        const uint32_t k = in ? s_keys[i] : 0u;
+        const uint32_t me = __ballot_sync(0xFFFFFFFFu, in && k == thr);
+        const bool sel = in && (k > thr || (k == thr && r + __popc(me & lt) < take));
+        r += __popc(me);
+        const uint32_t ms = __ballot_sync(0xFFFFFFFFu, sel);
+        if (sel) atomicAdd(cnt + i, 1u);
+        if (tm && lane == 0) tm[i0 >> 5] = ms;
+    }
+}
+
+// a6: one CTA per sequence. Top-beta of the counts among non-static positions
+// (ties to the lower position), united with the static positions, written as
+// an ascending list of n_sel positions.
+// Counts are small integers (at most the prompt length), so one 2048-bin
+// histogram of min(count, 2047) finds the threshold count and how many
+// neurons equal to it are taken (in index order). One blocked pass with two
+// CTA scans (ranks among equal counts, then output slots) writes S. Only a
+// threshold in the saturated top bin (counts >= 2047) falls back to the
+// general radix selection.
+constexpr int kBetaBins = 2048;
 
 __global__ void __launch_bounds__(1024) k_topk_beta(const uint32_t* __restrict__ counts,
                                                    const uint8_t* __restrict__ is_static, int n, int beta,
@@ -259,7 +332,7 @@ __global__ void __launch_bounds__(1024) k_topk_beta(const uint32_t* __restrict__
     // thread t owns bins 2047 - 2t and 2046 - 2t (counting from the top)
     const uint32_t h0 = hist[kBetaBins - 1 - 2 * tid], h1 = hist[kBetaBins - 2 - 2 * tid];
     uint32_t eligible;
-    const uint32_t above = cta_excl_scan_1024(h0 + h1, s_w, &eligible);
+    const uint32_t above = cta_excl_scan<1024>(h0 + h1, s_w, &eligible);
     if (beta > 0 && above < (uint32_t)beta && (uint32_t)beta <= above + h0 + h1) {
         if ((uint32_t)beta <= above + h0) {
             s_cut[0] = (uint32_t)(kBetaBins - 1 - 2 * tid);
@@ -297,7 +370,7 @@ __global__ void __launch_bounds__(1024) k_topk_beta(const uint32_t* __restrict__
     uint32_t q = 0u;
     for (int i = lo; i < hi; ++i) q += (!s_take[i] && s_keys[i] == thr) ? 1u : 0u;
     uint32_t unused;
-    const uint32_t r0 = cta_excl_scan_1024(q, s_w, &unused);  // equal counts before this run
+    const uint32_t r0 = cta_excl_scan<1024>(q, s_w, &unused);  // equal counts before this run
     uint32_t r = r0, c = 0u;
     for (int i = lo; i < hi; ++i) {
         const uint32_t k = s_keys[i];
@@ -309,7 +382,7 @@ __global__ void __launch_bounds__(1024) k_topk_beta(const uint32_t* __restrict__
         c += sel ? 1u : 0u;
     }
     uint32_t total;
-    uint32_t pos = cta_excl_scan_1024(c, s_w, &total);
+    uint32_t pos = cta_excl_scan<1024>(c, s_w, &total);
     r = r0;
     for (int i = lo; i < hi; ++i) {
         const uint32_t k = s_keys[i];

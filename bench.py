@@ -334,6 +334,8 @@ def run_gpu(args, world, rank, local):
         "roofline": {"kernel": "k_sparse_decode_b1", "bound": "hbm", "achieved": round(achieved_gbs, 1),
                      "peak": hbm_peak, "unit": "GB/s", "frac": round(achieved_gbs / hbm_peak, 4),
                      "peak_source": peak_kind, "traffic": args.traffic,
+                     "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum, one launch"
+                     if args.traffic is not None else None,
                      "bytes_per_launch": launch_bytes, "launch_us": round(launch_s * 1e6, 3)},
         "prefill_roofline": {"kernel": "k_act_gemm", "bound": "tensor", "achieved": round(gemm_tfs, 1),
                              "peak": tf_peak, "unit": "TFLOP/s", "frac": round(gemm_tfs / tf_peak, 4),
@@ -586,6 +588,13 @@ def run_profile_case(args):
     print(json.dumps({"profile_case": case, "launches": args.steps, "ms_per_launch": e0.elapsed_time(e1) / args.steps}))
 
 
+# DRAM bytes (read + write) of one k_sparse_decode_b1 launch on one
+# Llama3.2-1B layer, from the ncu capture summarised in
+# profiles/k_sparse_decode_b1_llama3.2-1b_layer.md (40.3256 MB read, 7.4 KB
+# written). Set to None whenever that kernel changes until it is re-captured.
+DECODE_TRAFFIC_BYTES = 40325632 + 7424
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -595,7 +604,7 @@ def main(argv=None):
     ap.add_argument("--no-spax", action="store_true", help="skip the SpAx Llama-3.1-8B measurement")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU oracle time budget")
-    ap.add_argument("--traffic", type=float, default=None,
+    ap.add_argument("--traffic", type=float, default=DECODE_TRAFFIC_BYTES,
                     help="DRAM bytes per k_sparse_decode_b1 launch from an ncu capture (null when unknown)")
     ap.add_argument("--out-dir", default=None, help="directory for the clock samples (optional)")
     ap.add_argument("--profile-case", choices=["decode", "prefill", "dense", "tiered"], default=None,
