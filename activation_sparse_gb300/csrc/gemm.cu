@@ -8,11 +8,13 @@
 //   mode 1  offline profiler score (section 3, Eq. (1)): adds
 //           sum over tokens of |a| into a per-neuron score.
 //
-// Tile: 128 tokens x 128 neurons, K in blocks of 64 (one 128-byte swizzle row).
-// The gate rows and the up rows of the same 128 neurons are loaded side by
-// side into one 256-row B tile, so a single tcgen05.mma (M=128, N=256, K=16,
-// bf16 in, fp32 accumulate) produces both projections; the accumulator lives
-// in 256 TMEM columns (gate in 0..127, up in 128..255) and the epilogue reads
+// Tile: 256 tokens x 128 neurons, K in blocks of 64 (one 128-byte swizzle
+// row). The gate rows and the up rows of the same 128 neurons are loaded side
+// by side into one 256-row B tile, so one tcgen05.mma (M=128, N=256, K=16,
+// bf16 in, fp32 accumulate) produces both projections for 128 tokens; two
+// such MMAs (token rows 0..127 and 128..255) share each B tile, which halves
+// the B traffic per flop. The two accumulators fill the 512 TMEM columns
+// (per 128-token half: gate in 0..127, up in 128..255) and the epilogue reads
 // matching gate/up columns of the same row with tcgen05.ld.
 //
 // Warp roles (192 threads): warp 0 lane 0 issues TMA loads into a 4-stage
@@ -32,21 +34,24 @@ namespace si {
 
 namespace {
 
-constexpr int BM = 128;       // token rows per tile (MMA M)
+constexpr int BM = 128;       // token rows per MMA (MMA M)
+constexpr int MT = 2;         // MMA row blocks per tile: 256 token rows
 constexpr int BNN = 128;      // neurons per tile (gate + up -> MMA N = 256)
 constexpr int BK = 64;        // K per stage (128 bytes of bf16)
-constexpr int STAGES = 4;
-constexpr int A_BYTES = BM * BK * 2;          // 16 KB
+constexpr int STAGES = 3;
+constexpr int A_BYTES = BM * BK * 2;          // 16 KB per row block
+constexpr int STAGE_A = MT * A_BYTES;         // 32 KB
 constexpr int B_BYTES = 2 * BNN * BK * 2;     // 32 KB (gate tile then up tile)
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int TMEM_COLS = 256;
+constexpr int STAGE_BYTES = STAGE_A + B_BYTES;
+constexpr int ACC_COLS = 2 * BNN;             // TMEM columns of one accumulator
+constexpr int TMEM_COLS = MT * ACC_COLS;      // 512: all of TMEM
 constexpr int kThreads = 192;
 constexpr int kEpiWarps = 4;
 constexpr int COLSUM_FLOATS = kEpiWarps * 32 * 33;
 
 // shared-memory layout (offsets from a 1024-aligned base)
 constexpr int OFF_A = 0;
-constexpr int OFF_B = STAGES * A_BYTES;
+constexpr int OFF_B = STAGES * STAGE_A;
 constexpr int OFF_COLSUM = OFF_B + STAGES * B_BYTES;
 constexpr int OFF_BAR = OFF_COLSUM + COLSUM_FLOATS * 4;
 constexpr int OFF_TMEM_SLOT = OFF_BAR + (2 * STAGES + 1) * 8;
@@ -132,7 +137,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n0 = blockIdx.x * BNN;
-    const int m0 = blockIdx.y * BM;
+    const int m0 = blockIdx.y * (MT * BM);
     const int KB = P.K / BK;
 
     if (threadIdx.x == 0) {
@@ -160,9 +165,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int s = kb % STAGES;
                 if (kb >= STAGES) mbar_wait(&empty[s], (uint32_t)((kb / STAGES - 1) & 1), P.err, kSiteGemm | kSiteEmpty);
                 mbar_arrive_expect_tx(&full[s], STAGE_BYTES);
-                uint8_t* a_dst = smem + OFF_A + s * A_BYTES;
+                uint8_t* a_dst = smem + OFF_A + s * STAGE_A;
                 uint8_t* b_dst = smem + OFF_B + s * B_BYTES;
-                tma_load_2d(a_dst, &map_x, kb * BK, m0, &full[s]);
+#pragma unroll
+                for (int t = 0; t < MT; ++t) tma_load_2d(a_dst + t * A_BYTES, &map_x, kb * BK, m0 + t * BM, &full[s]);
                 tma_load_2d(b_dst, &map_g, kb * BK, n0, &full[s]);
                 tma_load_2d(b_dst + B_BYTES / 2, &map_u, kb * BK, n0, &full[s]);
             }
@@ -179,14 +185,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int s = kb % STAGES;
                 mbar_wait(&full[s], (uint32_t)((kb / STAGES) & 1), P.err, kSiteGemm | kSiteFull);
                 tc_fence_after();
-                const uint32_t a_addr = smem_u32(smem + OFF_A + s * A_BYTES);
+                const uint32_t a_addr = smem_u32(smem + OFF_A + s * STAGE_A);
                 const uint32_t b_addr = smem_u32(smem + OFF_B + s * B_BYTES);
-                const uint64_t adesc = sw128_desc(a_addr), bdesc = sw128_desc(b_addr);
+                const uint64_t bdesc = sw128_desc(b_addr);
 #pragma unroll
-                for (int k = 0; k < BK / 16; ++k) {
-                    // +32 bytes per K step of 16 bf16 inside the swizzled 128-byte row
-                    tc_mma(tmem, adesc + (uint64_t)(2 * k), bdesc + (uint64_t)(2 * k), kIdesc,
-                           (kb > 0 || k > 0) ? 1u : 0u);
+                for (int t = 0; t < MT; ++t) {
+                    const uint64_t adesc = sw128_desc(a_addr + (uint32_t)(t * A_BYTES));
+#pragma unroll
+                    for (int k = 0; k < BK / 16; ++k) {
+                        // +32 bytes per K step of 16 bf16 inside the swizzled 128-byte row
+                        tc_mma(tmem + (uint32_t)(t * ACC_COLS), adesc + (uint64_t)(2 * k), bdesc + (uint64_t)(2 * k),
+                               kIdesc, (kb > 0 || k > 0) ? 1u : 0u);
+                    }
                 }
                 tc_commit(&empty[s]);
             }
@@ -194,14 +204,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
     } else {
-        // epilogue: warp w reads TMEM lanes 32*(w%4) .. +31, one token row per thread
+        // epilogue: warp w reads TMEM lanes 32*(w%4) .. +31, one token row per
+        // thread in each of the two 128-token halves
         const int q = warp & 3;
-        const int row = m0 + q * 32 + lane;
         mbar_wait(accum, 0u, P.err, kSiteGemm | kSiteAccum);
         tc_fence_after();
-        const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16);
         float* cs = reinterpret_cast<float*>(smem + OFF_COLSUM) + (warp - 2) * 32 * 33;
+        for (int t = 0; t < MT; ++t)
         for (int j0 = 0; j0 < BNN; j0 += 32) {
+            const int row = m0 + t * BM + q * 32 + lane;
+            const uint32_t tbase = tmem + (uint32_t)(t * ACC_COLS) + ((uint32_t)(q * 32) << 16);
             uint32_t g[32], u[32];
             tmem_ld32(tbase + (uint32_t)j0, g);
             tmem_ld32(tbase + (uint32_t)(BNN + j0), u);
@@ -290,7 +302,7 @@ cudaError_t launch_act_gemm(const ActGemmParams& P, cudaStream_t st) {
     if ((e = make_map(&mg, P.Wgate, P.K, P.Nrows, P.w_stride)) != cudaSuccess) return e;
     if ((e = make_map(&mu, P.Wup, P.K, P.Nrows, P.w_stride)) != cudaSuccess) return e;
     if ((e = allow_max_smem(k_act_gemm)) != cudaSuccess) return e;
-    dim3 grid((P.Nvalid + BNN - 1) / BNN, (P.M + BM - 1) / BM);
+    dim3 grid((P.Nvalid + BNN - 1) / BNN, (P.M + MT * BM - 1) / (MT * BM));
     if (grid.y > 65535) return cudaErrorInvalidValue;
     k_act_gemm<<<grid, kThreads, SMEM_BYTES, st>>>(mx, mg, mu, P);
     return cudaGetLastError();
