@@ -23,6 +23,8 @@ PROFILE_CASES = [
     (256, 1024, 128, None),       # single-layer workload
     (256, 1000, 100, None),       # ragged N and T
     (128, 130, 1, None),          # one token, ragged tile
+    (256, 1000, 600, None),       # 5 token tiles: clusters of 4 with padding tiles
+    (256, 300, 300, None),        # 3 token tiles: clusters of 2 with a padding tile
     (2048, 8192, 4096, 96),       # Llama3.2-1B layer, 4096 calibration tokens
     (3072, 8192, 512, 64),        # Llama3.2-3B width
 ]
@@ -52,6 +54,7 @@ SELECT_CASES = [
     (3072, 8192, 0.7, 0.25, 0.5, 1024, 1024, 1, 8),       # Llama3.2-3B prompt
     (2048, 11008, 0.8, 0.25, 0.5, 1024, 256, 8, 8),       # Qwen2.5-3B, 8 prompts
     (512, 700, 0.9, 0.3, 0.5, 40, 77, 2, None),           # ragged M and neurons
+    (256, 1024, 0.7, 0.2, 0.4, 64, 150, 2, None),         # 3 token tiles: a padding tile in the cluster
 ]
 
 
