@@ -1194,9 +1194,14 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_tiered_down(TieredDownParams
     __syncthreads();  // the records are in place and the staged keys are no longer read
 
     if (warp == kConsWarps) {
-        if (lane == 0) {
+        // kIssueLanes lanes issue the copies, lane l the records l, l + 4, ...
+        // (R is a multiple of 8, so every stage is filled by one lane, in
+        // order): one lane alone cannot keep the small middle-column copies
+        // flowing.
+        constexpr int kIssueLanes = 4;
+        if (lane < kIssueLanes) {
             const uint64_t pol = policy_evict_first();
-            for (int i = 0; i < nrec; ++i) {
+            for (int i = lane; i < nrec; i += kIssueLanes) {
                 const int s = i % R;
                 if (i >= R) mbar_wait(&empty[s], (uint32_t)((i / R - 1) & 1), P.err, kSiteTiered | kSiteEmpty);
                 uint8_t* dst = ring + (size_t)s * L.stage;
