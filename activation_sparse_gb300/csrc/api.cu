@@ -117,7 +117,8 @@ struct spax_layer {
     int d = 0, N = 0, bits = 0, group = 0, ngp = 0;
     uint16_t* WdT = nullptr;
     uint8_t* codes = nullptr;
-    float* params = nullptr;
+    float* params = nullptr;    // inside the records: codes + d / 2 (not a separate allocation)
+    int rec_bytes = 0;          // per-column record: d / 2 code bytes, then ngp (scale, min) pairs
     unsigned* hist = nullptr;  // tier histogram of the current a (zero between calls) + its ticket
     float* a = nullptr;
     float* part = nullptr;
@@ -159,7 +160,6 @@ void destroy_spax(spax_layer* L) {
     if (!L) return;
     dfree(L->WdT);
     dfree(L->codes);
-    dfree(L->params);
     dfree(L->hist);
     dfree(L->a);
     dfree(L->part);
@@ -540,19 +540,20 @@ int spax_encode(const uint16_t* Wd, int d, int N, int bits, int group, spax_laye
     L->bits = bits;
     L->group = group;
     L->ngp = round_up(d / group, 2);
+    L->rec_bytes = d / 2 + 8 * L->ngp;
     int rc;
     if ((rc = dalloc(&L->WdT, (size_t)N * d, "column-major Wd")) ||
-        (rc = dalloc(&L->codes, (size_t)N * d / 2, "codes")) ||
-        (rc = dalloc(&L->params, (size_t)N * L->ngp * 2, "code params")) ||
+        (rc = dalloc(&L->codes, (size_t)N * (d / 2 + 8 * L->ngp), "code records")) ||
         (rc = dalloc(&L->hist, si::kTierBins + 1, "tier histogram")) || (rc = dalloc(&L->a, N, "activations")) ||
         (rc = dalloc(&L->tickets, 16, "tickets")) || (rc = grow_part(&L->part, &L->part_floats, d, 1))) {
         destroy_spax(L);
         return rc;
     }
+    L->params = reinterpret_cast<float*>(L->codes + d / 2);
     cudaError_t e = cudaMemsetAsync(L->tickets, 0, 16 * sizeof(unsigned), st);
     if (e == cudaSuccess) e = cudaMemsetAsync(L->hist, 0, (si::kTierBins + 1) * sizeof(unsigned), st);
-    if (e == cudaSuccess) e = cudaMemsetAsync(L->params, 0, (size_t)N * L->ngp * 2 * sizeof(float), st);
-    if (e == cudaSuccess) e = si::launch_spax_encode(Wd, d, N, group, L->ngp, L->WdT, L->codes, L->params, st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(L->codes, 0, (size_t)N * L->rec_bytes, st);
+    if (e == cudaSuccess) e = si::launch_spax_encode(Wd, d, N, group, L->ngp, L->WdT, L->codes, L->rec_bytes, st);
     if (e == cudaSuccess) e = cudaStreamSynchronize(st);
     if (e != cudaSuccess) {
         destroy_spax(L);
@@ -633,7 +634,7 @@ int tiered_core(spax_layer* L, const float* a, long long k_top, long long k_mid,
     si::TieredDownParams P = {};
     P.WdT = L->WdT;
     P.codes = L->codes;
-    P.params = L->params;
+    P.rec_bytes = L->rec_bytes;
     P.a = a;
     P.hist = L->hist;
     P.top_out = top_out;

@@ -1102,7 +1102,7 @@ template <int MAXC>
 __global__ void __launch_bounds__(kDecThreads, 1) k_tiered_down(TieredDownParams P) {
     extern __shared__ __align__(1024) uint8_t smem[];
     const int d = P.d;
-    const int mid_bytes = d / 2 + P.ngp * 8;
+    const int mid_bytes = P.rec_bytes;  // d / 2 code bytes, then ngp (scale, min) pairs
     const RingLayout L = ring_layout(P.R, 2 * d, P.aux_floats * 4, 0);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.off_full);
     uint64_t* empty = reinterpret_cast<uint64_t*>(smem + L.off_empty);
@@ -1216,8 +1216,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_tiered_down(TieredDownParams
                     bulk_g2s_hint(dst, P.WdT + col * d, (uint32_t)(2 * d), &full[s], pol);
                 } else {
                     mbar_arrive_expect_tx(&full[s], (uint32_t)mid_bytes);
-                    bulk_g2s_hint(dst, P.codes + col * (d / 2), (uint32_t)(d / 2), &full[s], pol);
-                    bulk_g2s_hint(dst + d / 2, P.params + col * P.ngp * 2, (uint32_t)(P.ngp * 8), &full[s], pol);
+                    bulk_g2s_hint(dst, P.codes + col * P.rec_bytes, (uint32_t)P.rec_bytes, &full[s], pol);
                 }
             }
         }

@@ -49,8 +49,8 @@ struct DenseActParams {
 
 struct TieredDownParams {
     const uint16_t* WdT;      // [N][d] bf16
-    const uint8_t* codes;     // [N][d/2]
-    const float* params;      // [N][ngp][2]
+    const uint8_t* codes;     // [N] records of rec_bytes: d/2 code bytes, then ngp (scale, min) pairs
+    int rec_bytes;
     const float* a;           // [N]
     unsigned* hist;           // tier histogram of a (kTierBins + 1 words), re-zeroed by the kernel
     int32_t* top_out;         // optional [k_top]: the top tier, ascending
@@ -81,8 +81,8 @@ cudaError_t launch_merge_scores(const float* const* s, const float* tok, int nfi
 // pack.cu
 cudaError_t launch_pack_loaded(const uint16_t* Wg, const uint16_t* Wu, const uint16_t* Wd, int d, int N,
                                const int32_t* loaded, int n_loaded, int n_pad, uint16_t* packed, cudaStream_t st);
-cudaError_t launch_spax_encode(const uint16_t* Wd, int d, int N, int group, int ngp, uint16_t* WdT, uint8_t* codes,
-                               float* params, cudaStream_t st);
+cudaError_t launch_spax_encode(const uint16_t* Wd, int d, int N, int group, int ngp, uint16_t* WdT, uint8_t* recs,
+                               int rec_bytes, cudaStream_t st);
 
 // api.cu: sets the message si_last_error_string() returns on this thread
 void set_error_message(const char* msg);

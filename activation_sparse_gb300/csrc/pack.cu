@@ -9,7 +9,9 @@
 //  k_spax_encode   SpAx offline encoding (Fig. 2, Fig. 3): per column and
 //                  per row group, float32 min / max / scale and 4-bit codes,
 //                  plus a column-major bf16 copy of Wd so that a top-tier
-//                  column is one contiguous read.
+//                  column is one contiguous read. A column's codes and its
+//                  (scale, min) pairs form one record, so a middle-tier
+//                  column is one contiguous read too.
 #include "common.cuh"
 #include "internal.h"
 
@@ -50,11 +52,13 @@ __global__ void __launch_bounds__(256) k_pack_loaded(const uint16_t* __restrict_
 }
 
 // grid (ceil(N/32), d/group); block 256 = 8 warps, each warp owns 4 columns.
+// Column n's record at recs + n * rec_bytes: d/2 code bytes, then ngp
+// (scale, min) float pairs.
 // All quantisation arithmetic is float32 with explicit round-to-nearest
 // intrinsics (no contraction), so codes are reproducible bit for bit.
 __global__ void __launch_bounds__(256) k_spax_encode(const uint16_t* __restrict__ Wd, int d, int N, int group,
                                                     int ngp, uint16_t* __restrict__ WdT,
-                                                    uint8_t* __restrict__ codes, float* __restrict__ params) {
+                                                    uint8_t* __restrict__ recs, int rec_bytes) {
     extern __shared__ __align__(16) uint16_t s_tile[];  // [group][33]
     const int n0 = blockIdx.x * 32;
     const int g = blockIdx.y;
@@ -96,11 +100,12 @@ __global__ void __launch_bounds__(256) k_spax_encode(const uint16_t* __restrict_
                 }
                 q[h] = v;
             }
-            codes[(size_t)n * (d / 2) + (r0 + r) / 2] = (uint8_t)(q[0] | (q[1] << 4));
+            recs[(size_t)n * rec_bytes + (r0 + r) / 2] = (uint8_t)(q[0] | (q[1] << 4));
         }
         if (tx == 0) {
-            params[((size_t)n * ngp + g) * 2 + 0] = scale;
-            params[((size_t)n * ngp + g) * 2 + 1] = mn;
+            float* prm = reinterpret_cast<float*>(recs + (size_t)n * rec_bytes + d / 2);
+            prm[g * 2 + 0] = scale;
+            prm[g * 2 + 1] = mn;
         }
     }
 }
@@ -111,13 +116,13 @@ cudaError_t launch_pack_loaded(const uint16_t* Wg, const uint16_t* Wu, const uin
     return cudaGetLastError();
 }
 
-cudaError_t launch_spax_encode(const uint16_t* Wd, int d, int N, int group, int ngp, uint16_t* WdT, uint8_t* codes,
-                               float* params, cudaStream_t st) {
+cudaError_t launch_spax_encode(const uint16_t* Wd, int d, int N, int group, int ngp, uint16_t* WdT, uint8_t* recs,
+                               int rec_bytes, cudaStream_t st) {
     const size_t smem = (size_t)group * 33 * 2;
     cudaError_t e = allow_max_smem(k_spax_encode);
     if (e != cudaSuccess) return e;
     dim3 grid((N + 31) / 32, d / group);
-    k_spax_encode<<<grid, 256, smem, st>>>(Wd, d, N, group, ngp, WdT, codes, params);
+    k_spax_encode<<<grid, 256, smem, st>>>(Wd, d, N, group, ngp, WdT, recs, rec_bytes);
     return cudaGetLastError();
 }
 

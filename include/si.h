@@ -252,9 +252,10 @@ int si_sparse_ffn_decode_noalloc(const uint16_t *packed, int n_records, int d, c
  * q = clamp(floor((w - min) / scale + 0.5), 0, 2^bits - 1) (q = 0 when
  * scale == 0), all in float32; a middle-tier weight is rebuilt as
  * min + q * scale. The handle keeps a column-major bf16 copy of Wd (top tier,
- * one contiguous column per neuron), the codes [N][d*bits/8] bytes (element
- * 2i in the low nibble for bits = 4) and fp32 (scale, min) pairs
- * [N][ng_pad][2], ng_pad = d/group rounded up to even.
+ * one contiguous column per neuron) and, per column, one record of
+ * rec = d*bits/8 + 8*ng_pad bytes (ng_pad = d/group rounded up to even): the
+ * codes (element 2i in the low nibble for bits = 4), then ng_pad fp32
+ * (scale, min) pairs, so a middle-tier column is one contiguous read.
  *   Wd bf16 [d x N]. Synchronous (allocates, enqueues, waits).
  * Requires bits == 4, group a power of two >= 8 dividing d, d % 64 == 0,
  * d <= 4096. */
@@ -264,8 +265,10 @@ int spax_encode(const uint16_t *Wd, int d, int N, int bits, int group, spax_laye
 /* Shape of an encoded layer; outputs (host) may be NULL. */
 int spax_layer_info(const spax_layer *layer, int *d, int *N, int *bits, int *group, int *ng_pad);
 
-/* Device buffers of an encoded layer (read-only): WdT bf16 [N][d], codes
- * uint8 [N][d*bits/8], params fp32 [N][ng_pad][2] = (scale, min). */
+/* Device buffers of an encoded layer (read-only): WdT bf16 [N][d]; codes
+ * points at column 0's record and params at its (scale, min) pairs
+ * (codes + d*bits/8); column n's codes and params are at the same offsets
+ * n * rec bytes further, rec = d*bits/8 + 8*ng_pad. */
 int spax_layer_buffers(const spax_layer *layer, const uint16_t **WdT, const uint8_t **codes,
                        const float **params);
 

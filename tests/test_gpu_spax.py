@@ -18,10 +18,15 @@ def si():
 
 
 def encoded_buffers(layer):
+    """The column-major copy, and the per-column records split into codes
+    [N][d/2] and (scale, min) pairs [N][ng_pad][2]."""
     p_wdt, p_codes, p_params = layer.buffers()
+    rec = layer.d // 2 + 8 * layer.ngp
+    assert p_params == p_codes + layer.d // 2
     WdT = device_view(p_wdt, (layer.N, layer.d), "<i2").cpu().numpy().view(np.uint16)
-    codes = device_view(p_codes, (layer.N, layer.d // 2), "|u1").cpu().numpy()
-    params = device_view(p_params, (layer.N, layer.ngp, 2), "<f4").cpu().numpy()
+    recs = device_view(p_codes, (layer.N, rec), "|u1").cpu().numpy()
+    codes = np.ascontiguousarray(recs[:, :layer.d // 2])
+    params = np.ascontiguousarray(recs[:, layer.d // 2:]).view(np.float32).reshape(layer.N, layer.ngp, 2)
     return WdT, codes, params
 
 
