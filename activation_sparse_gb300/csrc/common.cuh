@@ -146,15 +146,24 @@ __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w <<
 __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
 // dot of 8 bf16 pairs packed in two uint4, accumulated into acc (fp32)
+// acc + sum of the 8 products a[e] * b[e] of bf16 pairs, in element order.
+// fma.rn.f32.bf16 takes the bf16 operands directly: their product is exact
+// in float32 and is added with one rounding, so the result is bit for bit
+// that of converting to float32 and calling fmaf, without the conversions.
+__device__ __forceinline__ float fma_bf16x2(uint32_t a, uint32_t b, float acc) {
+    asm("{\n\t.reg .b16 al, ah, bl, bh;\n\t"
+        "mov.b32 {al, ah}, %1;\n\tmov.b32 {bl, bh}, %2;\n\t"
+        "fma.rn.f32.bf16 %0, al, bl, %0;\n\tfma.rn.f32.bf16 %0, ah, bh, %0;\n\t}"
+        : "+f"(acc)
+        : "r"(a), "r"(b));
+    return acc;
+}
+
 __device__ __forceinline__ float dot8(const uint4 a, const uint4 b, float acc) {
-    acc = fmaf(bf_lo(a.x), bf_lo(b.x), acc);
-    acc = fmaf(bf_hi(a.x), bf_hi(b.x), acc);
-    acc = fmaf(bf_lo(a.y), bf_lo(b.y), acc);
-    acc = fmaf(bf_hi(a.y), bf_hi(b.y), acc);
-    acc = fmaf(bf_lo(a.z), bf_lo(b.z), acc);
-    acc = fmaf(bf_hi(a.z), bf_hi(b.z), acc);
-    acc = fmaf(bf_lo(a.w), bf_lo(b.w), acc);
-    acc = fmaf(bf_hi(a.w), bf_hi(b.w), acc);
+    acc = fma_bf16x2(a.x, b.x, acc);
+    acc = fma_bf16x2(a.y, b.y, acc);
+    acc = fma_bf16x2(a.z, b.z, acc);
+    acc = fma_bf16x2(a.w, b.w, acc);
     return acc;
 }
 
