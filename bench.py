@@ -590,9 +590,9 @@ def run_profile_case(args):
 
 # DRAM bytes (read + write) of one k_sparse_decode_b1 launch on one
 # Llama3.2-1B layer, from the ncu capture summarised in
-# profiles/k_sparse_decode_b1_llama3.2-1b_layer.md (40.3256 MB read, 7.4 KB
+# profiles/k_sparse_decode_b1_llama3.2-1b_layer.md (40.3226 MB read, 1.0 KB
 # written). Set to None whenever that kernel changes until it is re-captured.
-DECODE_TRAFFIC_BYTES = 40325632 + 7424
+DECODE_TRAFFIC_BYTES = 40322560 + 1024
 
 
 def main(argv=None):
