@@ -33,6 +33,8 @@ SIGNATURES = {
     "si_layer_destroy": (_i, [_vp]),
     "si_select_dynamic": (_i, [_vp, _vp, _i, _i, _i, _d, _vp, _vp, _vp]),
     "si_prefill_absact": (_i, [_vp, _vp, _i, _i, _vp, _vp]),
+    "si_set_gemm_tile": (_i, [_i]),
+    "si_gemm_tile_for": (_i, [_i, _i, _ip]),
     "si_select_from_absact": (_i, [_vp, _vp, _i, _i, _i, _i, _d, _vp, _vp, _vp, _vp]),
     "si_decode_plan": (_i, [_vp, _vp, _i, _i, _vp]),
     "si_sparse_ffn_decode": (_i, [_vp, _vp, _i, _i, _vp, _vp, _vp]),
@@ -209,6 +211,18 @@ def si_select_dynamic(layer: Layer, X, T, B, alpha, phi, S, absact_out=None, str
                                     _ptr(S, torch.int32, "S"), _ptr(absact_out, torch.float32, "absact_out"),
                                     _stream(stream)))
     return S
+
+
+def si_set_gemm_tile(bnn: int):
+    """Forces the activation GEMM's neuron-tile width (64, 80, 96, 112, 128) or, with 0, restores the per-launch choice."""
+    _check(load().si_set_gemm_tile(int(bnn)))
+
+
+def si_gemm_tile_for(M: int, N: int) -> int:
+    """The neuron-tile width a GEMM launch over M token rows and N neurons would use now."""
+    b = C.c_int(0)
+    _check(load().si_gemm_tile_for(int(M), int(N), C.byref(b)))
+    return b.value
 
 
 def si_prefill_absact(layer: Layer, X, T, B, absact_out, stream=None):

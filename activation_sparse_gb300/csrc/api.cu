@@ -378,14 +378,30 @@ int absact_core(si_layer* L, const uint16_t* X, int M, float* A, cudaStream_t st
 
 int si_prefill_absact(si_layer* L, const uint16_t* X, int T, int B, float* absact_out, void* stream) {
     if (!L || !X || !absact_out) return fail(SI_ERR_INVALID_ARG, "NULL pointer");
+    if (reinterpret_cast<uintptr_t>(absact_out) & 15u) return fail(SI_ERR_INVALID_ARG, "absact_out must be 16-byte aligned");
     if (T < 1 || B < 1) return fail(SI_ERR_INVALID_ARG, "need T, B >= 1");
     if ((long long)T * B > (1LL << 30) / L->n_pad) return fail(SI_ERR_INVALID_ARG, "T * B too large");
     return absact_core(L, X, T * B, absact_out, (cudaStream_t)stream);
 }
 
+int si_set_gemm_tile(int bnn) {
+    if (si::set_gemm_tile(bnn) != cudaSuccess) return fail(SI_ERR_INVALID_ARG, "bnn must be 0, 64, 80, 96, 112 or 128");
+    return SI_OK;
+}
+
+int si_gemm_tile_for(int M, int N, int* bnn) {
+    if (!bnn) return fail(SI_ERR_INVALID_ARG, "NULL pointer");
+    if (M < 1 || N < 1) return fail(SI_ERR_INVALID_ARG, "need M, N >= 1");
+    const int b = si::gemm_tile_for(M, N);
+    if (!b) return fail(SI_ERR_CUDA, "no current CUDA device");
+    *bnn = b;
+    return SI_OK;
+}
+
 int si_select_dynamic(si_layer* L, const uint16_t* X, int T, int B, int alpha, double phi, int32_t* S,
                       float* absact_out, void* stream) {
     if (!L || !X || !S) return fail(SI_ERR_INVALID_ARG, "NULL pointer");
+    if (reinterpret_cast<uintptr_t>(absact_out) & 15u) return fail(SI_ERR_INVALID_ARG, "absact_out must be 16-byte aligned");
     if (T < 1 || B < 1) return fail(SI_ERR_INVALID_ARG, "need T, B >= 1");
     if ((long long)T * B > (1LL << 30) / L->n_pad) return fail(SI_ERR_INVALID_ARG, "T * B too large");
     if (alpha < 1 || alpha > L->n_loaded) return fail(SI_ERR_INVALID_ARG, "need 1 <= alpha <= n_loaded");

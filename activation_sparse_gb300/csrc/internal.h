@@ -117,5 +117,9 @@ struct ActGemmParams {
     unsigned* err;
 };
 cudaError_t launch_act_gemm(const ActGemmParams& P, cudaStream_t st);
+// Neuron-tile width override for the activation GEMM (0 = per-launch choice).
+cudaError_t set_gemm_tile(int bnn);
+// The width a launch over M token rows and Nvalid neurons would use now.
+int gemm_tile_for(int M, int Nvalid);
 
 }  // namespace si

@@ -160,17 +160,33 @@ int si_layer_destroy(si_layer *layer);
  *       the static positions.
  *   X bf16 [B*T x d]; S int32 [B x n_sel] receives ascending packed
  *   positions, n_sel = si_count(phi, N); absact_out (optional, may be NULL)
- *   fp32 [B*T x n_pad] receives |A| (pad columns zero).
+ *   fp32 [B*T x n_pad], 16-byte aligned (the kernel stores it with TMA;
+ *   SI_ERR_INVALID_ARG otherwise), receives |A| (pad columns zero).
  * Requires 1 <= alpha <= n_loaded, n_static <= n_sel <= n_loaded, T, B >= 1. */
 int si_select_dynamic(si_layer *layer, const uint16_t *X, int T, int B, int alpha, double phi,
                       int32_t *S, float *absact_out, void *stream);
 
-/* Step a3 of si_select_dynamic alone: absact_out fp32 [B*T x n_pad] receives
- * |A| for every token row and packed position (pad columns zero), computed on
- * the tcgen05 tensor cores exactly as si_select_dynamic does. Together with
- * si_select_from_absact(layer, absact_out, n_pad, ...) it gives the same S. */
+/* Step a3 of si_select_dynamic alone: absact_out fp32 [B*T x n_pad], 16-byte
+ * aligned, receives |A| for every token row and packed position (pad columns
+ * zero), computed on the tcgen05 tensor cores exactly as si_select_dynamic
+ * does. Together with si_select_from_absact(layer, absact_out, n_pad, ...) it
+ * gives the same S. */
 int si_prefill_absact(si_layer *layer, const uint16_t *X, int T, int B, float *absact_out,
                       void *stream);
+
+/* Neuron-tile width of the activation GEMM behind si_profile_scores,
+ * si_select_dynamic and si_prefill_absact. Each launch covers 256 token rows
+ * by `bnn` neurons per CTA; bnn = 0 (the default) lets every launch pick,
+ * among 64, 80, 96, 112 and 128, the width that fills the GPU's SMs best;
+ * 64, 80, 96, 112 or 128 forces that width for every later launch in this
+ * process (any other value fails with SI_ERR_INVALID_ARG). A tuning and test
+ * knob: the width changes no result, since every output element sums its K
+ * products in the same order whatever the tile. */
+int si_set_gemm_tile(int bnn);
+
+/* The width (see si_set_gemm_tile) that a launch over M token rows and N
+ * neurons would use on the current device right now, in *bnn. */
+int si_gemm_tile_for(int M, int N, int *bnn);
 
 /* Steps a4..a6 of si_select_dynamic on a given |A| matrix (fp32 [B*T x ld],
  * ld >= n_loaded, finite; only the first n_loaded columns are read, and they

@@ -71,3 +71,14 @@ def test_validation_before_cuda(si):
     assert lib.spax_encode(p, 256, 10, 4, 100, C.byref(h), None) == si.SI_ERR_INVALID_ARG
     assert lib.si_merge_scores(None, None, 1, 4, p, None) == si.SI_ERR_INVALID_ARG
     assert lib.si_layer_destroy(None) == si.SI_OK
+    # the GEMM tile override only takes the widths the kernel is built for
+    for bad in (-1, 1, 48, 72, 129, 256):
+        assert lib.si_set_gemm_tile(bad) == si.SI_ERR_INVALID_ARG
+    for good in (64, 80, 96, 112, 128, 0):
+        assert lib.si_set_gemm_tile(good) == si.SI_OK
+    assert lib.si_gemm_tile_for(512, 5734, None) == si.SI_ERR_INVALID_ARG
+    # |A| goes out by TMA: a misaligned output is refused before any launch
+    odd = C.c_void_p(16 * 1024 + 4)
+    assert lib.si_prefill_absact(p, p, 4, 1, odd, None) == si.SI_ERR_INVALID_ARG
+    assert b"aligned" in lib.si_last_error_string()
+    assert lib.si_select_dynamic(p, p, 4, 1, 1, 0.4, p, odd, None) == si.SI_ERR_INVALID_ARG

@@ -108,3 +108,70 @@ def test_prefill_absact_matches_select_dynamic(si):
     assert np.array_equal(A1.numpy().view(np.uint32), A2.numpy().view(np.uint32))
     assert np.array_equal(S1.numpy(), S2.numpy())
     layer.close()
+
+
+GEMM_TILES = [64, 80, 96, 112, 128]
+
+
+@pytest.fixture
+def forced_tile(si):
+    yield si.si_set_gemm_tile
+    si.si_set_gemm_tile(0)
+
+
+@pytest.mark.parametrize("bnn", GEMM_TILES)
+def test_absact_every_tile_width(si, forced_tile, bnn):
+    """Each neuron-tile width gives bit-identical |A| (the K order of every
+    element is the same) and matches the oracle; ragged tokens and neurons,
+    two token tiles, several neuron tiles and a partial last one."""
+    d, N, T = 512, 1500, 300
+    Wg, Wu, Wd = synth.layer_weights(65, 0, d, N)
+    s = synth.lognormal_absact(65, 1, N)[0]
+    layer = si.si_pack_loaded(dev_bf16(Wg), dev_bf16(Wu), dev_bf16(Wd), dev(s), dev(s), 0.7, 0.2)
+    loaded, _ = oracle.rank_loaded(s, s, 0.7, 0.2)
+    X = synth.tokens(66, 0, synth.T_PROMPT, T, d)
+    Xd = dev_bf16(X)
+    forced_tile(0)
+    A0 = Guarded((T, layer.n_pad), torch().float32, fill=float("nan"))
+    si.si_prefill_absact(layer, Xd, T, 1, A0.t)
+    forced_tile(bnn)
+    A1 = Guarded((T, layer.n_pad), torch().float32, fill=float("nan"))
+    si.si_prefill_absact(layer, Xd, T, 1, A1.t)
+    got = A1.numpy()
+    assert np.array_equal(got.view(np.uint32), A0.numpy().view(np.uint32))
+    ref = oracle.absact(Wg, Wu, loaded, X)
+    err = np.abs(got[:, :layer.n_loaded] - ref)
+    assert err.max() <= 1e-3 * ref.max() + 1e-6, err.max() / ref.max()
+    assert not got[:, layer.n_loaded:].any()
+    layer.close()
+
+
+@pytest.mark.parametrize("bnn", GEMM_TILES)
+def test_profile_scores_every_tile_width(si, forced_tile, bnn):
+    d, N, T = 256, 1000, 600
+    Wg, Wu, _ = synth.layer_weights(67, 0, d, N)
+    X = synth.tokens(67, 0, synth.T_CALIB, T, d)
+    forced_tile(bnn)
+    scores = Guarded((N,), torch().float32, fill=0.0)
+    si.si_profile_scores(dev_bf16(Wg), dev_bf16(Wu), dev_bf16(X), scores.t)
+    ref = oracle.profile_scores(Wg, Wu, X)
+    rel = np.abs(scores.numpy().astype(np.float64) - ref) / np.maximum(ref, 1e-30)
+    assert rel.max() < 1e-3, rel.max()
+
+
+def test_tile_choice_fills_the_sms(si):
+    """The per-launch width minimises waves * (width + 24), wider on ties."""
+    sms = torch().cuda.get_device_properties(0).multi_processor_count
+
+    def cost(M, N, b):
+        ctas = -(-N // b) * -(-M // 256)
+        return -(-ctas // sms) * (b + 24)
+
+    for M, N in [(512, 5734), (4096, 8192), (1024, 5734), (256, 1000), (8 * 256, 8812), (512, 9728)]:
+        b = si.si_gemm_tile_for(M, N)
+        assert b in GEMM_TILES
+        best = min(cost(M, N, c) for c in GEMM_TILES)
+        assert cost(M, N, b) == best
+        assert all(cost(M, N, c) > best for c in GEMM_TILES if c > b)
+    if sms >= 144:
+        assert si.si_gemm_tile_for(512, 5734) == 80   # 144 CTAs instead of 90
