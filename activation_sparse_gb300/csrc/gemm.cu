@@ -222,6 +222,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_init(accum, 1);
         fence_mbar_init();
+    } else if (threadIdx.x == 32) {
+        // fetch the descriptors the first copies need while the barriers are set up
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_x)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_g)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_u)) : "memory");
     }
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
@@ -304,7 +309,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) {
                 tma_store_2d(&map_o, stage, n0, row0);
                 asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-                asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+                // the CTA may leave once the tile has been read out of shared
+                // memory; the global writes complete with the grid
+                asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
             }
             __syncwarp();
         }
