@@ -112,6 +112,8 @@ SEL_CASES = [
     (1000, 1.0, 0.3, 0.4, 50, 8, 1, "zeros"),             # all |A| equal (zero)
     (33, 1.0, 0.1, 0.5, 7, 9, 2, "ties"),                 # tiny, ragged word
     (256, 1.0, 0.1, 0.5, 200, 2100, 1, "lognormal"),      # counts above 2047: top-beta's general path
+    (600, 0.7, 0.2, 0.4, 64, 32, 1, "narrow"),            # every key in one top-digit bin: ranked directly
+    (1024, 0.7, 0.2, 0.4, 64, 32, 1, "narrow"),           # same, 717 keys: top-alpha's radix passes
 ]
 
 
@@ -120,6 +122,9 @@ def absact_of(kind, seed, rows, n, ld):
         A = synth.lognormal_absact(seed, rows, n)
     elif kind == "ties":
         A = synth.tie_heavy_absact(seed, rows, n, levels=6)
+    elif kind == "narrow":
+        # distinct values in [1, 1.12): one bin of the 11-bit top digit
+        A = (1.0 + 0.12 * np.random.default_rng(seed).random((rows, n))).astype(np.float32)
     else:
         A = np.zeros((rows, n), np.float32)
     out = np.full((rows, ld), 1e30, np.float32)   # columns past n_loaded must be ignored
