@@ -26,7 +26,9 @@
 // 4-stage shared-memory ring; warp 1 owns TMEM and lane 0 issues the MMAs
 // (tcgen05.commit releases a stage once its MMAs are done); warps 2..9 run
 // the epilogue, warp w reading TMEM lanes 32*(w%4) .. +31 of token half
-// (w-2)/4. All waits are bounded; TMEM is always released.
+// (w-2)/4. All waits are bounded; TMEM is always released. Launched with
+// programmatic dependent launch: barrier set-up, TMEM allocation and the
+// tensor-map prefetch overlap the previous launch in the stream.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -238,6 +240,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // The set-up above overlaps the previous launch's tail; X, the weights
+    // and the outputs may belong to that launch, so every thread waits for
+    // it before touching global memory, and lets the next launch begin
+    // scheduling.
+    grid_launch_dependents();
+    grid_dependency_wait();
 
     if (warp == 0) {
         if (lane == 0) {
@@ -402,9 +410,19 @@ cudaError_t launch_tile(const CUtensorMap& mx, const ActGemmParams& P, int mtile
     memset(&mo, 0, sizeof(mo));  // mode 1 writes no |A|
     if (P.mode == 0 && (e = make_out_map(&mo, P.out, P.Nvalid, P.M, P.ldo, BNN)) != cudaSuccess) return e;
     if ((e = allow_max_smem(k_act_gemm<BNN>)) != cudaSuccess) return e;
-    dim3 grid((P.Nvalid + BNN - 1) / BNN, mtiles);
-    k_act_gemm<BNN><<<grid, kThreads, GemmCfg<BNN>::SMEM_BYTES, st>>>(mx, mg, mu, mo, P);
-    return cudaGetLastError();
+    // programmatic dependent launch: this grid's set-up overlaps the tail of
+    // the previous launch in the stream (the kernel waits before any access)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((P.Nvalid + BNN - 1) / BNN, mtiles, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = GemmCfg<BNN>::SMEM_BYTES;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k_act_gemm<BNN>, mx, mg, mu, mo, P);
 }
 
 }  // namespace
