@@ -1194,11 +1194,11 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_tiered_down(TieredDownParams
     __syncthreads();  // the records are in place and the staged keys are no longer read
 
     if (warp == kConsWarps) {
-        // kIssueLanes lanes issue the copies, lane l the records l, l + 4, ...
+        // kIssueLanes lanes issue the copies, lane l the records l, l + 8, ...
         // (R is a multiple of 8, so every stage is filled by one lane, in
         // order): one lane alone cannot keep the small middle-column copies
         // flowing.
-        constexpr int kIssueLanes = 4;
+        constexpr int kIssueLanes = 8;
         if (lane < kIssueLanes) {
             const uint64_t pol = policy_evict_first();
             for (int i = lane; i < nrec; i += kIssueLanes) {
