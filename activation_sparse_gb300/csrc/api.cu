@@ -120,6 +120,7 @@ struct spax_layer {
     float* params = nullptr;    // inside the records: codes + d / 2 (not a separate allocation)
     int rec_bytes = 0;          // per-column record: d / 2 code bytes, then ngp (scale, min) pairs
     unsigned* hist = nullptr;  // tier histogram of the current a (zero between calls) + its ticket
+    int32_t* slab = nullptr;   // the histogram's per-bin member lists [kTierBins][kSlabCap]
     float* a = nullptr;
     float* part = nullptr;
     long long part_floats = 0;
@@ -161,6 +162,7 @@ void destroy_spax(spax_layer* L) {
     dfree(L->WdT);
     dfree(L->codes);
     dfree(L->hist);
+    dfree(L->slab);
     dfree(L->a);
     dfree(L->part);
     dfree(L->tickets);
@@ -560,7 +562,9 @@ int spax_encode(const uint16_t* Wd, int d, int N, int bits, int group, spax_laye
     int rc;
     if ((rc = dalloc(&L->WdT, (size_t)N * d, "column-major Wd")) ||
         (rc = dalloc(&L->codes, (size_t)N * (d / 2 + 8 * L->ngp), "code records")) ||
-        (rc = dalloc(&L->hist, si::kTierBins + 1, "tier histogram")) || (rc = dalloc(&L->a, N, "activations")) ||
+        (rc = dalloc(&L->hist, si::kTierBins + 1, "tier histogram")) ||
+        (rc = dalloc(&L->slab, (size_t)si::kTierBins * si::kSlabCap, "tier member lists")) ||
+        (rc = dalloc(&L->a, N, "activations")) ||
         (rc = dalloc(&L->tickets, 16, "tickets")) || (rc = grow_part(&L->part, &L->part_floats, d, 1))) {
         destroy_spax(L);
         return rc;
@@ -609,7 +613,7 @@ int spax_layer_destroy(spax_layer* L) {
 namespace {
 
 int dense_act_core(const uint16_t* Wg, const uint16_t* Wu, int d, int N, const uint16_t* x, float* a, unsigned* hist,
-                   cudaStream_t stream) {
+                   int32_t* slab, cudaStream_t stream) {
     if (!Wg || !Wu || !x || !a) return fail(SI_ERR_INVALID_ARG, "NULL pointer");
     if (d < 8 || d % 8 || N < 1) return fail(SI_ERR_INVALID_ARG, "need d % 8 == 0, N >= 1");
     if (d > 4096) return fail(SI_ERR_UNSUPPORTED, "dense activation pass supports d <= 4096");
@@ -624,6 +628,7 @@ int dense_act_core(const uint16_t* Wg, const uint16_t* Wu, int d, int N, const u
     P.x = x;
     P.a = a;
     P.hist = hist;
+    P.slab = hist ? slab : nullptr;
     P.err = err;
     P.R = si::dense_act_stages(d);
     if (P.R < 8) return fail(SI_ERR_UNSUPPORTED, "d too large for the activation ring");
@@ -653,6 +658,7 @@ int tiered_core(spax_layer* L, const float* a, long long k_top, long long k_mid,
     P.rec_bytes = L->rec_bytes;
     P.a = a;
     P.hist = L->hist;
+    P.slab = L->slab;
     P.top_out = top_out;
     P.mid_out = mid_out;
     P.d = L->d;
@@ -679,7 +685,7 @@ int tiered_core(spax_layer* L, const float* a, long long k_top, long long k_mid,
 extern "C" {
 
 int spax_dense_act(const uint16_t* Wg, const uint16_t* Wu, int d, int N, const uint16_t* x, float* a, void* stream) {
-    return dense_act_core(Wg, Wu, d, N, x, a, nullptr, (cudaStream_t)stream);
+    return dense_act_core(Wg, Wu, d, N, x, a, nullptr, nullptr, (cudaStream_t)stream);
 }
 
 int spax_tiered_down(spax_layer* L, const float* a, double top_frac, double mid_frac, float* y, int32_t* top_idx,
@@ -689,7 +695,7 @@ int spax_tiered_down(spax_layer* L, const float* a, double top_frac, double mid_
     int rc = tier_counts(L, top_frac, mid_frac, &k_top, &k_mid);
     if (rc) return rc;
     cudaStream_t st = (cudaStream_t)stream;
-    SI_CK(si::launch_abs_hist(a, L->N, L->hist, st));
+    SI_CK(si::launch_abs_hist(a, L->N, L->hist, L->slab, st));
     return tiered_core(L, a, k_top, k_mid, y, top_idx, mid_idx, st);
 }
 
@@ -702,7 +708,7 @@ int spax_ffn_decode(spax_layer* L, const uint16_t* Wg, const uint16_t* Wu, const
     cudaStream_t st = (cudaStream_t)stream;
     float* a = a_out ? a_out : L->a;
     // the dense pass builds the tier histogram of a as it writes it
-    if ((rc = dense_act_core(Wg, Wu, L->d, L->N, x, a, L->hist, st))) return rc;
+    if ((rc = dense_act_core(Wg, Wu, L->d, L->N, x, a, L->hist, L->slab, st))) return rc;
     if ((rc = tiered_core(L, a, k_top, k_mid, y, nullptr, nullptr, st))) {
         cudaMemsetAsync(L->hist, 0, (si::kTierBins + 1) * sizeof(unsigned), st);  // leave it clean
         return rc;

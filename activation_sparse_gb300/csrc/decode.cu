@@ -640,6 +640,11 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_dense_act(DenseActParams P) 
             const int c = lane + 32 * j;
             xr[j] = (c < d / 8) ? reinterpret_cast<const uint4*>(s_x)[c] : make_uint4(0u, 0u, 0u, 0u);
         }
+        // the histogram slot of this warp's previous record: its slab entry
+        // is written one record later, so the atomic's round trip overlaps
+        // the next record's dot products
+        uint32_t pend_pos = 0xFFFFFFFFu, pend_bin = 0u;
+        int pend_n = -1;
         for (int i = warp; i < cnt; i += kConsWarps) {
             const int s = i % R;
             mbar_wait(&full[s], (uint32_t)((i / R) & 1), P.err, kSiteDenseAct | kSiteFull);
@@ -659,17 +664,31 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_dense_act(DenseActParams P) 
             if (lane == 0) {
                 const float av = swiglu(g, u);
                 P.a[lo + i] = av;
-                if (P.hist) atomicAdd(P.hist + (abs_key(av) >> kTierShift), 1u);
                 mbar_arrive(&empty[s]);
+                if (P.hist) {
+                    if (P.slab) {
+                        if (pend_pos < (uint32_t)kSlabCap) P.slab[(size_t)pend_bin * kSlabCap + pend_pos] = pend_n;
+                        pend_bin = abs_key(av) >> kTierShift;
+                        pend_pos = atomicAdd(P.hist + pend_bin, 1u);
+                        pend_n = lo + i;
+                    } else {
+                        atomicAdd(P.hist + (abs_key(av) >> kTierShift), 1u);
+                    }
+                }
             }
         }
+        if (lane == 0 && pend_pos < (uint32_t)kSlabCap) P.slab[(size_t)pend_bin * kSlabCap + pend_pos] = pend_n;
     }
 }
 
 // Tier histogram of a given activation vector, for a tiered call whose a
-// did not come from the dense pass (which builds the same histogram).
-__global__ void __launch_bounds__(256) k_abs_hist(const float* __restrict__ a, int N, unsigned* __restrict__ hist) {
+// did not come from the dense pass (which builds the same histogram), and
+// its per-bin member lists: each CTA reserves one run of slots per bin with
+// a single global atomic, then places its members by shared-memory rank.
+__global__ void __launch_bounds__(256) k_abs_hist(const float* __restrict__ a, int N, unsigned* __restrict__ hist,
+                                                 int32_t* __restrict__ slab) {
     __shared__ unsigned h[kTierBins];
+    __shared__ unsigned base[kTierBins];
     grid_launch_dependents();
     grid_dependency_wait();  // a may be the previous grid's output
     for (int i = threadIdx.x; i < kTierBins; i += blockDim.x) h[i] = 0u;
@@ -677,8 +696,17 @@ __global__ void __launch_bounds__(256) k_abs_hist(const float* __restrict__ a, i
     for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < N; i += gridDim.x * blockDim.x)
         atomicAdd(&h[abs_key(__ldcg(a + i)) >> kTierShift], 1u);
     __syncthreads();
-    for (int i = threadIdx.x; i < kTierBins; i += blockDim.x)
-        if (h[i]) atomicAdd(hist + i, h[i]);
+    for (int i = threadIdx.x; i < kTierBins; i += blockDim.x) {
+        base[i] = h[i] ? atomicAdd(hist + i, h[i]) : 0u;
+        h[i] = 0u;
+    }
+    if (!slab) return;
+    __syncthreads();
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < N; i += gridDim.x * blockDim.x) {
+        const uint32_t bin = abs_key(__ldcg(a + i)) >> kTierShift;
+        const uint32_t pos = base[bin] + atomicAdd(&h[bin], 1u);
+        if (pos < (uint32_t)kSlabCap) slab[(size_t)bin * kSlabCap + pos] = i;
+    }
 }
 
 // ---------------------------------------------------------- tiered down
@@ -997,28 +1025,42 @@ __device__ bool tier_own_range(const TieredDownParams& P, const float* s_a, int*
         }
         return m;
     };
-    uint32_t n = 0u;
-    if (act[0] || act[1])
-        for (int q = q_lo; q < q_hi; ++q) n += __popc(quad_matches(q));
-    uint32_t incl = n;  // lanes' counts, inclusive scan
+    // When both boundary bins fit their member lists (filled by the pass that
+    // built the histogram), the candidates are read from those lists rather
+    // than found by a scan of every key; their order does not matter below.
+    const bool two = act[1] && !(act[0] && d0[1] == d0[0]);
+    const uint32_t h0 = act[0] ? s_hist[0][d0[0]] : 0u, h1 = two ? s_hist[0][d0[1]] : 0u;
+    uint32_t C;
+    if (P.slab && h0 <= (uint32_t)kSlabCap && h1 <= (uint32_t)kSlabCap && h0 + h1 <= (uint32_t)cap) {
+        C = h0 + h1;
+        const uint32_t b0 = act[0] ? d0[0] : d0[1];  // the first list's bin
+        for (uint32_t c = (uint32_t)tid; c < C; c += blockDim.x)
+            cand[c] = __ldcg(P.slab + (c < h0 ? (size_t)b0 * kSlabCap + c : (size_t)d0[1] * kSlabCap + (c - h0)));
+        __syncthreads();
+    } else {
+        uint32_t n = 0u;
+        if (act[0] || act[1])
+            for (int q = q_lo; q < q_hi; ++q) n += __popc(quad_matches(q));
+        uint32_t incl = n;  // lanes' counts, inclusive scan
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-        if (lane >= o) incl += v;
-    }
-    uint32_t wbase, unused0, C, unused1;
-    cta_scan2(__shfl_sync(0xFFFFFFFFu, incl, 31), 0u, s_w, wbase, unused0, C, unused1);
-    if (C > (uint32_t)cap) return false;  // the same decision in every thread
-    if (n) {
-        uint32_t pos = wbase + incl - n;
-        for (int q = q_lo; q < q_hi; ++q) {
-            const uint32_t m = quad_matches(q);
-#pragma unroll
-            for (int u = 0; u < 4; ++u)
-                if (m & (1u << u)) cand[pos++] = 4 * q + u;
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+            if (lane >= o) incl += v;
         }
+        uint32_t wbase, unused0, unused1;
+        cta_scan2(__shfl_sync(0xFFFFFFFFu, incl, 31), 0u, s_w, wbase, unused0, C, unused1);
+        if (C > (uint32_t)cap) return false;  // the same decision in every thread
+        if (n) {
+            uint32_t pos = wbase + incl - n;
+            for (int q = q_lo; q < q_hi; ++q) {
+                const uint32_t m = quad_matches(q);
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    if (m & (1u << u)) cand[pos++] = 4 * q + u;
+            }
+        }
+        __syncthreads();
     }
-    __syncthreads();
 
     // both thresholds: bits 19..9, then 8..0, over the candidates
     const uint32_t pre1[2] = {d0[0], d0[1]};
@@ -1609,7 +1651,7 @@ cudaError_t launch_tiered_down(TieredDownParams P, cudaStream_t st) {
     return launch_clustered(k_tiered_down<1>, grid, cluster, smem, st, args, /*pdl=*/true);
 }
 
-cudaError_t launch_abs_hist(const float* a, int N, unsigned* hist, cudaStream_t st) {
+cudaError_t launch_abs_hist(const float* a, int N, unsigned* hist, int32_t* slab, cudaStream_t st) {
     int dev = 0, sms = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -1626,7 +1668,7 @@ cudaError_t launch_abs_hist(const float* a, int N, unsigned* hist, cudaStream_t 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, k_abs_hist, a, N, hist);
+    return cudaLaunchKernelEx(&cfg, k_abs_hist, a, N, hist, slab);
 }
 
 int streaming_grid_upper_bound() {

@@ -35,6 +35,10 @@ struct SparseDecodeParams {
 // ticket of the CTAs that have read it (the last one re-zeroes everything).
 constexpr int kTierBins = 2048;
 constexpr int kTierShift = 20;
+// Per-bin member lists of the tier histogram ("slabs"): bin b's first
+// kSlabCap members (neuron indices, any order) at slab + b * kSlabCap. A bin
+// whose count exceeds kSlabCap has an incomplete list and is not read.
+constexpr int kSlabCap = 512;
 
 struct DenseActParams {
     const uint16_t* Wg;
@@ -43,6 +47,7 @@ struct DenseActParams {
     const uint16_t* x;
     float* a;
     unsigned* hist;           // optional tier histogram of a (kTierBins + 1 words, zero on entry)
+    int32_t* slab;            // optional per-bin member lists of hist ([kTierBins][kSlabCap]); needs hist
     unsigned* err;
     int R;
 };
@@ -53,6 +58,7 @@ struct TieredDownParams {
     int rec_bytes;
     const float* a;           // [N]
     unsigned* hist;           // tier histogram of a (kTierBins + 1 words), re-zeroed by the kernel
+    const int32_t* slab;      // optional per-bin member lists of hist (see kSlabCap)
     int32_t* top_out;         // optional [k_top]: the top tier, ascending
     int32_t* mid_out;         // optional [k_mid]: the middle tier, ascending
     int d, group, ngp, k_top, k_mid;
@@ -94,7 +100,7 @@ int decode_max_partial_floats(int d, int B);
 cudaError_t launch_sparse_decode(SparseDecodeParams P, int B, cudaStream_t st);
 int dense_act_stages(int d);
 cudaError_t launch_dense_act(DenseActParams P, cudaStream_t st);
-cudaError_t launch_abs_hist(const float* a, int N, unsigned* hist, cudaStream_t st);
+cudaError_t launch_abs_hist(const float* a, int N, unsigned* hist, int32_t* slab, cudaStream_t st);
 int tiered_down_stages(int d, int aux_floats);
 cudaError_t launch_tiered_down(TieredDownParams P, cudaStream_t st);
 int streaming_grid_upper_bound();
