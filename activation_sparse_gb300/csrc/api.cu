@@ -118,7 +118,7 @@ struct spax_layer {
     uint16_t* WdT = nullptr;
     uint8_t* codes = nullptr;
     float* params = nullptr;    // inside the records: codes + d / 2 (not a separate allocation)
-    int rec_bytes = 0;          // per-column record: d / 2 code bytes, then ngp (scale, min) pairs
+    int rec_bytes = 0;          // per-column record: d * bits / 8 code bytes, then ngp (scale, min) pairs
     unsigned* hist = nullptr;  // tier histogram of the current a (zero between calls) + its ticket
     int32_t* slab = nullptr;   // the histogram's per-bin member lists [kTierBins][kSlabCap]
     float* a = nullptr;
@@ -544,7 +544,7 @@ int spax_encode(const uint16_t* Wd, int d, int N, int bits, int group, spax_laye
     if (!out) return fail(SI_ERR_INVALID_ARG, "out is NULL");
     *out = nullptr;
     if (!Wd) return fail(SI_ERR_INVALID_ARG, "NULL pointer");
-    if (bits != 4) return fail(SI_ERR_UNSUPPORTED, "only 4-bit codes are implemented");
+    if (bits != 2 && bits != 4 && bits != 8) return fail(SI_ERR_UNSUPPORTED, "codes are 2, 4 or 8 bits wide");
     if (group < 8 || (group & (group - 1)) || d < 64 || d % 64 || d % group)
         return fail(SI_ERR_INVALID_ARG, "need group a power of two >= 8, d % 64 == 0, d % group == 0");
     if (d > 4096) return fail(SI_ERR_UNSUPPORTED, "tiered decode supports d <= 4096");
@@ -558,10 +558,10 @@ int spax_encode(const uint16_t* Wd, int d, int N, int bits, int group, spax_laye
     L->bits = bits;
     L->group = group;
     L->ngp = round_up(d / group, 2);
-    L->rec_bytes = d / 2 + 8 * L->ngp;
+    L->rec_bytes = d * bits / 8 + 8 * L->ngp;
     int rc;
     if ((rc = dalloc(&L->WdT, (size_t)N * d, "column-major Wd")) ||
-        (rc = dalloc(&L->codes, (size_t)N * (d / 2 + 8 * L->ngp), "code records")) ||
+        (rc = dalloc(&L->codes, (size_t)N * L->rec_bytes, "code records")) ||
         (rc = dalloc(&L->hist, si::kTierBins + 1, "tier histogram")) ||
         (rc = dalloc(&L->slab, (size_t)si::kTierBins * si::kSlabCap, "tier member lists")) ||
         (rc = dalloc(&L->a, N, "activations")) ||
@@ -569,11 +569,12 @@ int spax_encode(const uint16_t* Wd, int d, int N, int bits, int group, spax_laye
         destroy_spax(L);
         return rc;
     }
-    L->params = reinterpret_cast<float*>(L->codes + d / 2);
+    L->params = reinterpret_cast<float*>(L->codes + d * bits / 8);
     cudaError_t e = cudaMemsetAsync(L->tickets, 0, 16 * sizeof(unsigned), st);
     if (e == cudaSuccess) e = cudaMemsetAsync(L->hist, 0, (si::kTierBins + 1) * sizeof(unsigned), st);
     if (e == cudaSuccess) e = cudaMemsetAsync(L->codes, 0, (size_t)N * L->rec_bytes, st);
-    if (e == cudaSuccess) e = si::launch_spax_encode(Wd, d, N, group, L->ngp, L->WdT, L->codes, L->rec_bytes, st);
+    if (e == cudaSuccess)
+        e = si::launch_spax_encode(Wd, d, N, bits, group, L->ngp, L->WdT, L->codes, L->rec_bytes, st);
     if (e == cudaSuccess) e = cudaStreamSynchronize(st);
     if (e != cudaSuccess) {
         destroy_spax(L);
@@ -656,6 +657,7 @@ int tiered_core(spax_layer* L, const float* a, long long k_top, long long k_mid,
     P.WdT = L->WdT;
     P.codes = L->codes;
     P.rec_bytes = L->rec_bytes;
+    P.bits = L->bits;
     P.a = a;
     P.hist = L->hist;
     P.slab = L->slab;

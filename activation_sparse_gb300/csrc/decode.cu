@@ -10,8 +10,8 @@
 //                      sequences that selected it).
 //  k_dense_act         SpAx dense gate/up pass: a[n] for every neuron.
 //  k_tiered_down       SpAx three-tier down-projection (abstract, Fig. 2/3):
-//                      top columns in bf16, middle columns rebuilt from 4-bit
-//                      codes (min + q * scale), the rest never read.
+//                      top columns in bf16, middle columns rebuilt from 2-, 4-
+//                      or 8-bit codes (min + q * scale), the rest never read.
 //
 // Common structure (warp-specialised, one CTA per SM):
 //   * the producer warp streams whole records into a ring of shared-memory
@@ -1140,11 +1140,11 @@ __device__ bool tier_own_range(const TieredDownParams& P, const float* s_a, int*
 // registers (lane l holds chunks l + 32 j of 8 columns). The partials meet
 // in shared memory at the end and the CTAs' sums are reduced through the
 // cluster and a fixed-order final pass (deterministic).
-template <int MAXC>
+template <int MAXC, int BITS>
 __global__ void __launch_bounds__(kDecThreads, 1) k_tiered_down(TieredDownParams P) {
     extern __shared__ __align__(1024) uint8_t smem[];
     const int d = P.d;
-    const int mid_bytes = P.rec_bytes;  // d / 2 code bytes, then ngp (scale, min) pairs
+    const int mid_bytes = P.rec_bytes;  // d * BITS / 8 code bytes, then ngp (scale, min) pairs
     const RingLayout L = ring_layout(P.R, 2 * d, P.aux_floats * 4, 0);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.off_full);
     uint64_t* empty = reinterpret_cast<uint64_t*>(smem + L.off_empty);
@@ -1292,33 +1292,52 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_tiered_down(TieredDownParams
                     }
                 }
             } else {
-                const float2* prm = reinterpret_cast<const float2*>(st + d / 2);
+                const float2* prm = reinterpret_cast<const float2*>(st + (d * BITS) / 8);
 #pragma unroll
                 for (int j = 0; j < XJ; ++j) {
                     const int c = lane + 32 * j;
                     if (c < nch) {
-                        const uint32_t q = reinterpret_cast<const uint32_t*>(st)[c];
                         const float2 sm = prm[(8 * c) >> gshift];  // (scale, min)
                         const float c1 = av * sm.x, c0 = av * sm.y;
                         if constexpr (kSepMin) amin[j] += c0;
-                        // acc += c1 * code (+ c0 unless it is kept apart)
+                        // acc += c1 * code (+ c0 unless it is kept apart); a code
+                        // arrives as the float bits of 2^23 + code, exact for
+                        // codes below 2^23, and 2^23 is subtracted
                         auto mac = [&](float& acc_e, uint32_t word) {
                             const float qf = __uint_as_float(word) - 8388608.0f;
                             if constexpr (kSepMin) acc_e = fmaf(c1, qf, acc_e);
                             else acc_e = fmaf(c1, qf, acc_e + c0);
                         };
-                        // codes of elements 0,2,4,6 (low nibbles) and 1,3,5,7 (high
-                        // nibbles) as bytes; byte -> float exactly as the float
-                        // 2^23 + code minus 2^23
-                        const uint32_t lo = q & 0x0F0F0F0Fu, hi = (q >> 4) & 0x0F0F0F0Fu;
-                        mac(acc[j][0], __byte_perm(lo, 0x4B000000u, 0x7440));
-                        mac(acc[j][1], __byte_perm(hi, 0x4B000000u, 0x7440));
-                        mac(acc[j][2], __byte_perm(lo, 0x4B000000u, 0x7441));
-                        mac(acc[j][3], __byte_perm(hi, 0x4B000000u, 0x7441));
-                        mac(acc[j][4], __byte_perm(lo, 0x4B000000u, 0x7442));
-                        mac(acc[j][5], __byte_perm(hi, 0x4B000000u, 0x7442));
-                        mac(acc[j][6], __byte_perm(lo, 0x4B000000u, 0x7443));
-                        mac(acc[j][7], __byte_perm(hi, 0x4B000000u, 0x7443));
+                        // the eight codes of chunk c: element i at bit i * BITS
+                        if constexpr (BITS == 4) {
+                            // elements 0,2,4,6 in the low nibbles, 1,3,5,7 in the high ones
+                            const uint32_t q = reinterpret_cast<const uint32_t*>(st)[c];
+                            const uint32_t lo = q & 0x0F0F0F0Fu, hi = (q >> 4) & 0x0F0F0F0Fu;
+                            mac(acc[j][0], __byte_perm(lo, 0x4B000000u, 0x7440));
+                            mac(acc[j][1], __byte_perm(hi, 0x4B000000u, 0x7440));
+                            mac(acc[j][2], __byte_perm(lo, 0x4B000000u, 0x7441));
+                            mac(acc[j][3], __byte_perm(hi, 0x4B000000u, 0x7441));
+                            mac(acc[j][4], __byte_perm(lo, 0x4B000000u, 0x7442));
+                            mac(acc[j][5], __byte_perm(hi, 0x4B000000u, 0x7442));
+                            mac(acc[j][6], __byte_perm(lo, 0x4B000000u, 0x7443));
+                            mac(acc[j][7], __byte_perm(hi, 0x4B000000u, 0x7443));
+                        } else if constexpr (BITS == 8) {
+                            // one byte per element
+                            const uint2 q = reinterpret_cast<const uint2*>(st)[c];
+                            mac(acc[j][0], __byte_perm(q.x, 0x4B000000u, 0x7440));
+                            mac(acc[j][1], __byte_perm(q.x, 0x4B000000u, 0x7441));
+                            mac(acc[j][2], __byte_perm(q.x, 0x4B000000u, 0x7442));
+                            mac(acc[j][3], __byte_perm(q.x, 0x4B000000u, 0x7443));
+                            mac(acc[j][4], __byte_perm(q.y, 0x4B000000u, 0x7440));
+                            mac(acc[j][5], __byte_perm(q.y, 0x4B000000u, 0x7441));
+                            mac(acc[j][6], __byte_perm(q.y, 0x4B000000u, 0x7442));
+                            mac(acc[j][7], __byte_perm(q.y, 0x4B000000u, 0x7443));
+                        } else {
+                            // BITS == 2: sixteen bits per chunk, element e at bits 2e, 2e + 1
+                            const uint32_t q = reinterpret_cast<const uint16_t*>(st)[c];
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) mac(acc[j][e], 0x4B000000u | ((q >> (2 * e)) & 3u));
+                        }
                     }
                 }
             }
@@ -1470,7 +1489,7 @@ struct GridCache {
 
 template <class K>
 cudaError_t cached_grid(K kernel, size_t smem, int* grid, int* cluster) {
-    static thread_local GridCache cache[32];
+    static thread_local GridCache cache[64];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -1628,15 +1647,11 @@ int tiered_down_stages(int d, int aux_floats) {
     return (R >= kConsWarps && (long long)R * stage >= need) ? R : 0;
 }
 
-cudaError_t launch_tiered_down(TieredDownParams P, cudaStream_t st) {
-    const size_t smem = (size_t)ring_layout(P.R, 2 * P.d, P.aux_floats * 4, 0).total;
+template <int MAXC, int BITS>
+cudaError_t launch_tiered(TieredDownParams& P, size_t smem, cudaStream_t st) {
+    auto kern = k_tiered_down<MAXC, BITS>;
     int grid = 0, cluster = 0;
-    cudaError_t e;
-    if (P.d > 2048) {
-        e = cached_grid(k_tiered_down<2>, smem, &grid, &cluster);
-    } else {
-        e = cached_grid(k_tiered_down<1>, smem, &grid, &cluster);
-    }
+    cudaError_t e = cached_grid(kern, smem, &grid, &cluster);
     if (e != cudaSuccess) return e;
     if (P.part_floats < (long long)(grid / cluster) * P.d) return cudaErrorInvalidValue;
     // per-CTA record counts (rank windows, or an own range of N / grid
@@ -1647,8 +1662,18 @@ cudaError_t launch_tiered_down(TieredDownParams P, cudaStream_t st) {
     if (own > per) per = own;
     if (2 * per > P.aux_floats) return cudaErrorInvalidValue;
     void* args[] = {&P};
-    if (P.d > 2048) return launch_clustered(k_tiered_down<2>, grid, cluster, smem, st, args, /*pdl=*/true);
-    return launch_clustered(k_tiered_down<1>, grid, cluster, smem, st, args, /*pdl=*/true);
+    return launch_clustered(kern, grid, cluster, smem, st, args, /*pdl=*/true);
+}
+
+cudaError_t launch_tiered_down(TieredDownParams P, cudaStream_t st) {
+    const size_t smem = (size_t)ring_layout(P.R, 2 * P.d, P.aux_floats * 4, 0).total;
+    const bool wide = P.d > 2048;
+    switch (P.bits) {
+        case 2: return wide ? launch_tiered<2, 2>(P, smem, st) : launch_tiered<1, 2>(P, smem, st);
+        case 4: return wide ? launch_tiered<2, 4>(P, smem, st) : launch_tiered<1, 4>(P, smem, st);
+        case 8: return wide ? launch_tiered<2, 8>(P, smem, st) : launch_tiered<1, 8>(P, smem, st);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 cudaError_t launch_abs_hist(const float* a, int N, unsigned* hist, int32_t* slab, cudaStream_t st) {

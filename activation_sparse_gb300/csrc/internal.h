@@ -54,8 +54,9 @@ struct DenseActParams {
 
 struct TieredDownParams {
     const uint16_t* WdT;      // [N][d] bf16
-    const uint8_t* codes;     // [N] records of rec_bytes: d/2 code bytes, then ngp (scale, min) pairs
+    const uint8_t* codes;     // [N] records of rec_bytes: d*bits/8 code bytes, then ngp (scale, min) pairs
     int rec_bytes;
+    int bits;                 // code width: 2, 4 or 8
     const float* a;           // [N]
     unsigned* hist;           // tier histogram of a (kTierBins + 1 words), re-zeroed by the kernel
     const int32_t* slab;      // optional per-bin member lists of hist (see kSlabCap)
@@ -87,8 +88,8 @@ cudaError_t launch_merge_scores(const float* const* s, const float* tok, int nfi
 // pack.cu
 cudaError_t launch_pack_loaded(const uint16_t* Wg, const uint16_t* Wu, const uint16_t* Wd, int d, int N,
                                const int32_t* loaded, int n_loaded, int n_pad, uint16_t* packed, cudaStream_t st);
-cudaError_t launch_spax_encode(const uint16_t* Wd, int d, int N, int group, int ngp, uint16_t* WdT, uint8_t* recs,
-                               int rec_bytes, cudaStream_t st);
+cudaError_t launch_spax_encode(const uint16_t* Wd, int d, int N, int bits, int group, int ngp, uint16_t* WdT,
+                               uint8_t* recs, int rec_bytes, cudaStream_t st);
 
 // api.cu: sets the message si_last_error_string() returns on this thread
 void set_error_message(const char* msg);

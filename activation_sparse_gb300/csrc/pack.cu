@@ -7,8 +7,8 @@
 //                  sum over neurons, so the records can sit in any order; this
 //                  library keeps ascending neuron index).
 //  k_spax_encode   SpAx offline encoding (Fig. 2, Fig. 3): per column and
-//                  per row group, float32 min / max / scale and 4-bit codes,
-//                  plus a column-major bf16 copy of Wd so that a top-tier
+//                  per row group, float32 min / max / scale and 2-, 4- or
+//                  8-bit codes, plus a column-major bf16 copy of Wd so that a top-tier
 //                  column is one contiguous read. A column's codes and its
 //                  (scale, min) pairs form one record, so a middle-tier
 //                  column is one contiguous read too.
@@ -52,13 +52,16 @@ __global__ void __launch_bounds__(256) k_pack_loaded(const uint16_t* __restrict_
 }
 
 // grid (ceil(N/32), d/group); block 256 = 8 warps, each warp owns 4 columns.
-// Column n's record at recs + n * rec_bytes: d/2 code bytes, then ngp
-// (scale, min) float pairs.
+// Column n's record at recs + n * rec_bytes: d * BITS / 8 code bytes (element
+// i at bit i * BITS, little-endian), then ngp (scale, min) float pairs.
 // All quantisation arithmetic is float32 with explicit round-to-nearest
 // intrinsics (no contraction), so codes are reproducible bit for bit.
+template <int BITS>
 __global__ void __launch_bounds__(256) k_spax_encode(const uint16_t* __restrict__ Wd, int d, int N, int group,
                                                     int ngp, uint16_t* __restrict__ WdT,
                                                     uint8_t* __restrict__ recs, int rec_bytes) {
+    constexpr int EPB = 8 / BITS;            // codes per byte
+    constexpr int QMAX = (1 << BITS) - 1;
     extern __shared__ __align__(16) uint16_t s_tile[];  // [group][33]
     const int n0 = blockIdx.x * 32;
     const int g = blockIdx.y;
@@ -83,11 +86,11 @@ __global__ void __launch_bounds__(256) k_spax_encode(const uint16_t* __restrict_
             mn = fminf(mn, __shfl_xor_sync(0xFFFFFFFFu, mn, o));
             mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
         }
-        const float scale = __fdiv_rn(__fsub_rn(mx, mn), 15.0f);
-        for (int r = 2 * tx; r < group; r += 64) {
-            int q[2];
+        const float scale = __fdiv_rn(__fsub_rn(mx, mn), (float)QMAX);
+        for (int r = EPB * tx; r < group; r += 32 * EPB) {
+            uint32_t byte = 0u;
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
+            for (int h = 0; h < EPB; ++h) {
                 const uint16_t hb = s_tile[(r + h) * 33 + cc];
                 WdT[(size_t)n * d + r0 + r + h] = hb;
                 const float w = __uint_as_float((uint32_t)hb << 16);
@@ -96,14 +99,14 @@ __global__ void __launch_bounds__(256) k_spax_encode(const uint16_t* __restrict_
                     float t = __fdiv_rn(__fsub_rn(w, mn), scale);
                     t = __fadd_rn(t, 0.5f);
                     v = (int)floorf(t);
-                    v = v < 0 ? 0 : (v > 15 ? 15 : v);
+                    v = v < 0 ? 0 : (v > QMAX ? QMAX : v);
                 }
-                q[h] = v;
+                byte |= (uint32_t)v << (h * BITS);
             }
-            recs[(size_t)n * rec_bytes + (r0 + r) / 2] = (uint8_t)(q[0] | (q[1] << 4));
+            recs[(size_t)n * rec_bytes + (r0 + r) / EPB] = (uint8_t)byte;
         }
         if (tx == 0) {
-            float* prm = reinterpret_cast<float*>(recs + (size_t)n * rec_bytes + d / 2);
+            float* prm = reinterpret_cast<float*>(recs + (size_t)n * rec_bytes + (size_t)d * BITS / 8);
             prm[g * 2 + 0] = scale;
             prm[g * 2 + 1] = mn;
         }
@@ -116,13 +119,27 @@ cudaError_t launch_pack_loaded(const uint16_t* Wg, const uint16_t* Wu, const uin
     return cudaGetLastError();
 }
 
-cudaError_t launch_spax_encode(const uint16_t* Wd, int d, int N, int group, int ngp, uint16_t* WdT, uint8_t* recs,
-                               int rec_bytes, cudaStream_t st) {
+cudaError_t launch_spax_encode(const uint16_t* Wd, int d, int N, int bits, int group, int ngp, uint16_t* WdT,
+                               uint8_t* recs, int rec_bytes, cudaStream_t st) {
     const size_t smem = (size_t)group * 33 * 2;
-    cudaError_t e = allow_max_smem(k_spax_encode);
-    if (e != cudaSuccess) return e;
     dim3 grid((N + 31) / 32, d / group);
-    k_spax_encode<<<grid, 256, smem, st>>>(Wd, d, N, group, ngp, WdT, recs, rec_bytes);
+    cudaError_t e;
+    switch (bits) {
+        case 2:
+            if ((e = allow_max_smem(k_spax_encode<2>)) != cudaSuccess) return e;
+            k_spax_encode<2><<<grid, 256, smem, st>>>(Wd, d, N, group, ngp, WdT, recs, rec_bytes);
+            break;
+        case 4:
+            if ((e = allow_max_smem(k_spax_encode<4>)) != cudaSuccess) return e;
+            k_spax_encode<4><<<grid, 256, smem, st>>>(Wd, d, N, group, ngp, WdT, recs, rec_bytes);
+            break;
+        case 8:
+            if ((e = allow_max_smem(k_spax_encode<8>)) != cudaSuccess) return e;
+            k_spax_encode<8><<<grid, 256, smem, st>>>(Wd, d, N, group, ngp, WdT, recs, rec_bytes);
+            break;
+        default:
+            return cudaErrorInvalidValue;
+    }
     return cudaGetLastError();
 }
 

@@ -19,14 +19,15 @@ def si():
 
 def encoded_buffers(layer):
     """The column-major copy, and the per-column records split into codes
-    [N][d/2] and (scale, min) pairs [N][ng_pad][2]."""
+    [N][d*bits/8] and (scale, min) pairs [N][ng_pad][2]."""
     p_wdt, p_codes, p_params = layer.buffers()
-    rec = layer.d // 2 + 8 * layer.ngp
-    assert p_params == p_codes + layer.d // 2
+    cb = layer.d * layer.bits // 8
+    rec = cb + 8 * layer.ngp
+    assert p_params == p_codes + cb
     WdT = device_view(p_wdt, (layer.N, layer.d), "<i2").cpu().numpy().view(np.uint16)
     recs = device_view(p_codes, (layer.N, rec), "|u1").cpu().numpy()
-    codes = np.ascontiguousarray(recs[:, :layer.d // 2])
-    params = np.ascontiguousarray(recs[:, layer.d // 2:]).view(np.float32).reshape(layer.N, layer.ngp, 2)
+    codes = np.ascontiguousarray(recs[:, :cb])
+    params = np.ascontiguousarray(recs[:, cb:]).view(np.float32).reshape(layer.N, layer.ngp, 2)
     return WdT, codes, params
 
 
@@ -36,15 +37,18 @@ def llama8b_layer():
     return synth.layer_weights(50, 0, 4096, 14336)
 
 
-@pytest.mark.parametrize("d,N,group", [(256, 64, 128), (4096, 14336, 128), (512, 300, 64), (128, 5, 8)])
-def test_spax_encode_bit_exact(si, d, N, group, llama8b_layer):
+@pytest.mark.parametrize("d,N,group,bits", [(256, 64, 128, 4), (4096, 14336, 128, 4), (512, 300, 64, 4),
+                                            (128, 5, 8, 4), (256, 64, 128, 8), (512, 300, 64, 2),
+                                            (128, 5, 8, 2), (4096, 14336, 128, 8), (1024, 700, 32, 2)])
+def test_spax_encode_bit_exact(si, d, N, group, bits, llama8b_layer):
     if (d, N) == (4096, 14336):
         _, _, Wd = llama8b_layer
     else:
         _, _, Wd = synth.layer_weights(51, 0, d, N)
-    layer = si.spax_encode(dev_bf16(Wd), 4, group)
+    layer = si.spax_encode(dev_bf16(Wd), bits, group)
+    assert layer.bits == bits
     WdT, codes, params = encoded_buffers(layer)
-    rc, rp = oracle.spax_encode(Wd, 4, group)
+    rc, rp = oracle.spax_encode(Wd, bits, group)
     assert np.array_equal(WdT, Wd.T)
     assert np.array_equal(codes, rc)
     ng = d // group
@@ -60,14 +64,16 @@ def signed_acts(seed, N, ties=False):
     return a
 
 
-@pytest.mark.parametrize("N,top,mid,ties", [(14336, 0.3, 0.3, False), (14336, 0.3, 0.3, True),
-                                            (1000, 0.0, 0.5, True), (1000, 0.5, 0.0, False),
-                                            (1000, 1.0, 0.0, False), (1000, 0.0, 1.0, True),
-                                            (1000, 0.0, 0.0, False), (77, 0.4, 0.6, True)])
-def test_spax_tiers_and_down(si, N, top, mid, ties):
+@pytest.mark.parametrize("N,top,mid,ties,bits", [(14336, 0.3, 0.3, False, 4), (14336, 0.3, 0.3, True, 4),
+                                                 (1000, 0.0, 0.5, True, 4), (1000, 0.5, 0.0, False, 4),
+                                                 (1000, 1.0, 0.0, False, 4), (1000, 0.0, 1.0, True, 4),
+                                                 (1000, 0.0, 0.0, False, 4), (77, 0.4, 0.6, True, 4),
+                                                 (14336, 0.3, 0.3, False, 8), (14336, 0.3, 0.3, True, 2),
+                                                 (1000, 0.0, 1.0, True, 8), (1000, 0.2, 0.8, False, 2)])
+def test_spax_tiers_and_down(si, N, top, mid, ties, bits):
     d = 256 if N != 14336 else 4096
     _, _, Wd = synth.layer_weights(52, 0, d, N)
-    layer = si.spax_encode(dev_bf16(Wd), 4, 128)
+    layer = si.spax_encode(dev_bf16(Wd), bits, 128)
     a = signed_acts(53, N, ties)
     k_top, k_mid = si.si_count(top, N), si.si_count(mid, N)
     ti = Guarded((max(k_top, 1),), torch().int32, fill=-1)
@@ -79,8 +85,8 @@ def test_spax_tiers_and_down(si, N, top, mid, ties):
         assert np.array_equal(ti.numpy()[:k_top], rt)
     if k_mid:
         assert np.array_equal(mi.numpy()[:k_mid], rm)
-    codes, params = oracle.spax_encode(Wd, 4, 128)
-    ref = oracle.spax_down(a, Wd, codes, params, rt, rm)
+    codes, params = oracle.spax_encode(Wd, bits, 128)
+    ref = oracle.spax_down(a, Wd, codes, params, rt, rm, bits=bits)
     got = y.numpy()
     # without the lists each CTA takes the tier members of its own index range
     y2 = Guarded((d,), torch().float32, fill=float("nan"))
@@ -127,11 +133,12 @@ def test_spax_dense_act(si, d, N, llama8b_layer):
     assert rel_err(a.numpy(), ref) <= 1e-5
 
 
-def test_spax_ffn_decode_full_token(si, llama8b_layer):
-    """One Llama-3.1-8B layer token: dense gate/up, 30% bf16 / 30% 4-bit / 40% skipped."""
+@pytest.mark.parametrize("bits", [4, 8, 2])
+def test_spax_ffn_decode_full_token(si, llama8b_layer, bits):
+    """One Llama-3.1-8B layer token: dense gate/up, 30% bf16 / 30% b-bit / 40% skipped."""
     Wg, Wu, Wd = llama8b_layer
-    layer = si.spax_encode(dev_bf16(Wd), 4, 128)
-    codes, params = oracle.spax_encode(Wd, 4, 128)
+    layer = si.spax_encode(dev_bf16(Wd), bits, 128)
+    codes, params = oracle.spax_encode(Wd, bits, 128)
     N = 14336
     k_top, k_mid = si.si_count(0.3, N), si.si_count(0.3, N)
     Wg_d, Wu_d = dev_bf16(Wg), dev_bf16(Wu)
@@ -142,7 +149,7 @@ def test_spax_ffn_decode_full_token(si, llama8b_layer):
         si.spax_ffn_decode(layer, Wg_d, Wu_d, dev_bf16(x), 0.3, 0.3, y.t, a_out.t)
         a_ref = oracle.dense_act(Wg, Wu, x).astype(np.float32)
         rt, rm = oracle.spax_tiers(a_ref, k_top, k_mid)
-        ref = oracle.spax_down(a_ref, Wd, codes, params, rt, rm)
+        ref = oracle.spax_down(a_ref, Wd, codes, params, rt, rm, bits=bits)
         assert rel_err(y.numpy(), ref) <= TOL
         assert rel_err(a_out.numpy(), a_ref) <= 1e-5
     layer.close()
