@@ -461,13 +461,57 @@ def run_spax(si, torch, dev, stream, args):
     dense_bytes = w.L * 2 * w.N * w.d * 2
     dense_s = dense_ms / 1e3 / (toks * w.L)
     hbm_peak, _, _, kind = peaks()
+    widths = spax_code_widths(si, torch, dev, stream, W, seed)
     return {"workload": w.name, "tokens": toks, "tokens_per_s": round(1.0 / per_tok, 2),
             "ms_per_token": round(per_tok * 1e3, 4), "hbm_gbs": round(byts / per_tok / 1e9, 1),
             "bytes_per_token": byts, "top_frac": w.top_frac, "mid_frac": w.mid_frac,
             "dense_act_roofline": {"kernel": "k_dense_act", "bound": "hbm",
                                    "achieved": round(dense_bytes / w.L / dense_s / 1e9, 1), "peak": hbm_peak,
                                    "unit": "GB/s", "frac": round(dense_bytes / w.L / dense_s / 1e9 / hbm_peak, 4),
-                                   "peak_source": kind}}
+                                   "peak_source": kind},
+            "code_widths": widths}
+
+
+def spax_code_widths(si, torch, dev, stream, W, seed, layers=4, toks=64):
+    """The same SpAx layer-token with 2-, 4- and 8-bit middle-tier codes, on the
+    first `layers` layers of the stack: microseconds per layer-token and the
+    selected bytes (dense gate/up + bf16 top + b-bit records) per second."""
+    w = SPAX_WL
+    k_top, k_mid = si.si_count(w.top_frac, w.N), si.si_count(w.mid_frac, w.N)
+    ngp = -(-(w.d // w.group) // 2) * 2
+    x = gpu_tokens(torch, seed, 401, toks * layers, w.d, dev).view(toks, layers, w.d)
+    y = torch.empty((toks, layers, w.d), dtype=torch.float32, device=dev)
+    a = torch.empty((layers, w.N), dtype=torch.float32, device=dev)
+    out = {}
+    for bits in (2, 4, 8):
+        enc = []
+        for l in range(layers):
+            _, _, Wd = gpu_weights(torch, seed, l, w.d, w.N, w.sigma, dev)
+            enc.append(si.spax_encode(Wd, bits, w.group))
+            del Wd
+
+        def run():
+            for t in range(toks):
+                for l in range(layers):
+                    si.spax_ffn_decode(enc[l], W[l][0], W[l][1], x[t, l], w.top_frac, w.mid_frac, y[t, l], a[l])
+
+        with torch.cuda.stream(stream):
+            run()
+            stream.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                run()
+            g.replay()
+            e0, e1 = time_graph(torch, g, stream)
+            stream.synchronize()
+        assert si.si_device_error() == 0
+        us = e0.elapsed_time(e1) * 1e3 / (toks * layers)
+        byts = 2 * w.N * w.d * 2 + k_top * 2 * w.d + k_mid * (w.d * bits // 8 + 8 * ngp)
+        out[str(bits)] = {"us_per_layer_token": round(us, 2), "hbm_gbs": round(byts / us / 1e3, 1),
+                          "bytes_per_layer_token": byts}
+        for e in enc:
+            e.close()
+    return out
 
 
 # ------------------------------------------------------------------ CPU oracle
