@@ -56,6 +56,7 @@ def _declare(L):
     L.oracle_set_threads.argtypes = [i]
     L.oracle_profile_scores.argtypes = [_u16p, _u16p, i, i, _u16p, i, _f64p]
     L.oracle_merge_scores.argtypes = [C.POINTER(C.c_void_p), C.POINTER(ll), i, i, _f32p]
+    L.oracle_sparse_layers.argtypes, L.oracle_sparse_layers.restype = [i, i, i, _u8p], i
     L.oracle_rank_loaded.argtypes = [_f32p, _f32p, i, d, d, _i32p, _u8p, C.POINTER(i), C.POINTER(i)]
     L.oracle_rank_loaded.restype = i
     L.oracle_loaded_bytes.argtypes, L.oracle_loaded_bytes.restype = [i, i, i], ll
@@ -104,6 +105,16 @@ def merge_scores(score_list, token_counts):
     out = np.zeros(N, np.float32)
     lib().oracle_merge_scores(ptrs, toks, len(arrs), N, out)
     return out
+
+
+def sparse_layers(L, first=5, last=-2):
+    """Per-layer mask of the layers that run selection (Table 1's range); the
+    others keep their dense FFN."""
+    out = np.zeros(max(L, 1), np.uint8)
+    n = lib().oracle_sparse_layers(int(L), int(first), int(last), out)
+    if n < 0:
+        raise ValueError("need L >= 0, first >= 0")
+    return out[:L].astype(bool)
 
 
 def rank_loaded(task, model, gamma, delta):

@@ -21,6 +21,8 @@
  * Pins (what each function is checked against, besides itself), see tests:
  *   oracle_profile_scores  brute force per token + closed form silu values
  *   oracle_merge_scores    hand-computed file merges
+ *   oracle_sparse_layers   Table 1's values read as words ("first layer 5",
+ *                          "skip last 2") at several depths
  *   oracle_rank_loaded     subset enumeration on tiny N, Table 1 / Eq. 2 counts
  *   oracle_topk_rows       subset enumeration on tiny rows with forced ties
  *   oracle_select          subset enumeration of the top-beta step, counting
@@ -153,6 +155,25 @@ void oracle_merge_scores(const float *const *s, const long long *tokens, int nfi
         }
         out[n] = acc;
     }
+}
+
+/* Layer range, SelectInfer section 6.4, Table 1 ("First layer 5", "Last layer
+ * -2 (skip last 2)"): selection runs on layers first .. end-1 and every other
+ * layer keeps its dense FFN. `last` reads as a slice end: end = L + last when
+ * last <= 0 (so -2 skips the last two layers), else end = last; the range is
+ * clipped to [0, L]. sparse[l] = 1 inside it, 0 outside. Returns the number
+ * of sparse layers, or -1 for L < 0 or first < 0. */
+int oracle_sparse_layers(int L, int first, int last, uint8_t *sparse)
+{
+    if (L < 0 || first < 0) return -1;
+    int end = last <= 0 ? L + last : last;
+    if (end > L) end = L;
+    int count = 0;
+    for (int l = 0; l < L; ++l) {
+        sparse[l] = (uint8_t)(l >= first && l < end);
+        count += sparse[l];
+    }
+    return count;
 }
 
 /* ------------------------------------------------------------ a2 loading */

@@ -41,6 +41,25 @@ def test_counts_round_to_nearest():
     assert oracle.cnt(0.0, 100) == 0 and oracle.cnt(1.0, 100) == 100
 
 
+def test_table1_layer_range(golden_dir):
+    """Table 1: selection starts at layer 5 ("First layer 5") and skips the
+    last two ("Last layer -2 (skip last 2)"); the other layers stay dense."""
+    g = json.load(open(os.path.join(golden_dir, "selectinfer_table1.json")))
+    first, last = g["first_layer"], g["last_layer"]
+    for L in (16, 28, 36, 8):          # Llama3.2-1B, -3B, Qwen2.5-3B depths, a shallow stack
+        m = oracle.sparse_layers(L, first, last)
+        assert m.shape == (L,)
+        assert not m[:5].any()          # layers 0..4 keep the dense FFN
+        assert not m[-2:].any()         # so do the last two
+        assert m[5:L - 2].all()         # and every layer in between selects
+        assert int(m.sum()) == L - 7
+    assert oracle.sparse_layers(16, 0, 0).all()                 # skip the last 0: the whole stack
+    assert oracle.sparse_layers(16, 2, 10).sum() == 8           # a positive end is a layer index
+    assert not oracle.sparse_layers(6, 5, -2).any()             # too shallow for the range
+    with pytest.raises(ValueError):
+        oracle.sparse_layers(16, -1, -2)
+
+
 def test_table1_fractions(golden_dir):
     g = json.load(open(os.path.join(golden_dir, "selectinfer_table1.json")))
     # static + dynamic = computed (phi = delta + epsilon), base + secondary = loaded
