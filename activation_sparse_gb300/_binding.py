@@ -24,6 +24,7 @@ SIGNATURES = {
     "si_count": (_ll, [_d, _ll]),
     "si_counts": (_i, [_i, _d, _d, _d, _ip, _ip, _ip, _ip]),
     "si_packed_bytes": (_ll, [_i, _i]),
+    "si_sparse_layers": (_i, [_i, _i, _i, _vp, _ip]),
     "si_device_error": (_i, [_u32p, _i]),
     "si_profile_scores": (_i, [_vp, _vp, _i, _i, _vp, _i, _vp, _vp]),
     "si_merge_scores": (_i, [C.POINTER(_vp), C.POINTER(_ll), _i, _i, _vp, _vp]),
@@ -142,6 +143,15 @@ def si_device_error(clear: bool = True) -> int:
     v = C.c_uint32()
     _check(L.si_device_error(C.byref(v), 1 if clear else 0))
     return v.value
+
+
+def si_sparse_layers(L: int, first: int = 5, last: int = -2):
+    """Per-layer mask (numpy bool [L]) of the layers that run selection; the others stay dense."""
+    import numpy as np
+    out = np.zeros(max(int(L), 1), np.uint8)
+    n = C.c_int(0)
+    _check(load().si_sparse_layers(int(L), int(first), int(last), out.ctypes.data_as(C.c_void_p), C.byref(n)))
+    return out[:int(L)].astype(bool)
 
 
 def si_profile_scores(Wg, Wu, X, scores, stream=None):

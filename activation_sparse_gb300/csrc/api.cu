@@ -206,6 +206,21 @@ int si_abi_version(void) { return 1; }
 
 long long si_count(double ratio, long long n) { return count_of(ratio, n); }
 
+int si_sparse_layers(int L, int first, int last, uint8_t* sparse, int* n_sparse) {
+    if (L < 0 || first < 0) return fail(SI_ERR_INVALID_ARG, "need L >= 0, first >= 0");
+    if (L > 0 && !sparse) return fail(SI_ERR_INVALID_ARG, "NULL pointer");
+    const long long end_raw = last <= 0 ? (long long)L + last : (long long)last;
+    const long long end = end_raw > L ? L : end_raw;
+    int n = 0;
+    for (int l = 0; l < L; ++l) {
+        const bool in = l >= first && l < end;
+        sparse[l] = in ? 1 : 0;
+        n += in ? 1 : 0;
+    }
+    if (n_sparse) *n_sparse = n;
+    return SI_OK;
+}
+
 int si_counts(int N, double gamma, double delta, double phi, int* n_loaded, int* n_static, int* n_sel, int* beta) {
     if (N < 1 || !ratios_ok(delta, phi, gamma))
         return fail(SI_ERR_INVALID_ARG, "need N >= 1 and 0 <= delta <= phi <= gamma <= 1");

@@ -309,6 +309,10 @@ def run_gpu(args, world, rank, local):
     # e2e: host buffers through the same C-ABI calls, copies inside the timed region
     e2e = run_e2e(si, torch, dev, stream, layers, S, n_sel, args)
 
+    # Table 1's layer range on the same stack: the first five and the last two
+    # layers keep the dense FFN (packed at gamma = 1, decoded on S = every position)
+    layer_range = run_layer_range(si, torch, dev, stream, layers, Ws, S, n_sel, xdec, y)
+
     spax = None
     if not args.no_spax and rank == 0:
         del Ws
@@ -344,6 +348,7 @@ def run_gpu(args, world, rank, local):
         "clocks": {"sm_mhz": clocks["sm_mhz"], "sm_max_mhz": clocks["sm_max_mhz"], "reasons": clocks["reasons"]},
         "wall_s_timed": round(t_wall, 4),
     }
+    out["layer_range"] = layer_range
     if spax is not None:
         out["spax"] = spax
     if rank == 0 and not args.no_cpu_baseline:
@@ -353,6 +358,51 @@ def run_gpu(args, world, rank, local):
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def run_layer_range(si, torch, dev, stream, layers, Ws, S, n_sel, xdec, y, toks=64):
+    """Decode tokens/s of the stack with SelectInfer's layer range (Table 1: first
+    layer 5, skip the last 2): layers outside it run the dense FFN through the
+    same decode, packed at gamma = 1 with S = every position."""
+    w = WL
+    mask = si.si_sparse_layers(w.L, 5, -2)
+    full = torch.arange(w.N, dtype=torch.int32, device=dev).view(1, -1).contiguous()
+    ones = torch.ones(w.N, dtype=torch.float32, device=dev)
+    dense = {}
+    for l in range(w.L):
+        if not mask[l]:
+            Wg, Wu, Wd = Ws[l]
+            dense[l] = si.si_pack_loaded(Wg, Wu, Wd, ones, ones, 1.0, 0.0)
+
+    def run():
+        for t in range(toks):
+            for l in range(w.L):
+                if mask[l]:
+                    si.si_sparse_ffn_decode_residual(layers[l], S[l], n_sel, 1, xdec[t, l], y[t, l])
+                else:
+                    si.si_sparse_ffn_decode_residual(dense[l], full, w.N, 1, xdec[t, l], y[t, l])
+
+    with torch.cuda.stream(stream):
+        for l in dense:
+            si.si_decode_plan(dense[l], full, w.N, 1)
+        run()
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            run()
+        g.replay()
+        e0, e1 = time_graph(torch, g, stream)
+        stream.synchronize()
+    assert si.si_device_error() == 0
+    s_tok = e0.elapsed_time(e1) / 1e3 / toks
+    n_sp = int(mask.sum())
+    per = lambda n: n * 6 * w.d + n * 4 + 2 * w.d + 4 * w.d
+    byts = n_sp * per(n_sel) + (w.L - n_sp) * per(w.N)
+    for l in dense:
+        dense[l].close()
+    return {"first_layer": 5, "last_layer": -2, "sparse_layers": n_sp, "dense_layers": w.L - n_sp,
+            "tokens": toks, "tokens_per_s": round(1.0 / s_tok, 2), "ms_per_token": round(s_tok * 1e3, 4),
+            "bytes_per_token": byts, "hbm_gbs": round(byts / s_tok / 1e9, 1)}
 
 
 def run_e2e(si, torch, dev, stream, layers, S, n_sel, args):

@@ -83,6 +83,17 @@ int si_counts(int N, double gamma, double delta, double phi,
  * [SI] Eq. (2)'s saving, before tile padding). */
 long long si_packed_bytes(int d, int n_loaded);
 
+/* Layer range of selection, [SI] section 6.4 Table 1 (first layer 5, last
+ * layer -2: "skip last 2"): sparse[l] (host, L bytes) = 1 for the layers
+ * first <= l < end that run selective loading and computation, 0 for the
+ * layers that keep their dense FFN. `last` is a slice end: end = L + last
+ * when last <= 0, else end = last, clipped to L. A dense layer runs through
+ * the same decode with a layer packed at gamma = 1 and S = every position
+ * (phi = 1). Returns SI_OK and the number of sparse layers in *n_sparse
+ * (may be NULL); SI_ERR_INVALID_ARG for L < 0, first < 0 or sparse NULL
+ * with L > 0. */
+int si_sparse_layers(int L, int first, int last, uint8_t *sparse, int *n_sparse);
+
 /* Reads (and with clear != 0 resets) the device error word of the current
  * device. *code (host) receives 0 when no kernel reported a failure, else a
  * bit set of SI_DEVERR_* values. Synchronises the device. */

@@ -5,6 +5,7 @@ import os
 import re
 import subprocess
 
+import numpy as np
 import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
@@ -82,3 +83,17 @@ def test_validation_before_cuda(si):
     assert lib.si_prefill_absact(p, p, 4, 1, odd, None) == si.SI_ERR_INVALID_ARG
     assert b"aligned" in lib.si_last_error_string()
     assert lib.si_select_dynamic(p, p, 4, 1, 1, 0.4, p, odd, None) == si.SI_ERR_INVALID_ARG
+
+
+def test_sparse_layers_match_oracle(si):
+    """Host-side layer range: the library's mask equals the oracle's for
+    Table 1's range at the pages' depths and for other slices."""
+    import oracle
+    for L in (0, 1, 6, 7, 8, 16, 28, 36):
+        for first, last in ((5, -2), (0, 0), (0, -1), (3, 10), (2, 40), (9, -9)):
+            got = si.si_sparse_layers(L, first, last)
+            ref = oracle.sparse_layers(L, first, last)
+            assert np.array_equal(got, ref), (L, first, last)
+    lib = si.load()
+    assert lib.si_sparse_layers(4, -1, -2, None, None) == si.SI_ERR_INVALID_ARG
+    assert lib.si_sparse_layers(4, 1, -2, None, None) == si.SI_ERR_INVALID_ARG

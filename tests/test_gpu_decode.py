@@ -39,6 +39,7 @@ DECODE_CASES = [
     (2048, 11008, 0.8, 0.25, 0.5, 1024, 16, 3, 1.5),     # 3 sequences
     (4096, 2048, 0.5, 0.2, 0.3, 64, 8, 1, 1.0),          # widest supported d
     (64, 100, 1.0, 0.0, 1.0, 8, 4, 1, 1.0),              # phi = gamma = 1: dense FFN
+    (2048, 8192, 1.0, 0.0, 1.0, 1024, 8, 1, 1.0),        # a dense Llama3.2-1B layer (outside the layer range)
     (1088, 300, 0.9, 0.1, 0.2, 8, 4, 2, 1.0),            # d not a multiple of 256
 ]
 
@@ -181,3 +182,24 @@ def test_residual_decode_accumulates(si, planned):
     with pytest.raises(si.SIError):
         si.si_sparse_ffn_decode_residual(c.layer, S, c.n_sel, 2, dev_bf16(xs[0]), y.t)
     c.layer.close()
+
+
+def test_layer_range_stack(si):
+    """Table 1's layer range on an 8-layer stack: layers 5 .. 5 run selection
+    (gamma 0.7, phi 0.4), the first five and the last two keep the dense FFN
+    (gamma = phi = 1, S = every position). Every layer matches the oracle."""
+    L, d, N = 8, 256, 1024
+    mask = si.si_sparse_layers(L, 5, -2)
+    assert np.array_equal(mask, oracle.sparse_layers(L, 5, -2))
+    for l in range(L):
+        if mask[l]:
+            c = Case(si, d, N, 0.7, 0.2, 0.4, 64, 16, 1, seed=60 + l)
+        else:
+            c = Case(si, d, N, 1.0, 0.0, 1.0, 64, 16, 1, seed=60 + l)
+            assert c.n_sel == N and np.array_equal(c.S[0], np.arange(N))
+        x = synth.tokens(61, l, synth.T_DECODE, 1, d)
+        y = Guarded((1, d), torch().float32, fill=float("nan"))
+        si.si_sparse_ffn_decode(c.layer, dev(c.S), c.n_sel, 1, dev_bf16(x), y.t)
+        ref = oracle.sparse_ffn(c.Wg, c.Wu, c.Wd, c.loaded, c.S[0], x[0])
+        assert rel_err(y.numpy()[0], ref) <= TOL
+        c.layer.close()
