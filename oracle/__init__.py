@@ -57,6 +57,7 @@ def _declare(L):
     L.oracle_profile_scores.argtypes = [_u16p, _u16p, i, i, _u16p, i, _f64p]
     L.oracle_merge_scores.argtypes = [C.POINTER(C.c_void_p), C.POINTER(ll), i, i, _f32p]
     L.oracle_sparse_layers.argtypes, L.oracle_sparse_layers.restype = [i, i, i, _u8p], i
+    L.oracle_down_norms.argtypes = [_u16p, i, i, _i32p, i, _f64p]
     L.oracle_rank_loaded.argtypes = [_f32p, _f32p, i, d, d, _i32p, _u8p, C.POINTER(i), C.POINTER(i)]
     L.oracle_rank_loaded.restype = i
     L.oracle_loaded_bytes.argtypes, L.oracle_loaded_bytes.restype = [i, i, i], ll
@@ -115,6 +116,16 @@ def sparse_layers(L, first=5, last=-2):
     if n < 0:
         raise ValueError("need L >= 0, first >= 0")
     return out[:L].astype(bool)
+
+
+def down_norms(Wd, loaded):
+    """||Wd[:, n]||_2 of each loaded neuron n (float64), the weight half of the
+    weight-aware salience |a_n| * ||Wd[:, n]||_2."""
+    Wd, loaded = _c(Wd, np.uint16), _c(loaded, np.int32)
+    d, N = Wd.shape
+    out = np.zeros(loaded.shape[0], np.float64)
+    lib().oracle_down_norms(Wd, d, N, loaded, loaded.shape[0], out)
+    return out
 
 
 def rank_loaded(task, model, gamma, delta):

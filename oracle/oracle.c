@@ -23,6 +23,7 @@
  *   oracle_merge_scores    hand-computed file merges
  *   oracle_sparse_layers   Table 1's values read as words ("first layer 5",
  *                          "skip last 2") at several depths
+ *   oracle_down_norms      closed forms (constant columns) and numpy.linalg.norm
  *   oracle_rank_loaded     subset enumeration on tiny N, Table 1 / Eq. 2 counts
  *   oracle_topk_rows       subset enumeration on tiny rows with forced ties
  *   oracle_select          subset enumeration of the top-beta step, counting
@@ -174,6 +175,23 @@ int oracle_sparse_layers(int L, int first, int last, uint8_t *sparse)
         count += sparse[l];
     }
     return count;
+}
+
+/* Weight-aware salience (WiSparse abstract: activation magnitudes combined
+ * with precomputed weight norms). Read as the size of neuron n's contribution
+ * to the FFN output: salience_n = |a_n| * ||Wd[:, n]||_2. This computes the
+ * norms of the loaded neurons' down columns, norm[p] = sqrt(sum_j
+ * Wd[j, loaded[p]]^2), in float64. */
+void oracle_down_norms(const uint16_t *Wd, int d, int N, const int *loaded, int n, double *norm)
+{
+    for (int p = 0; p < n; ++p) {
+        double acc = 0.0;
+        for (int j = 0; j < d; ++j) {
+            double w = bf(Wd[(size_t)j * N + loaded[p]]);
+            acc += w * w;
+        }
+        norm[p] = sqrt(acc);
+    }
 }
 
 /* ------------------------------------------------------------ a2 loading */

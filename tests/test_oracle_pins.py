@@ -377,3 +377,20 @@ def test_spax_down_limits():
     assert np.all(np.abs(y2 - f32(Wd) @ a.astype(np.float64)) <= bound * (1 + 1e-5) + 1e-12)
     # nothing selected: zero
     assert np.all(oracle.spax_down(a, Wd, codes, params, none, none) == 0)
+
+
+def test_down_norms():
+    """Weight norms of the salience |a_n| * ||Wd[:, n]||_2: closed forms on
+    constant and one-hot columns, and numpy's norm on random bf16 columns."""
+    d, N = 64, 5
+    Wd = np.zeros((d, N))
+    Wd[:, 0] = 1.0                 # sqrt(d)
+    Wd[:, 1] = -0.5                # 0.5 sqrt(d)
+    Wd[7, 2] = 3.0                 # one-hot: |3|
+    Wd[:, 4] = 2.0                 # sqrt(4 d)
+    got = oracle.down_norms(bf16(Wd), np.array([4, 0, 2, 1, 3], np.int32))
+    assert np.allclose(got, [2 * np.sqrt(d), np.sqrt(d), 3.0, 0.5 * np.sqrt(d), 0.0], rtol=0, atol=1e-12)
+    Wr = bf16(np.random.default_rng(5).standard_normal((256, 40)) * 0.1)
+    loaded = np.array([39, 0, 17, 5], np.int32)
+    ref = np.linalg.norm(f32(Wr)[:, loaded], axis=0)
+    assert np.allclose(oracle.down_norms(Wr, loaded), ref, rtol=1e-12, atol=0)
