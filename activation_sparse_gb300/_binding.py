@@ -35,6 +35,8 @@ SIGNATURES = {
     "si_select_dynamic": (_i, [_vp, _vp, _i, _i, _i, _d, _vp, _vp, _vp]),
     "si_prefill_absact": (_i, [_vp, _vp, _i, _i, _vp, _vp]),
     "si_set_gemm_tile": (_i, [_i]),
+    "si_layer_set_salience": (_i, [_vp, _i]),
+    "si_layer_norms": (_i, [_vp, C.POINTER(_vp)]),
     "si_gemm_tile_for": (_i, [_i, _i, _ip]),
     "si_select_from_absact": (_i, [_vp, _vp, _i, _i, _i, _i, _d, _vp, _vp, _vp, _vp]),
     "si_decode_plan": (_i, [_vp, _vp, _i, _i, _vp]),
@@ -221,6 +223,18 @@ def si_select_dynamic(layer: Layer, X, T, B, alpha, phi, S, absact_out=None, str
                                     _ptr(S, torch.int32, "S"), _ptr(absact_out, torch.float32, "absact_out"),
                                     _stream(stream)))
     return S
+
+
+def si_layer_set_salience(layer: Layer, weight_aware: bool):
+    """Prefill ranking key of this layer: |a| (False, default) or |a| * ||Wd[:, n]||_2 (True)."""
+    _check(load().si_layer_set_salience(layer.handle, 1 if weight_aware else 0))
+
+
+def si_layer_norms(layer: Layer) -> int:
+    """Device pointer of the layer's fp32 [n_pad] down-column norms."""
+    p = C.c_void_p()
+    _check(load().si_layer_norms(layer.handle, C.byref(p)))
+    return p.value
 
 
 def si_set_gemm_tile(bnn: int):

@@ -93,6 +93,8 @@ struct si_layer {
     int32_t* loaded = nullptr;
     uint8_t* is_static = nullptr;
     uint16_t* packed = nullptr;
+    float* wnorm = nullptr;     // ||Wd[:, n]||_2 per packed position (pads 0)
+    int salience = 0;           // 1: prefill ranks by |a| * wnorm (weight-aware)
     uint32_t* counts = nullptr;
     int counts_B = 0;
     float* absA = nullptr;
@@ -146,6 +148,7 @@ void destroy_layer(si_layer* L) {
     dfree(L->loaded);
     dfree(L->is_static);
     dfree(L->packed);
+    dfree(L->wnorm);
     dfree(L->counts);
     dfree(L->absA);
     dfree(L->part);
@@ -312,6 +315,7 @@ int si_pack_loaded(const uint16_t* Wg, const uint16_t* Wu, const uint16_t* Wd, i
     L->n_pad = round_up(n_loaded, 128);
     if ((rc = dalloc(&L->loaded, n_loaded, "loaded index")) || (rc = dalloc(&L->is_static, n_loaded, "static flags")) ||
         (rc = dalloc(&L->packed, (size_t)L->n_pad * 3 * d, "packed weights")) ||
+        (rc = dalloc(&L->wnorm, L->n_pad, "down-column norms")) ||
         (rc = dalloc(&L->tickets, 16, "tickets")) || (rc = dalloc(&L->acc, d, "decode accumulator")) ||
         (rc = grow_part(&L->part, &L->part_floats, d, 1))) {
         destroy_layer(L);
@@ -322,6 +326,7 @@ int si_pack_loaded(const uint16_t* Wg, const uint16_t* Wu, const uint16_t* Wd, i
     if (e == cudaSuccess) e = si::launch_rank_loaded(task_scores, model_scores, N, n_static, n_loaded, L->loaded,
                                                      L->is_static, err, st);
     if (e == cudaSuccess) e = si::launch_pack_loaded(Wg, Wu, Wd, d, N, L->loaded, n_loaded, L->n_pad, L->packed, st);
+    if (e == cudaSuccess) e = si::launch_down_norms(L->packed, d, n_loaded, L->n_pad, L->wnorm, st);
     if (e == cudaSuccess) e = cudaStreamSynchronize(st);
     if (e != cudaSuccess) {
         destroy_layer(L);
@@ -347,6 +352,19 @@ int si_layer_buffers(const si_layer* L, const int32_t** loaded_idx, const uint8_
     if (loaded_idx) *loaded_idx = L->loaded;
     if (is_static) *is_static = L->is_static;
     if (packed) *packed = L->packed;
+    return SI_OK;
+}
+
+int si_layer_norms(const si_layer* L, const float** norms) {
+    if (!L || !norms) return fail(SI_ERR_INVALID_ARG, "NULL pointer");
+    *norms = L->wnorm;
+    return SI_OK;
+}
+
+int si_layer_set_salience(si_layer* L, int weight_aware) {
+    if (!L) return fail(SI_ERR_INVALID_ARG, "layer is NULL");
+    if (weight_aware != 0 && weight_aware != 1) return fail(SI_ERR_INVALID_ARG, "weight_aware must be 0 or 1");
+    L->salience = weight_aware;
     return SI_OK;
 }
 
@@ -386,6 +404,7 @@ int absact_core(si_layer* L, const uint16_t* X, int M, float* A, cudaStream_t st
     P.mode = 0;
     P.out = A;
     P.ldo = L->n_pad;
+    P.wnorm = L->salience ? L->wnorm : nullptr;
     P.err = err;
     SI_CK(si::launch_act_gemm(P, st));
     return SI_OK;

@@ -168,6 +168,11 @@ __device__ __forceinline__ void epi_group(const ActGemmParams& P, uint32_t tg, i
     float v[NC];
 #pragma unroll
     for (int e = 0; e < NC; ++e) v[e] = abs_act(__uint_as_float(g[e]), __uint_as_float(u[e]));
+    if (P.wnorm) {
+        // weight-aware salience |a| * ||Wd[:, n]||_2 (columns past Nvalid are clipped by the store)
+#pragma unroll
+        for (int e = 0; e < NC; ++e) v[e] *= (col0 + e < P.Nvalid) ? __ldg(P.wnorm + col0 + e) : 0.0f;
+    }
     if (P.mode == 0) {
         float* dst = stage + lane * BNN + j0;
 #pragma unroll

@@ -88,6 +88,7 @@ cudaError_t launch_merge_scores(const float* const* s, const float* tok, int nfi
 // pack.cu
 cudaError_t launch_pack_loaded(const uint16_t* Wg, const uint16_t* Wu, const uint16_t* Wd, int d, int N,
                                const int32_t* loaded, int n_loaded, int n_pad, uint16_t* packed, cudaStream_t st);
+cudaError_t launch_down_norms(const uint16_t* packed, int d, int n_loaded, int n_pad, float* norms, cudaStream_t st);
 cudaError_t launch_spax_encode(const uint16_t* Wd, int d, int N, int bits, int group, int ngp, uint16_t* WdT,
                                uint8_t* recs, int rec_bytes, cudaStream_t st);
 
@@ -120,6 +121,7 @@ struct ActGemmParams {
     int mode;
     float* out;
     long long ldo;
+    const float* wnorm;       // optional [Nvalid]: mode 0 writes |a| * wnorm[col] (weight-aware salience)
     float* colsum;
     unsigned* err;
 };

@@ -6,6 +6,8 @@
 //                  permutation-invariance argument: a SwiGLU FFN output is a
 //                  sum over neurons, so the records can sit in any order; this
 //                  library keeps ascending neuron index).
+//  k_down_norms    ||Wd[:, n]||_2 per packed neuron, for the weight-aware
+//                  salience |a_n| * ||Wd[:, n]||_2 (WiSparse abstract).
 //  k_spax_encode   SpAx offline encoding (Fig. 2, Fig. 3): per column and
 //                  per row group, float32 min / max / scale and 2-, 4- or
 //                  8-bit codes, plus a column-major bf16 copy of Wd so that a top-tier
@@ -111,6 +113,31 @@ __global__ void __launch_bounds__(256) k_spax_encode(const uint16_t* __restrict_
             prm[g * 2 + 1] = mn;
         }
     }
+}
+
+// ||Wd[:, n]||_2 of each packed neuron, from its record's down column: one
+// warp per position, lane-strided float32 squares summed in a fixed order
+// (deterministic), then a butterfly; pad positions get 0.
+__global__ void __launch_bounds__(256) k_down_norms(const uint16_t* __restrict__ packed, int d, int n_loaded,
+                                                   int n_pad, float* __restrict__ norms) {
+    const int p = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+    if (p >= n_pad) return;
+    float acc = 0.0f;
+    if (p < n_loaded) {
+        const uint16_t* col = packed + ((size_t)p * 3 + 2) * d;
+        for (int j = lane; j < d; j += 32) {
+            const float w = __uint_as_float((uint32_t)col[j] << 16);
+            acc = fmaf(w, w, acc);
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
+    if (lane == 0) norms[p] = sqrtf(acc);
+}
+
+cudaError_t launch_down_norms(const uint16_t* packed, int d, int n_loaded, int n_pad, float* norms, cudaStream_t st) {
+    k_down_norms<<<(n_pad + 7) / 8, 256, 0, st>>>(packed, d, n_loaded, n_pad, norms);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_pack_loaded(const uint16_t* Wg, const uint16_t* Wu, const uint16_t* Wd, int d, int N,

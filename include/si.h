@@ -199,6 +199,21 @@ int si_set_gemm_tile(int bnn);
  * neurons would use on the current device right now, in *bnn. */
 int si_gemm_tile_for(int M, int N, int *bnn);
 
+/* Ranking key of the prefill selection of this handle (si_select_dynamic and
+ * si_prefill_absact): weight_aware = 0 (the default) ranks by |a_n| as
+ * SelectInfer does; 1 ranks by the weight-aware salience |a_n| *
+ * ||Wd[:, n]||_2 (WiSparse abstract: activation magnitudes combined with
+ * precomputed weight norms, read as the size of neuron n's contribution to
+ * the FFN output), which is then what absact_out receives. The profiler
+ * score (si_profile_scores, Eq. (1)) is unaffected. SI_ERR_INVALID_ARG for
+ * other values. */
+int si_layer_set_salience(si_layer *layer, int weight_aware);
+
+/* Device pointer (read-only) to the handle's down-column norms: fp32
+ * [n_pad], norms[p] = ||Wd[:, loaded[p]]||_2 (float32 sum of squares of the
+ * bf16 column, then sqrt), 0 for pad positions; computed by si_pack_loaded. */
+int si_layer_norms(const si_layer *layer, const float **norms);
+
 /* Steps a4..a6 of si_select_dynamic on a given |A| matrix (fp32 [B*T x ld],
  * ld >= n_loaded, finite; only the first n_loaded columns are read, and they
  * are ranked by magnitude). Optional outputs (may be NULL): topmask

@@ -175,3 +175,52 @@ def test_tile_choice_fills_the_sms(si):
         assert all(cost(M, N, c) > best for c in GEMM_TILES if c > b)
     if sms >= 144:
         assert si.si_gemm_tile_for(512, 5734) == 80   # 144 CTAs instead of 90
+
+
+def test_weight_aware_salience(si):
+    """WiSparse-style ranking key |a_n| * ||Wd[:, n]||_2: the handle's norms,
+    the prefill matrix and the selection it drives, against the oracle; the
+    default key comes back when the switch is off."""
+    from gpu_util import device_view
+    d, N, T = 512, 1500, 96
+    Wg, Wu, Wd = synth.layer_weights(68, 0, d, N)
+    s = synth.lognormal_absact(68, 1, N)[0]
+    layer = si.si_pack_loaded(dev_bf16(Wg), dev_bf16(Wu), dev_bf16(Wd), dev(s), dev(s), 0.7, 0.2)
+    loaded, st = oracle.rank_loaded(s, s, 0.7, 0.2)
+    nl, n_pad = layer.n_loaded, layer.n_pad
+    norms = device_view(si.si_layer_norms(layer), (n_pad,), "<f4").cpu().numpy()
+    ref_norms = oracle.down_norms(Wd, loaded)
+    assert np.allclose(norms[:nl], ref_norms, rtol=5e-6, atol=0)   # float32 sums of 16 + 5 terms per lane path
+    assert not norms[nl:].any()
+    X = synth.tokens(69, 0, synth.T_PROMPT, T, d)
+    Xd = dev_bf16(X)
+    A0 = Guarded((T, n_pad), torch().float32, fill=float("nan"))
+    si.si_prefill_absact(layer, Xd, T, 1, A0.t)
+    si.si_layer_set_salience(layer, True)
+    A1 = Guarded((T, n_pad), torch().float32, fill=float("nan"))
+    si.si_prefill_absact(layer, Xd, T, 1, A1.t)
+    ref = oracle.absact(Wg, Wu, loaded, X) * ref_norms[None, :]
+    got = A1.numpy()
+    assert np.abs(got[:, :nl] - ref).max() <= 1e-3 * ref.max()
+    assert not got[:, nl:].any()
+    # the selection on salience is the exact selection of the matrix the GPU computed
+    alpha, phi = 64, 0.4
+    n_sel = si.si_count(phi, N)
+    S1 = Guarded((1, n_sel), torch().int32, fill=-1)
+    S2 = Guarded((1, n_sel), torch().int32, fill=-1)
+    si.si_select_dynamic(layer, Xd, T, 1, alpha, phi, S1.t)
+    si.si_select_from_absact(layer, A1.t, T, 1, alpha, phi, S2.t)
+    assert np.array_equal(S1.numpy(), S2.numpy())
+    ref_S = oracle.select(ref.astype(np.float32), T, 1, nl, st, alpha, n_sel)
+    overlap = len(np.intersect1d(S1.numpy()[0], ref_S[0])) / n_sel
+    assert overlap >= 0.98, overlap
+    # and it differs from the |a| ranking somewhere (the norms matter)
+    S0 = Guarded((1, n_sel), torch().int32, fill=-1)
+    si.si_select_from_absact(layer, A0.t, T, 1, alpha, phi, S0.t)
+    assert not np.array_equal(S0.numpy(), S1.numpy())
+    # switching back restores |a| bit for bit
+    si.si_layer_set_salience(layer, False)
+    A2 = Guarded((T, n_pad), torch().float32, fill=float("nan"))
+    si.si_prefill_absact(layer, Xd, T, 1, A2.t)
+    assert np.array_equal(A2.numpy().view(np.uint32), A0.numpy().view(np.uint32))
+    layer.close()
