@@ -50,6 +50,7 @@ SIGNATURES = {
     "spax_dense_act": (_i, [_vp, _vp, _i, _i, _vp, _vp, _vp]),
     "spax_tiered_down": (_i, [_vp, _vp, _d, _d, _vp, _vp, _vp, _vp]),
     "spax_ffn_decode": (_i, [_vp, _vp, _vp, _vp, _d, _d, _vp, _vp, _vp]),
+    "spax_select_decode": (_i, [_vp, _vp, _vp, _vp, _i, _vp, _d, _d, _vp, _vp, _vp]),
 }
 
 _lib = None
@@ -342,6 +343,17 @@ def spax_tiered_down(layer: SpaxLayer, a, top_frac, mid_frac, y, top_idx=None, m
     _check(load().spax_tiered_down(layer.handle, _ptr(a, torch.float32, "a"), float(top_frac), float(mid_frac),
                                    _ptr(y, torch.float32, "y"), _ptr(top_idx, torch.int32, "top_idx"),
                                    _ptr(mid_idx, torch.int32, "mid_idx"), _stream(stream)))
+    return y
+
+
+def spax_select_decode(layer: SpaxLayer, Wg, Wu, rows, x, top_frac, mid_frac, y, a_out=None, stream=None):
+    """SpAx tiers inside a selected set: rows (device int32) are the neurons computed."""
+    torch = _torch()
+    n_rows = int(rows.numel()) if rows is not None else 0
+    _check(load().spax_select_decode(layer.handle, _bf16(Wg, "Wg"), _bf16(Wu, "Wu"),
+                                     _ptr(rows, torch.int32, "rows") if n_rows else None, n_rows, _bf16(x, "x"),
+                                     float(top_frac), float(mid_frac), _ptr(y, torch.float32, "y"),
+                                     _ptr(a_out, torch.float32, "a_out"), _stream(stream)))
     return y
 
 

@@ -648,7 +648,7 @@ int spax_layer_destroy(spax_layer* L) {
 namespace {
 
 int dense_act_core(const uint16_t* Wg, const uint16_t* Wu, int d, int N, const uint16_t* x, float* a, unsigned* hist,
-                   int32_t* slab, cudaStream_t stream) {
+                   int32_t* slab, cudaStream_t stream, const int32_t* rows = nullptr, int n_rows = 0) {
     if (!Wg || !Wu || !x || !a) return fail(SI_ERR_INVALID_ARG, "NULL pointer");
     if (d < 8 || d % 8 || N < 1) return fail(SI_ERR_INVALID_ARG, "need d % 8 == 0, N >= 1");
     if (d > 4096) return fail(SI_ERR_UNSUPPORTED, "dense activation pass supports d <= 4096");
@@ -664,6 +664,8 @@ int dense_act_core(const uint16_t* Wg, const uint16_t* Wu, int d, int N, const u
     P.a = a;
     P.hist = hist;
     P.slab = hist ? slab : nullptr;
+    P.rows = rows;
+    P.n_rows = n_rows;
     P.err = err;
     P.R = si::dense_act_stages(d);
     if (P.R < 8) return fail(SI_ERR_UNSUPPORTED, "d too large for the activation ring");
@@ -733,6 +735,32 @@ int spax_tiered_down(spax_layer* L, const float* a, double top_frac, double mid_
     cudaStream_t st = (cudaStream_t)stream;
     SI_CK(si::launch_abs_hist(a, L->N, L->hist, L->slab, st));
     return tiered_core(L, a, k_top, k_mid, y, top_idx, mid_idx, st);
+}
+
+int spax_select_decode(spax_layer* L, const uint16_t* Wg, const uint16_t* Wu, const int32_t* rows, int n_rows,
+                       const uint16_t* x, double top_frac, double mid_frac, float* y, float* a_out, void* stream) {
+    if (!L || !Wg || !Wu || !x || !y || (n_rows > 0 && !rows)) return fail(SI_ERR_INVALID_ARG, "NULL pointer");
+    if (n_rows < 0 || n_rows > L->N) return fail(SI_ERR_INVALID_ARG, "need 0 <= n_rows <= N");
+    if (!(top_frac >= 0.0 && mid_frac >= 0.0 && top_frac + mid_frac <= 1.0))
+        return fail(SI_ERR_INVALID_ARG, "tier fractions must be >= 0 with top + mid <= 1");
+    const long long k_top = count_of(top_frac, n_rows), k_mid = count_of(mid_frac, n_rows);
+    if (k_top + k_mid > n_rows) return fail(SI_ERR_INVALID_ARG, "top + mid tiers exceed the selected rows");
+    cudaStream_t st = (cudaStream_t)stream;
+    float* a = a_out ? a_out : L->a;
+    // unlisted neurons have a = 0; the dense pass over the listed rows fills
+    // the rest and counts the zeros in the tier histogram
+    SI_CK(cudaMemsetAsync(a, 0, (size_t)L->N * sizeof(float), st));
+    if (n_rows == 0) {
+        SI_CK(cudaMemsetAsync(y, 0, (size_t)L->d * sizeof(float), st));
+        return SI_OK;
+    }
+    int rc = dense_act_core(Wg, Wu, L->d, L->N, x, a, L->hist, L->slab, st, rows, n_rows);
+    if (rc) return rc;
+    if ((rc = tiered_core(L, a, k_top, k_mid, y, nullptr, nullptr, st))) {
+        cudaMemsetAsync(L->hist, 0, (si::kTierBins + 1) * sizeof(unsigned), st);  // leave it clean
+        return rc;
+    }
+    return SI_OK;
 }
 
 int spax_ffn_decode(spax_layer* L, const uint16_t* Wg, const uint16_t* Wu, const uint16_t* x, double top_frac,

@@ -592,10 +592,20 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_dense_act(DenseActParams P) 
         return;
     }
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int lo = (int)((long long)P.N * blockIdx.x / gridDim.x);
-    const int hi = (int)((long long)P.N * (blockIdx.x + 1) / gridDim.x);
+    // the rows this CTA computes: an even share of all N neurons, or of the
+    // n_rows listed ones (their indices in P.rows)
+    const int total = P.rows ? P.n_rows : P.N;
+    const int lo = (int)((long long)total * blockIdx.x / gridDim.x);
+    const int hi = (int)((long long)total * (blockIdx.x + 1) / gridDim.x);
     const int cnt = hi - lo;
     const uint32_t row_bytes = (uint32_t)(2 * d);
+    // neuron of the CTA's i-th row; a listed index outside [0, N) is flagged
+    // and read as neuron 0 (never outside the weights)
+    auto row = [&](int i) -> int {
+        if (!P.rows) return lo + i;
+        const int n = P.rows[lo + i];
+        return (n >= 0 && n < P.N) ? n : 0;
+    };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < R; ++s) {
@@ -606,14 +616,18 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_dense_act(DenseActParams P) 
     }
     grid_launch_dependents();
     // The weights belong to the caller and may be the previous grid's output,
-    // so before the dependency wait they are only prefetched into L2; x and a
-    // are touched after it.
-    if (warp == kConsWarps)
+    // so before the dependency wait they are only prefetched into L2; x, a and
+    // a row list (which may be that grid's output too) are touched after it.
+    if (warp == kConsWarps && !P.rows)
         for (int i = lane; i < cnt && i < R; i += 32) {
-            prefetch_l2(P.Wg + (size_t)(lo + i) * d, row_bytes);
-            prefetch_l2(P.Wu + (size_t)(lo + i) * d, row_bytes);
+            prefetch_l2(P.Wg + (size_t)row(i) * d, row_bytes);
+            prefetch_l2(P.Wu + (size_t)row(i) * d, row_bytes);
         }
     grid_dependency_wait();
+    // with a row list, every unlisted neuron has a = 0 (the caller zeroes a):
+    // its key falls in bin 0 of the tier histogram
+    if (P.rows && P.hist && blockIdx.x == 0 && threadIdx.x == 0 && P.N > P.n_rows)
+        atomicAdd(P.hist, (unsigned)(P.N - P.n_rows));
     for (int i = threadIdx.x; i < d / 8; i += blockDim.x)
         reinterpret_cast<uint4*>(s_x)[i] = reinterpret_cast<const uint4*>(P.x)[i];
     __syncthreads();
@@ -624,7 +638,8 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_dense_act(DenseActParams P) 
             for (int i = 0; i < cnt; ++i) {
                 const int s = i % R;
                 if (i >= R) mbar_wait(&empty[s], (uint32_t)((i / R - 1) & 1), P.err, kSiteDenseAct | kSiteEmpty);
-                const size_t n = (size_t)(lo + i);
+                if (P.rows && (P.rows[lo + i] < 0 || P.rows[lo + i] >= P.N)) atomicOr(P.err, SI_DEVERR_COUNT);
+                const size_t n = (size_t)row(i);
                 uint8_t* dst = ring + (size_t)s * L.stage;
                 mbar_arrive_expect_tx(&full[s], 2 * row_bytes);
                 bulk_g2s_hint(dst, P.Wg + n * d, row_bytes, &full[s], pol);
@@ -663,14 +678,14 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_dense_act(DenseActParams P) 
             __syncwarp();
             if (lane == 0) {
                 const float av = swiglu(g, u);
-                P.a[lo + i] = av;
+                P.a[row(i)] = av;
                 mbar_arrive(&empty[s]);
                 if (P.hist) {
                     if (P.slab) {
                         if (pend_pos < (uint32_t)kSlabCap) P.slab[(size_t)pend_bin * kSlabCap + pend_pos] = pend_n;
                         pend_bin = abs_key(av) >> kTierShift;
                         pend_pos = atomicAdd(P.hist + pend_bin, 1u);
-                        pend_n = lo + i;
+                        pend_n = row(i);
                     } else {
                         atomicAdd(P.hist + (abs_key(av) >> kTierShift), 1u);
                     }
@@ -1031,7 +1046,10 @@ __device__ bool tier_own_range(const TieredDownParams& P, const float* s_a, int*
     const bool two = act[1] && !(act[0] && d0[1] == d0[0]);
     const uint32_t h0 = act[0] ? s_hist[0][d0[0]] : 0u, h1 = two ? s_hist[0][d0[1]] : 0u;
     uint32_t C;
-    if (P.slab && h0 <= (uint32_t)kSlabCap && h1 <= (uint32_t)kSlabCap && h0 + h1 <= (uint32_t)cap) {
+    // (bin 0 holds a = 0; a dense pass over a row list counts the unlisted
+    // zeros there without listing them, so bin 0 is always scanned)
+    const bool zero_bin = (act[0] && d0[0] == 0u) || (two && d0[1] == 0u);
+    if (P.slab && !zero_bin && h0 <= (uint32_t)kSlabCap && h1 <= (uint32_t)kSlabCap && h0 + h1 <= (uint32_t)cap) {
         C = h0 + h1;
         const uint32_t b0 = act[0] ? d0[0] : d0[1];  // the first list's bin
         for (uint32_t c = (uint32_t)tid; c < C; c += blockDim.x)
@@ -1621,7 +1639,9 @@ cudaError_t launch_dense_act(DenseActParams P, cudaStream_t st) {
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
     const size_t smem = (size_t)ring_layout(P.R, 4 * P.d, 0, P.d * 2).total;
-    const int grid = P.N < sms ? P.N : sms;
+    const int rows = P.rows ? P.n_rows : P.N;
+    if (rows < 1) return cudaErrorInvalidValue;
+    const int grid = rows < sms ? rows : sms;
     void* args[] = {&P};
     if (P.d > 2048) {
         if ((e = allow_max_smem(k_dense_act<2>)) != cudaSuccess) return e;

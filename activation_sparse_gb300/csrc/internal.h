@@ -48,6 +48,8 @@ struct DenseActParams {
     float* a;
     unsigned* hist;           // optional tier histogram of a (kTierBins + 1 words, zero on entry)
     int32_t* slab;            // optional per-bin member lists of hist ([kTierBins][kSlabCap]); needs hist
+    const int32_t* rows;      // optional: compute only these n_rows neurons (others untouched, counted as a = 0)
+    int n_rows;
     unsigned* err;
     int R;
 };

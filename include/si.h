@@ -345,6 +345,22 @@ int spax_ffn_decode(spax_layer *layer, const uint16_t *Wg, const uint16_t *Wu,
                     const uint16_t *x, double top_frac, double mid_frac, float *y,
                     float *a_out, void *stream);
 
+/* SelectInfer x SpAx: the SpAx token restricted to a selected set. Only the
+ * n_rows neurons listed in rows (device int32, distinct, in [0, N); e.g. the
+ * loaded indices of si_select_dynamic's S) get their gate/up dot products
+ * (a[n] = silu(Wg[n].x) * (Wu[n].x)); every other neuron has a = 0. The
+ * tiers are then taken inside the selected set: k_top = si_count(top_frac,
+ * n_rows) columns by |a| in bf16, the next k_mid = si_count(mid_frac, n_rows)
+ * from their codes, the rest (and every unselected column) skipped, so the
+ * call reads only the selected rows of Wg/Wu and the top/middle columns of
+ * the selected set. y fp32 [d]; a_out (optional) fp32 [N] receives a (zeros
+ * outside the set). n_rows = 0 gives y = 0. An index outside [0, N) sets
+ * SI_DEVERR_COUNT and reads neuron 0 instead. Requires top_frac, mid_frac
+ * >= 0, top_frac + mid_frac <= 1. */
+int spax_select_decode(spax_layer *layer, const uint16_t *Wg, const uint16_t *Wu, const int32_t *rows,
+                       int n_rows, const uint16_t *x, double top_frac, double mid_frac, float *y,
+                       float *a_out, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

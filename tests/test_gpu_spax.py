@@ -169,3 +169,43 @@ def test_spax_dense_act_repeated_calls(si, llama8b_layer):
         si.spax_dense_act(gWg, gWu, xd, a.t)
     assert rel_err(a.numpy(), ref) <= 1e-5
     assert si.si_device_error() == 0
+
+
+@pytest.mark.parametrize("d,N,frac,top,mid,bits", [(4096, 14336, 0.4, 0.3, 0.3, 4), (256, 1000, 0.5, 0.5, 0.5, 2),
+                                                  (256, 1000, 0.05, 0.2, 0.3, 8), (256, 1000, 0.0, 0.3, 0.3, 4)])
+def test_spax_select_decode(si, d, N, frac, top, mid, bits, llama8b_layer):
+    """SelectInfer x SpAx: gate/up only on a selected set, tiers inside it
+    (fractions of the set), the down-projection over its top and middle
+    columns; against the oracle's dense activations zeroed outside the set."""
+    if (d, N) == (4096, 14336):
+        Wg, Wu, Wd = llama8b_layer
+    else:
+        Wg, Wu, Wd = synth.layer_weights(58, 0, d, N)
+    layer = si.spax_encode(dev_bf16(Wd), bits, 128)
+    codes, params = oracle.spax_encode(Wd, bits, 128)
+    n_rows = si.si_count(frac, N)
+    rows = np.sort(np.random.default_rng(59).choice(N, n_rows, replace=False)).astype(np.int32)
+    x = synth.tokens(58, 0, synth.T_DECODE, 1, d)[0]
+    y = Guarded((d,), torch().float32, fill=float("nan"))
+    a_out = Guarded((N,), torch().float32, fill=float("nan"))
+    rows_d = dev(rows) if n_rows else torch().empty((0,), dtype=torch().int32, device="cuda")
+    si.spax_select_decode(layer, dev_bf16(Wg), dev_bf16(Wu), rows_d, dev_bf16(x), top, mid, y.t, a_out.t)
+    if n_rows == 0:
+        assert not y.numpy().any() and not a_out.numpy().any()
+        layer.close()
+        return
+    a_ref = np.zeros(N, np.float32)
+    a_ref[rows] = oracle.dense_act(Wg[rows], Wu[rows], x).astype(np.float32)
+    got_a = a_out.numpy()
+    assert not np.delete(got_a, rows).any()
+    assert rel_err(got_a[rows], a_ref[rows]) <= 1e-5
+    k_top, k_mid = si.si_count(top, n_rows), si.si_count(mid, n_rows)
+    rt, rm = oracle.spax_tiers(got_a, k_top, k_mid)        # the tiers of the a the GPU computed
+    assert np.isin(rt, rows).all() and np.isin(rm, rows).all()
+    ref = oracle.spax_down(got_a, Wd, codes, params, rt, rm, bits=bits)
+    assert rel_err(y.numpy(), ref) <= 2e-5
+    # and within the FFN bar of the oracle's own activations
+    rt2, rm2 = oracle.spax_tiers(a_ref, k_top, k_mid)
+    ref2 = oracle.spax_down(a_ref, Wd, codes, params, rt2, rm2, bits=bits)
+    assert rel_err(y.numpy(), ref2) <= TOL
+    layer.close()
