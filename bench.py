@@ -511,6 +511,7 @@ def run_spax(si, torch, dev, stream, args):
     dense_bytes = w.L * 2 * w.N * w.d * 2
     dense_s = dense_ms / 1e3 / (toks * w.L)
     hbm_peak, _, _, kind = peaks()
+    select = spax_in_selected_set(si, torch, dev, stream, W, enc, seed)
     widths = spax_code_widths(si, torch, dev, stream, W, seed)
     return {"workload": w.name, "tokens": toks, "tokens_per_s": round(1.0 / per_tok, 2),
             "ms_per_token": round(per_tok * 1e3, 4), "hbm_gbs": round(byts / per_tok / 1e9, 1),
@@ -519,7 +520,41 @@ def run_spax(si, torch, dev, stream, args):
                                    "achieved": round(dense_bytes / w.L / dense_s / 1e9, 1), "peak": hbm_peak,
                                    "unit": "GB/s", "frac": round(dense_bytes / w.L / dense_s / 1e9 / hbm_peak, 4),
                                    "peak_source": kind},
-            "code_widths": widths}
+            "code_widths": widths, "in_selected_set": select}
+
+
+def spax_in_selected_set(si, torch, dev, stream, W, enc, seed, layers=4, toks=64, phi=0.4):
+    """SelectInfer x SpAx on the first `layers` layers: gate/up only on a selected
+    set of phi*N neurons, then the top/middle tiers as fractions of that set."""
+    w = SPAX_WL
+    n_rows = si.si_count(phi, w.N)
+    gen = torch.Generator(device="cpu").manual_seed(seed + 7)
+    rows = [torch.sort(torch.randperm(w.N, generator=gen)[:n_rows])[0].to(torch.int32).to(dev) for _ in range(layers)]
+    x = gpu_tokens(torch, seed, 402, toks * layers, w.d, dev).view(toks, layers, w.d)
+    y = torch.empty((toks, layers, w.d), dtype=torch.float32, device=dev)
+    a = torch.empty((layers, w.N), dtype=torch.float32, device=dev)
+
+    def run():
+        for t in range(toks):
+            for l in range(layers):
+                si.spax_select_decode(enc[l], W[l][0], W[l][1], rows[l], x[t, l], w.top_frac, w.mid_frac, y[t, l], a[l])
+
+    with torch.cuda.stream(stream):
+        run()
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            run()
+        g.replay()
+        e0, e1 = time_graph(torch, g, stream)
+        stream.synchronize()
+    assert si.si_device_error() == 0
+    us = e0.elapsed_time(e1) * 1e3 / (toks * layers)
+    k_top, k_mid = si.si_count(w.top_frac, n_rows), si.si_count(w.mid_frac, n_rows)
+    ngp = -(-(w.d // w.group) // 2) * 2
+    byts = n_rows * 2 * w.d * 2 + k_top * 2 * w.d + k_mid * (w.d * w.bits // 8 + 8 * ngp)
+    return {"phi": phi, "selected": n_rows, "k_top": k_top, "k_mid": k_mid, "us_per_layer_token": round(us, 2),
+            "bytes_per_layer_token": byts, "hbm_gbs": round(byts / us / 1e3, 1)}
 
 
 def spax_code_widths(si, torch, dev, stream, W, seed, layers=4, toks=64):
