@@ -10,6 +10,9 @@
  *          Decoding on Offloaded Weights": abstract; Fig. 2 (offline
  *          encoding, per-token tier choice); Fig. 3 (middle-tier column
  *          rebuilt from its own b-bit codes).
+ *   [WI]   WiSparse ("Weight-aware Mixed-Granularity Training-free
+ *          Activation Sparsity"), abstract: activation magnitudes combined
+ *          with precomputed weight norms (si_layer_set_salience).
  *   [LS]   "LeanStream: A Speculate-and-Refine Streaming Framework for
  *          Efficient on-Device LLM Inference", permutation-invariant
  *          execution: a SwiGLU FFN output is a sum over hidden neurons, so

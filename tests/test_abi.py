@@ -78,6 +78,10 @@ def test_validation_before_cuda(si):
     for good in (64, 80, 96, 112, 128, 0):
         assert lib.si_set_gemm_tile(good) == si.SI_OK
     assert lib.si_gemm_tile_for(512, 5734, None) == si.SI_ERR_INVALID_ARG
+    # the extensions' entry points validate on the host too
+    assert lib.si_layer_set_salience(None, 1) == si.SI_ERR_INVALID_ARG
+    assert lib.si_layer_norms(None, C.byref(C.c_void_p())) == si.SI_ERR_INVALID_ARG
+    assert lib.spax_select_decode(None, p, p, p, 1, p, 0.3, 0.3, p, None, None) == si.SI_ERR_INVALID_ARG
     # |A| goes out by TMA: a misaligned output is refused before any launch
     odd = C.c_void_p(16 * 1024 + 4)
     assert lib.si_prefill_absact(p, p, 4, 1, odd, None) == si.SI_ERR_INVALID_ARG
