@@ -58,6 +58,7 @@ def _declare(L):
     L.oracle_merge_scores.argtypes = [C.POINTER(C.c_void_p), C.POINTER(ll), i, i, _f32p]
     L.oracle_sparse_layers.argtypes, L.oracle_sparse_layers.restype = [i, i, i, _u8p], i
     L.oracle_down_norms.argtypes = [_u16p, i, i, _i32p, i, _f64p]
+    L.oracle_expand_clusters.argtypes, L.oracle_expand_clusters.restype = [_i32p, i, _i32p, i, i, i, _i32p], i
     L.oracle_rank_loaded.argtypes = [_f32p, _f32p, i, d, d, _i32p, _u8p, C.POINTER(i), C.POINTER(i)]
     L.oracle_rank_loaded.restype = i
     L.oracle_loaded_bytes.argtypes, L.oracle_loaded_bytes.restype = [i, i, i], ll
@@ -126,6 +127,17 @@ def down_norms(Wd, loaded):
     out = np.zeros(loaded.shape[0], np.float64)
     lib().oracle_down_norms(Wd, d, N, loaded, loaded.shape[0], out)
     return out
+
+
+def expand_clusters(loaded, S, N, cluster):
+    """Positions of every loaded neuron in a cluster (contiguous block of
+    `cluster` neuron indices) that holds a neuron of the selected positions S."""
+    loaded, S = _c(loaded, np.int32), _c(S, np.int32)
+    out = np.zeros(max(loaded.shape[0], 1), np.int32)
+    n = lib().oracle_expand_clusters(loaded, loaded.shape[0], S, S.shape[0], int(N), int(cluster), out)
+    if n < 0:
+        raise ValueError("cluster size must be >= 1")
+    return out[:n].copy()
 
 
 def rank_loaded(task, model, gamma, delta):

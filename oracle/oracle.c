@@ -24,6 +24,7 @@
  *   oracle_sparse_layers   Table 1's values read as words ("first layer 5",
  *                          "skip last 2") at several depths
  *   oracle_down_norms      closed forms (constant columns) and numpy.linalg.norm
+ *   oracle_expand_clusters hand-worked expansions, S_c = 1 identity, brute force
  *   oracle_rank_loaded     subset enumeration on tiny N, Table 1 / Eq. 2 counts
  *   oracle_topk_rows       subset enumeration on tiny rows with forced ties
  *   oracle_select          subset enumeration of the top-beta step, counting
@@ -192,6 +193,26 @@ void oracle_down_norms(const uint16_t *Wd, int d, int N, const int *loaded, int 
         }
         norm[p] = sqrt(acc);
     }
+}
+
+/* Cluster-granular selection (PowerInfer-2 neuron clusters, quoted as prior
+ * art on the pages: contiguous blocks C_k of S_c neuron indices, k*S_c ..
+ * (k+1)*S_c - 1; when one neuron of a cluster is predicted active the whole
+ * cluster is brought in). Applied to a computed set: out receives, in
+ * ascending order, every packed position p (loaded neuron loaded[p]) whose
+ * cluster loaded[p] / S_c holds the neuron of some selected position S[i].
+ * Returns the count, or -1 for S_c < 1. */
+int oracle_expand_clusters(const int *loaded, int n_loaded, const int *S, int n_sel, int N, int S_c, int *out)
+{
+    if (S_c < 1) return -1;
+    int nc = (N + S_c - 1) / S_c;
+    uint8_t *hit = (uint8_t *)calloc((size_t)(nc > 0 ? nc : 1), 1);
+    for (int i = 0; i < n_sel; ++i) hit[loaded[S[i]] / S_c] = 1;
+    int n = 0;
+    for (int p = 0; p < n_loaded; ++p)
+        if (hit[loaded[p] / S_c]) out[n++] = p;
+    free(hit);
+    return n;
 }
 
 /* ------------------------------------------------------------ a2 loading */

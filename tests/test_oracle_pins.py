@@ -394,3 +394,34 @@ def test_down_norms():
     loaded = np.array([39, 0, 17, 5], np.int32)
     ref = np.linalg.norm(f32(Wr)[:, loaded], axis=0)
     assert np.allclose(oracle.down_norms(Wr, loaded), ref, rtol=1e-12, atol=0)
+
+
+def test_expand_clusters():
+    """Cluster-granular selection: whole clusters of contiguous neuron indices
+    come in when any of their neurons is selected."""
+    # loaded neurons (positions 0..7) and clusters of 4 neuron indices
+    loaded = np.array([0, 2, 3, 5, 6, 9, 12, 13], np.int32)
+    # select position 1 (neuron 2, cluster 0) and position 6 (neuron 12, cluster 3)
+    got = oracle.expand_clusters(loaded, np.array([1, 6], np.int32), 16, 4)
+    assert got.tolist() == [0, 1, 2, 6, 7]           # neurons 0, 2, 3 and 12, 13
+    # position 3 (neuron 5, cluster 1) brings neuron 6 too; cluster 2 holds only neuron 9
+    assert oracle.expand_clusters(loaded, np.array([3], np.int32), 16, 4).tolist() == [3, 4]
+    assert oracle.expand_clusters(loaded, np.array([5], np.int32), 16, 4).tolist() == [5]
+    # clusters of one neuron change nothing; an empty selection stays empty
+    S = np.array([0, 3, 7], np.int32)
+    assert np.array_equal(oracle.expand_clusters(loaded, S, 16, 1), S)
+    assert oracle.expand_clusters(loaded, np.zeros(0, np.int32), 16, 8).size == 0
+    # brute force on random sets: the result is the positions whose cluster meets S
+    rng = np.random.default_rng(11)
+    for _ in range(20):
+        N = int(rng.integers(8, 200))
+        loaded = np.sort(rng.choice(N, int(rng.integers(1, N)), replace=False)).astype(np.int32)
+        S = np.sort(rng.choice(len(loaded), int(rng.integers(0, len(loaded) + 1)), replace=False)).astype(np.int32)
+        c = int(rng.choice([1, 2, 3, 32, 64]))
+        hit = {int(loaded[s]) // c for s in S}
+        ref = [p for p in range(len(loaded)) if int(loaded[p]) // c in hit]
+        got = oracle.expand_clusters(loaded, S, N, c)
+        assert got.tolist() == ref
+        assert set(S.tolist()) <= set(got.tolist())
+    with pytest.raises(ValueError):
+        oracle.expand_clusters(loaded, S, N, 0)
