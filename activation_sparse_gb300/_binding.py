@@ -40,6 +40,7 @@ SIGNATURES = {
     "si_gemm_tile_for": (_i, [_i, _i, _ip]),
     "si_select_from_absact": (_i, [_vp, _vp, _i, _i, _i, _i, _d, _vp, _vp, _vp, _vp]),
     "si_decode_plan": (_i, [_vp, _vp, _i, _i, _vp]),
+    "si_expand_clusters": (_i, [_vp, _vp, _i, _i, _vp, _ip, _vp]),
     "si_sparse_ffn_decode": (_i, [_vp, _vp, _i, _i, _vp, _vp, _vp]),
     "si_sparse_ffn_decode_residual": (_i, [_vp, _vp, _i, _i, _vp, _vp, _vp]),
     "si_sparse_ffn_decode_noalloc": (_i, [_vp, _i, _i, _vp, _i, _vp, _vp, _vp]),
@@ -264,6 +265,15 @@ def si_select_from_absact(layer: Layer, absA, T, B, alpha, phi, S, topmask=None,
                                         _ptr(topmask, u32, "topmask"), _ptr(counts, u32, "counts"),
                                         _stream(stream)))
     return S
+
+
+def si_expand_clusters(layer: Layer, S, n_sel, cluster, S_out, stream=None) -> int:
+    """Whole clusters of `cluster` contiguous neurons around the selected positions S; returns len."""
+    n = C.c_int(0)
+    _check(load().si_expand_clusters(layer.handle, _ptr(S, _torch().int32, "S") if n_sel else None, int(n_sel),
+                                     int(cluster), _ptr(S_out, _torch().int32, "S_out"), C.byref(n),
+                                     _stream(stream)))
+    return n.value
 
 
 def si_decode_plan(layer: Layer, S, n_sel, B, stream=None):

@@ -106,6 +106,7 @@ struct si_layer {
     int32_t* plan_pos = nullptr;
     uint32_t* plan_mask = nullptr;
     int* plan_n = nullptr;
+    int* cluster_n = nullptr;   // count of si_expand_clusters (allocated on first use)
     const int32_t* plan_S = nullptr;
     int plan_nsel = -1, plan_B = 0;
     // True from si_decode_plan until the next decode launch on this handle: that
@@ -157,6 +158,7 @@ void destroy_layer(si_layer* L) {
     dfree(L->plan_pos);
     dfree(L->plan_mask);
     dfree(L->plan_n);
+    dfree(L->cluster_n);
     delete L;
 }
 
@@ -469,6 +471,25 @@ int si_select_dynamic(si_layer* L, const uint16_t* X, int T, int B, int alpha, d
 }
 
 // ------------------------------------------------------------------ a7
+
+int si_expand_clusters(si_layer* L, const int32_t* S, int n_sel, int cluster, int32_t* S_out, int* n_out,
+                       void* stream) {
+    if (!L || !S_out || !n_out || (n_sel > 0 && !S)) return fail(SI_ERR_INVALID_ARG, "NULL pointer");
+    if (cluster < 1) return fail(SI_ERR_INVALID_ARG, "cluster size must be >= 1");
+    if (n_sel < 0 || n_sel > L->n_loaded) return fail(SI_ERR_INVALID_ARG, "need 0 <= n_sel <= n_loaded");
+    cudaStream_t st = (cudaStream_t)stream;
+    if (capturing(st)) return fail(SI_ERR_INVALID_ARG, "si_expand_clusters reads its count back; not during capture");
+    unsigned* err = nullptr;
+    int rc = err_word(&err);
+    if (rc) return rc;
+    if (!L->cluster_n && (rc = dalloc(&L->cluster_n, 1, "cluster count"))) return rc;
+    SI_CK(si::launch_expand_clusters(L->loaded, L->n_loaded, S, n_sel, L->N, cluster, S_out, L->cluster_n, err, st));
+    int n = 0;
+    SI_CK(cudaMemcpyAsync(&n, L->cluster_n, sizeof(int), cudaMemcpyDeviceToHost, st));
+    SI_CK(cudaStreamSynchronize(st));
+    *n_out = n;
+    return SI_OK;
+}
 
 int si_decode_plan(si_layer* L, const int32_t* S, int n_sel, int B, void* stream) {
     if (!L || (!S && n_sel > 0)) return fail(SI_ERR_INVALID_ARG, "NULL pointer");

@@ -84,6 +84,8 @@ cudaError_t launch_rank_loaded(const float* task, const float* model, int N, int
                                int32_t* loaded, uint8_t* is_static, unsigned* err, cudaStream_t st);
 cudaError_t launch_decode_plan(const int32_t* S, int n_sel, int B, int n, int32_t* pos, uint32_t* pmask,
                                int* count, unsigned* err, cudaStream_t st);
+cudaError_t launch_expand_clusters(const int32_t* loaded, int n_loaded, const int32_t* S, int n_sel, int N,
+                                  int csize, int32_t* out, int* count, unsigned* err, cudaStream_t st);
 cudaError_t launch_merge_scores(const float* const* s, const float* tok, int nfiles, int N, float* out,
                                 cudaStream_t st);
 

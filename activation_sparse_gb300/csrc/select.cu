@@ -499,6 +499,40 @@ __global__ void k_merge_scores(MergeArgs args, int N, float* __restrict__ out) {
     }
 }
 
+// Cluster-granular selection (PowerInfer-2 neuron clusters: contiguous blocks
+// of csize neuron indices; when one neuron of a cluster is predicted active
+// the whole cluster is brought in), applied to a computed set S. One CTA:
+// the clusters of the selected positions' neurons are marked in a shared
+// bitmap, then every packed position whose neuron's cluster is marked is
+// written in ascending order (ballot compaction), with the count.
+__global__ void __launch_bounds__(1024) k_expand_clusters(const int32_t* __restrict__ loaded, int n_loaded,
+                                                         const int32_t* __restrict__ S, int n_sel, int N, int csize,
+                                                         int32_t* __restrict__ out, int* __restrict__ count,
+                                                         unsigned* err) {
+    extern __shared__ uint32_t s_hit[];  // one bit per cluster
+    __shared__ uint32_t scnt[2 * 1024 / 32];
+    const int nc = (N + csize - 1) / csize, nw = (nc + 31) / 32;
+    for (int i = threadIdx.x; i < nw; i += 1024) s_hit[i] = 0u;
+    __syncthreads();
+    for (int i = threadIdx.x; i < n_sel; i += 1024) {
+        const int p = S[i];
+        if (p < 0 || p >= n_loaded) {
+            atomicOr(err, SI_DEVERR_COUNT);
+            continue;
+        }
+        const int c = loaded[p] / csize;
+        atomicOr(&s_hit[c >> 5], 1u << (c & 31));
+    }
+    __syncthreads();
+    auto pred = [&](int p) -> bool {
+        const int c = loaded[p] / csize;
+        return (s_hit[c >> 5] >> (c & 31)) & 1u;
+    };
+    auto put = [&](int p, int r) { out[r] = p; };
+    const int total = block_compact<1024>(n_loaded, pred, put, scnt);
+    if (threadIdx.x == 0) *count = total;
+}
+
 // ------------------------------------------------------------------ launchers
 
 namespace {
@@ -567,6 +601,14 @@ cudaError_t launch_merge_scores(const float* const* s, const float* tok, int nfi
     a.nfiles = nfiles;
     const int blocks = (N + 255) / 256 < 1024 ? (N + 255) / 256 : 1024;
     k_merge_scores<<<blocks, 256, 0, st>>>(a, N, out);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_expand_clusters(const int32_t* loaded, int n_loaded, const int32_t* S, int n_sel, int N,
+                                  int csize, int32_t* out, int* count, unsigned* err, cudaStream_t st) {
+    const int nc = (N + csize - 1) / csize;
+    const size_t smem = (size_t)((nc + 31) / 32) * 4;
+    k_expand_clusters<<<1, 1024, smem, st>>>(loaded, n_loaded, S, n_sel, N, csize, out, count, err);
     return cudaGetLastError();
 }
 

@@ -228,6 +228,21 @@ int si_select_from_absact(si_layer *layer, const float *absA, int ld, int T, int
 
 /* --------------------------------------------------- a7: sparse decode */
 
+/* Cluster-granular selection (the PowerInfer-2 neuron clusters the pages
+ * quote: contiguous blocks of `cluster` neuron indices, k*cluster ..
+ * (k+1)*cluster - 1; when one neuron of a cluster is predicted active the
+ * whole cluster is brought in), applied to one computed set: S_out (device
+ * int32, capacity n_loaded) receives, ascending, every packed position whose
+ * loaded neuron lies in a cluster that holds the neuron of some position of
+ * S (device int32 [n_sel], packed positions); *n_out (host) its length. The
+ * result is a computed set for si_decode_plan / the decode calls. For B
+ * sequences call it once per sequence. Synchronous (reads the count back;
+ * not during stream capture). A position of S outside [0, n_loaded) sets
+ * SI_DEVERR_COUNT and is ignored. Requires cluster >= 1, 0 <= n_sel <=
+ * n_loaded. */
+int si_expand_clusters(si_layer *layer, const int32_t *S, int n_sel, int cluster, int32_t *S_out,
+                       int *n_out, void *stream);
+
 /* Builds, inside the handle, the decode plan for the computed sets S[b]
  * (b < B): the union of the B ascending lists S[b][0..n_sel) with, per union
  * entry, a bit mask of the sequences that selected it, so decode reads each

@@ -82,6 +82,8 @@ def test_validation_before_cuda(si):
     assert lib.si_layer_set_salience(None, 1) == si.SI_ERR_INVALID_ARG
     assert lib.si_layer_norms(None, C.byref(C.c_void_p())) == si.SI_ERR_INVALID_ARG
     assert lib.spax_select_decode(None, p, p, p, 1, p, 0.3, 0.3, p, None, None) == si.SI_ERR_INVALID_ARG
+    n = C.c_int(0)
+    assert lib.si_expand_clusters(None, p, 1, 32, p, C.byref(n), None) == si.SI_ERR_INVALID_ARG
     # |A| goes out by TMA: a misaligned output is refused before any launch
     odd = C.c_void_p(16 * 1024 + 4)
     assert lib.si_prefill_absact(p, p, 4, 1, odd, None) == si.SI_ERR_INVALID_ARG

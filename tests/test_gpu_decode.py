@@ -203,3 +203,23 @@ def test_layer_range_stack(si):
         ref = oracle.sparse_ffn(c.Wg, c.Wu, c.Wd, c.loaded, c.S[0], x[0])
         assert rel_err(y.numpy()[0], ref) <= TOL
         c.layer.close()
+
+
+@pytest.mark.parametrize("cluster", [1, 32, 64, 128])
+def test_expand_clusters_then_decode(si, cluster):
+    """Cluster-granular selection on a Llama3.2-1B layer's computed set:
+    bit-exact with the oracle's expansion, and the decode on the expanded set
+    matches the oracle's FFN on it."""
+    c = Case(si, 2048, 8192, 0.7, 0.2, 0.4, 1024, 16, 1)
+    out = Guarded((c.layer.n_loaded,), torch().int32, fill=-1)
+    n = si.si_expand_clusters(c.layer, dev(c.S[0]), c.n_sel, cluster, out.t)
+    ref = oracle.expand_clusters(c.loaded, c.S[0], c.N, cluster)
+    assert n == len(ref)
+    assert np.array_equal(out.numpy()[:n], ref)
+    assert (n == c.n_sel) == (cluster == 1)
+    x = synth.tokens(42, 0, synth.T_DECODE, 1, c.d)
+    y = Guarded((1, c.d), torch().float32, fill=float("nan"))
+    si.si_sparse_ffn_decode(c.layer, dev(ref).view(1, -1), n, 1, dev_bf16(x), y.t)
+    y_ref = oracle.sparse_ffn(c.Wg, c.Wu, c.Wd, c.loaded, ref, x[0])
+    assert rel_err(y.numpy()[0], y_ref) <= TOL
+    c.layer.close()
