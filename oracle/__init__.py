@@ -68,6 +68,7 @@ def _declare(L):
     L.oracle_select.restype = i
     L.oracle_sparse_ffn.argtypes = [_u16p, _u16p, _u16p, i, i, _i32p, _i32p, i, _u16p, _f64p]
     L.oracle_dense_act.argtypes = [_u16p, _u16p, i, i, _u16p, _f64p]
+    L.oracle_swiglu.argtypes = [_f64p, _f64p, i, _f64p]
     L.oracle_spax_encode.argtypes = [_u16p, i, i, i, i, _u8p, _f32p]
     L.oracle_spax_encode.restype = i
     L.oracle_spax_tiers.argtypes = [_f32p, i, i, i, _i32p, _i32p]
@@ -208,6 +209,33 @@ def dense_act(Wg, Wu, x):
     a = np.zeros(N, np.float64)
     lib().oracle_dense_act(Wg, Wu, d, N, x, a)
     return a
+
+
+def swiglu(g, u):
+    """silu(g) * u elementwise (float64)."""
+    g, u = _c(g, np.float64), _c(u, np.float64)
+    out = np.zeros(g.shape[0], np.float64)
+    lib().oracle_swiglu(g, u, g.shape[0], out)
+    return out
+
+
+def spax_gate_up(x, Wg, Wu, top_frac, mid_frac, bits=4, group=128):
+    """SpAx tiers on the gate/up projections by |x| (the pages' "ALL"
+    configuration, FFN part): the input channels j ranked by |x_j| (ties to
+    the lower index); the top k_top columns of Wg / Wu read in bf16, the next
+    k_mid rebuilt from b-bit codes of each column (groups along the neuron
+    axis), the rest skipped; then a = silu(g) * u. Wg, Wu: bf16 bits [N x d]
+    (output x input, like Wd), x: bf16 bits [d]. Returns (a, top, mid)."""
+    Wg, Wu, x = _c(Wg, np.uint16), _c(Wu, np.uint16), _c(x, np.uint16)
+    d = x.shape[0]
+    xf = (x.astype(np.uint32) << 16).view(np.float32)
+    k_top, k_mid = cnt(top_frac, d), cnt(mid_frac, d)
+    top, mid = spax_tiers(xf, k_top, k_mid)
+    cg, pg = spax_encode(Wg, bits, group)
+    cu, pu = spax_encode(Wu, bits, group)
+    g = spax_down(xf, Wg, cg, pg, top, mid, bits, group)
+    u = spax_down(xf, Wu, cu, pu, top, mid, bits, group)
+    return swiglu(g, u), top, mid
 
 
 def spax_encode(Wd, bits=4, group=128):

@@ -34,6 +34,8 @@
  *   oracle_spax_encode     error bound |w - w^| <= scale/2, constant and ramp groups
  *   oracle_spax_tiers      subset enumeration on tiny N
  *   oracle_spax_down       dense numpy product when top = 100% / mid = 100%
+ *   oracle_swiglu          closed-form silu values; with spax_down, the dense
+ *                          activations when every input channel is top tier
  */
 #include <math.h>
 #include <stdint.h>
@@ -372,6 +374,15 @@ void oracle_dense_act(const uint16_t *Wg, const uint16_t *Wu, int d, int N, cons
 {
     #pragma omp parallel for schedule(static)
     for (int n = 0; n < N; ++n) a[n] = act(Wg + (size_t)n * d, Wu + (size_t)n * d, x, d);
+}
+
+/* a_n = silu(g_n) * u_n from given projections (double): the last step of
+ * the gate/up pass when the projections themselves come from a tiered
+ * product (SpAx's tiers applied to gate/up by |x|, the pages' "ALL"
+ * configuration for the FFN). */
+void oracle_swiglu(const double *g, const double *u, int n, double *a)
+{
+    for (int i = 0; i < n; ++i) a[i] = silu(g[i]) * u[i];
 }
 
 /* --------------------------------------------------------- a8 SpAx encode */

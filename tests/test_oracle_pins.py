@@ -425,3 +425,33 @@ def test_expand_clusters():
         assert set(S.tolist()) <= set(got.tolist())
     with pytest.raises(ValueError):
         oracle.expand_clusters(loaded, S, N, 0)
+
+
+def test_swiglu_closed_form():
+    g = np.array([0.0, 1.0, -1.0, 30.0, -30.0])
+    u = np.array([5.0, 2.0, 2.0, 1.0, 1.0])
+    got = oracle.swiglu(g, u)
+    ref = [0.0, 2.0 / (1 + np.exp(-1.0)), -2.0 / (1 + np.exp(1.0)), 30.0 / (1 + np.exp(-30.0)),
+           -30.0 / (1 + np.exp(30.0))]
+    assert np.allclose(got, ref, rtol=1e-15, atol=1e-300)
+
+
+def test_spax_gate_up_special_cases():
+    """Tiers on gate/up by |x|: every channel in the top tier is the dense
+    activation pass; no channel at all gives silu(0) * 0 = 0; the tiers rank
+    the input channels by |x|."""
+    d, N = 256, 256                 # groups of 128 along the neuron axis
+    Wg, Wu, _ = synth.layer_weights(71, 0, d, N)
+    x = synth.tokens(72, 0, synth.T_DECODE, 1, d)[0]
+    a, top, mid = oracle.spax_gate_up(x, Wg, Wu, 1.0, 0.0)
+    assert len(top) == d and len(mid) == 0
+    assert np.allclose(a, oracle.dense_act(Wg, Wu, x), rtol=1e-12, atol=1e-15)
+    a0, top0, mid0 = oracle.spax_gate_up(x, Wg, Wu, 0.0, 0.0)
+    assert len(top0) == 0 and len(mid0) == 0 and not a0.any()
+    _, t, m = oracle.spax_gate_up(x, Wg, Wu, 0.25, 0.25)
+    ax = np.abs(f32(x))
+    assert ax[t].min() >= ax[m].max() and len(t) == len(m) == 64
+    # a middle tier rebuilt from 8-bit codes stays close to the dense pass
+    a8, _, _ = oracle.spax_gate_up(x, Wg, Wu, 0.0, 1.0, bits=8)
+    ref = oracle.dense_act(Wg, Wu, x)
+    assert np.abs(a8 - ref).max() <= 0.05 * np.abs(ref).max()
