@@ -267,7 +267,10 @@ def run_gpu(args, world, rank, local):
         g_gemm.replay()
     stream.synchronize()
 
-    launches_per_step = w.L * 4 + w.decode_tokens * w.L   # gemm, top-alpha, top-beta, plan per layer; decode
+    # our kernels per step: GEMM, top-alpha, top-beta per layer (the counts
+    # are zeroed by a memset and the batch-1 plan is a device copy, neither a
+    # kernel of ours; the B > 1 plan is), then one decode launch per layer-token
+    launches_per_step = w.L * (3 + (1 if w.B > 1 else 0)) + w.decode_tokens * w.L
     pre_ms, dec_ms = [], []
     barrier(world)
     torch.cuda.synchronize()
