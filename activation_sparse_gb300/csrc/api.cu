@@ -241,14 +241,26 @@ long long si_packed_bytes(int d, int n_loaded) { return 3LL * d * n_loaded * 2; 
 
 int si_device_error(uint32_t* code, int clear) {
     if (!code) return fail(SI_ERR_INVALID_ARG, "code is NULL");
+    int dev = 0;
+    SI_CK(cudaGetDevice(&dev));
+    if (dev < 0 || dev >= 128) return fail(SI_ERR_UNSUPPORTED, "device ordinal out of range");
     unsigned* w = nullptr;
-    int rc = err_word(&w);
+    {
+        std::lock_guard<std::mutex> lk(g_err_mu);
+        w = g_err_word[dev];  // not allocated yet: no kernel has used it, so it reads as 0
+    }
+    unsigned* wn = nullptr;   // the no-allocation decode's reported word (a static device array)
+    int rc = si::noalloc_error_word(&wn);
     if (rc) return rc;
     SI_CK(cudaDeviceSynchronize());
-    unsigned v = 0;
-    SI_CK(cudaMemcpy(&v, w, sizeof v, cudaMemcpyDeviceToHost));
-    if (clear) SI_CK(cudaMemset(w, 0, sizeof(unsigned)));
-    *code = v;
+    unsigned v = 0, vn = 0;
+    if (w) SI_CK(cudaMemcpy(&v, w, sizeof v, cudaMemcpyDeviceToHost));
+    SI_CK(cudaMemcpy(&vn, wn, sizeof vn, cudaMemcpyDeviceToHost));
+    if (clear) {
+        if (w) SI_CK(cudaMemset(w, 0, sizeof(unsigned)));
+        SI_CK(cudaMemset(wn, 0, sizeof(unsigned)));
+    }
+    *code = v | vn;
     return SI_OK;
 }
 

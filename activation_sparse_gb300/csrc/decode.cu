@@ -235,8 +235,13 @@ constexpr double kFixScale = 4294967296.0;          // 2^32
 constexpr double kFixInv = 1.0 / 4294967296.0;
 constexpr float kFixLimit = 8388608.0f;               // 2^23
 
+// With err_report set, *err is a word that only this launch writes into (its
+// bounded waits stop early once it holds a timeout): the last CTA, which runs
+// after every other CTA has recorded its failures, moves its bits into
+// *err_report and clears it, so a failure never cuts short a later launch's waits.
 __device__ void fixed_point_reduce(const float* ypart, int BD, unsigned long long* __restrict__ acc,
-                                   unsigned* ticket, float* __restrict__ y, unsigned* err) {
+                                   unsigned* ticket, float* __restrict__ y, unsigned* err,
+                                   unsigned* err_report = nullptr) {
     __shared__ unsigned s_last;
     bool range_ok = true;
     for (int k = threadIdx.x; k < BD; k += blockDim.x) {
@@ -259,7 +264,13 @@ __device__ void fixed_point_reduce(const float* ypart, int BD, unsigned long lon
             y[k] = (float)((double)q * kFixInv);
             __stcg(acc + k, 0ull);
         }
-        if (threadIdx.x == 0) *ticket = 0u;
+        if (threadIdx.x == 0) {
+            *ticket = 0u;
+            if (err_report) {
+                const unsigned v = atomicExch(err, 0u);
+                if (v) atomicOr(err_report, v);
+            }
+        }
     }
 }
 
@@ -568,7 +579,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_sparse_decode_b1(SparseDecod
     }
     if (!P.accumulate) {
         __syncthreads();
-        fixed_point_reduce(reinterpret_cast<float*>(ring), d, P.acc, P.acc_ticket, P.y, P.err);
+        fixed_point_reduce(reinterpret_cast<float*>(ring), d, P.acc, P.acc_ticket, P.y, P.err, P.err_report);
     }
 }
 

@@ -27,6 +27,8 @@ struct SparseDecodeParams {
     unsigned long long* acc;  // [B*d] fixed-point accumulator, zero between launches
     unsigned* acc_ticket;     // zero between launches
     int accumulate;           // 1: y += result with float atomics (no cross-CTA ordering)
+    unsigned* err_report;     // optional (overwrite form only): the last CTA moves the bits of *err, which
+                              // then covers this launch alone, into *err_report and clears *err
 };
 
 
@@ -98,6 +100,10 @@ cudaError_t launch_spax_encode(const uint16_t* Wd, int d, int N, int bits, int g
 
 // api.cu: sets the message si_last_error_string() returns on this thread
 void set_error_message(const char* msg);
+
+// noalloc.cu: device address of the no-allocation entry point's reported
+// error word on the current device (looked up once per device; allocates nothing)
+int noalloc_error_word(unsigned** out);
 
 // decode.cu
 int sparse_decode_b1_stages(int d);

@@ -10,7 +10,8 @@
 //
 // The scratch is the 64-bit fixed-point accumulator of the output row (one
 // word per output element), the ticket that elects the CTA which converts it
-// to float, and an error word. The kernel is the same batch-1 decode kernel
+// to float, and two error words: one the launch's bounded waits watch, one
+// that si_device_error() reports. The kernel is the same batch-1 decode kernel
 // si_sparse_ffn_decode uses; only the scratch pointers differ.
 #include <mutex>
 #include <string>
@@ -24,13 +25,18 @@ namespace {
 // Largest output width this entry point accepts.
 constexpr int kNoAllocMaxD = 4096;
 
-// [0, kNoAllocMaxD): accumulator words; then the ticket and the error word.
-// Every GPU that loads the library holds these 32 KB until the process exits.
-// The accumulator and the ticket must be zero when a call starts: they are
-// zero at load, and every call's last CTA sets them back to zero. The error
-// word collects device-side failures of this entry point (a position outside
-// the packed records, a wait that ran out); it is zero at load and the
-// library never clears it.
+// [0, kNoAllocMaxD): accumulator words; word kNoAllocMaxD: the ticket (low
+// half); word kNoAllocMaxD + 1: the reported error word (low half) and the
+// launch's own error word (high half). Every GPU that loads the library holds
+// these 32 KB until the process exits. The accumulator, the ticket and the
+// launch's error word must be zero when a call starts: they are zero at load,
+// and every call's last CTA sets them back to zero, moving any failure the
+// launch recorded (a position outside the packed records, a wait that ran out,
+// a partial beyond the accumulator's range) into the reported word first. The
+// kernel's bounded waits watch only the launch's own word, so one failed call
+// does not cut short the waits of the calls after it. si_device_error() reads
+// the reported word (together with the library's other error word) and, on
+// request, clears it.
 static __device__ __align__(256) unsigned long long g_noalloc_scratch[kNoAllocMaxD + 2];
 
 std::mutex g_noalloc_mu;
@@ -60,6 +66,16 @@ int scratch_for_current_device(unsigned long long** out) {
 
 }  // namespace
 
+namespace si {
+int noalloc_error_word(unsigned** out) {
+    unsigned long long* scratch = nullptr;
+    const int rc = scratch_for_current_device(&scratch);
+    if (rc) return rc;
+    *out = reinterpret_cast<unsigned*>(scratch + kNoAllocMaxD + 1);
+    return SI_OK;
+}
+}  // namespace si
+
 extern "C" int si_sparse_ffn_decode_noalloc(const uint16_t* packed, int n_records, int d, const int32_t* S,
                                             int n_sel, const uint16_t* x, float* y, void* stream) {
     if (!packed || (!S && n_sel > 0) || !x || !y) return fail(SI_ERR_INVALID_ARG, "NULL pointer");
@@ -86,7 +102,8 @@ extern "C" int si_sparse_ffn_decode_noalloc(const uint16_t* packed, int n_record
     P.tickets = nullptr;
     P.acc = scratch;
     P.acc_ticket = reinterpret_cast<unsigned*>(scratch + kNoAllocMaxD);
-    P.err = reinterpret_cast<unsigned*>(scratch + kNoAllocMaxD + 1);
+    P.err = reinterpret_cast<unsigned*>(scratch + kNoAllocMaxD + 1) + 1;       // this launch's failures
+    P.err_report = reinterpret_cast<unsigned*>(scratch + kNoAllocMaxD + 1);   // what si_device_error reads
     P.R = R;
     P.stable_plan = 0;
     P.accumulate = 0;

@@ -97,9 +97,11 @@ long long si_packed_bytes(int d, int n_loaded);
  * with L > 0. */
 int si_sparse_layers(int L, int first, int last, uint8_t *sparse, int *n_sparse);
 
-/* Reads (and with clear != 0 resets) the device error word of the current
- * device. *code (host) receives 0 when no kernel reported a failure, else a
- * bit set of SI_DEVERR_* values. Synchronises the device. */
+/* Reads (and with clear != 0 resets) the device error words of the current
+ * device: the one every entry point's kernels write, and the one of
+ * si_sparse_ffn_decode_noalloc (inside its static array). *code (host)
+ * receives 0 when no kernel reported a failure, else the bit set (OR of both
+ * words) of SI_DEVERR_* values. Synchronises the device; allocates nothing. */
 #define SI_DEVERR_WAIT_TIMEOUT 1u   /* a bounded mbarrier wait ran out */
 #define SI_DEVERR_COUNT 2u          /* an index or count check failed (bad S / tier list, count mismatch) */
 #define SI_DEVERR_RANGE 4u          /* a decode partial exceeded the fixed-point accumulator's range (|y| >= 2^23) */
@@ -300,8 +302,11 @@ int si_sparse_ffn_decode_residual(si_layer *layer, const int32_t *S, int n_sel, 
  * All calls share the array: calls that overlap on the GPU (other streams,
  * other threads) race and give wrong results; order them on one stream.
  * Each call leaves the accumulator and ticket at zero for the next one.
- * Device-side failures go to the array's error word, which this entry point
- * does not report. */
+ * Device-side failures (a position outside [0, n_records), a bounded wait that
+ * ran out, a partial beyond the accumulator's range) are recorded per launch
+ * and moved by the launch's last CTA into a reported word in the same array:
+ * read and clear it with si_device_error(). A failed launch's y is not valid;
+ * later calls are unaffected (their waits watch only their own launch). */
 int si_sparse_ffn_decode_noalloc(const uint16_t *packed, int n_records, int d, const int32_t *S,
                                  int n_sel, const uint16_t *x, float *y, void *stream);
 

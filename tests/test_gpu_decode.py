@@ -50,8 +50,9 @@ def test_sparse_decode_parity(si, d, N, gamma, delta, phi, alpha, T, B, sigma):
     S_dev = dev(c.S)
     if B > 1:
         si.si_decode_plan(c.layer, S_dev, c.n_sel, B)
-    # batch 1: two calls without a plan (fused kernel), then three with one
-    # (gate/up pass + row-split down pass; the first waits for the plan)
+    # batch 1: two calls without a plan, then three with one (the first of
+    # them reads the plan after its dependency wait, the later ones stream
+    # the planned records before it)
     for tok in range(2 if B > 1 else 5):
         if B == 1 and tok == 2:
             si.si_decode_plan(c.layer, S_dev, c.n_sel, 1)
