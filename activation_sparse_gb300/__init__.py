@@ -13,6 +13,7 @@ from ._binding import (  # noqa: F401
     si_select_dynamic, si_prefill_absact, si_select_from_absact,
     si_set_gemm_tile, si_gemm_tile_for, si_layer_set_salience, si_layer_norms,
     si_decode_plan, si_expand_clusters, si_sparse_ffn_decode, si_sparse_ffn_decode_residual, si_sparse_ffn_decode_noalloc,
+    Stack, si_stack_create, si_stack_plan, si_sparse_ffn_decode_stack,
     spax_encode, spax_dense_act, spax_tiered_down, spax_ffn_decode, spax_select_decode,
     SI_OK, SI_ERR_INVALID_ARG, SI_ERR_CUDA, SI_ERR_OOM, SI_ERR_UNSUPPORTED, SI_ERR_DEVICE,
 )

@@ -44,6 +44,10 @@ SIGNATURES = {
     "si_sparse_ffn_decode": (_i, [_vp, _vp, _i, _i, _vp, _vp, _vp]),
     "si_sparse_ffn_decode_residual": (_i, [_vp, _vp, _i, _i, _vp, _vp, _vp]),
     "si_sparse_ffn_decode_noalloc": (_i, [_vp, _i, _i, _vp, _i, _vp, _vp, _vp]),
+    "si_stack_create": (_i, [C.POINTER(_vp), _i, C.POINTER(_vp)]),
+    "si_stack_plan": (_i, [_vp, C.POINTER(_vp), _ip, _vp]),
+    "si_sparse_ffn_decode_stack": (_i, [_vp, _vp, _vp, _vp]),
+    "si_stack_destroy": (_i, [_vp]),
     "spax_encode": (_i, [_vp, _i, _i, _i, _i, C.POINTER(_vp), _vp]),
     "spax_layer_info": (_i, [_vp, _ip, _ip, _ip, _ip, _ip]),
     "spax_layer_buffers": (_i, [_vp, C.POINTER(_vp), C.POINTER(_vp), C.POINTER(_vp)]),
@@ -301,6 +305,61 @@ def si_sparse_ffn_decode_noalloc(packed_ptr: int, n_records: int, d: int, S, n_s
                                                _ptr(S, torch.int32, "S"), int(n_sel), _bf16(x, "x"),
                                                _ptr(y, torch.float32, "y"), _stream(stream)))
     return y
+
+
+class Stack:
+    """A decode stack over packed layers (owns the library handle; the layers
+    must outlive it, and it keeps references to them)."""
+
+    def __init__(self, handle, layers):
+        self._h = handle
+        self.layers = list(layers)
+        self.L = len(self.layers)
+        self.d = self.layers[0].d
+
+    @property
+    def handle(self):
+        return self._h
+
+    def close(self):
+        if self._h:
+            load().si_stack_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def si_stack_create(layers) -> Stack:
+    hs = (C.c_void_p * len(layers))(*[l.handle for l in layers])
+    h = C.c_void_p()
+    _check(load().si_stack_create(hs, len(layers), C.byref(h)))
+    return Stack(h, layers)
+
+
+def si_stack_plan(stack: Stack, S_list, n_sel_list, stream=None):
+    """Copies each layer's computed set (device int32, ascending positions) into the stack."""
+    torch = _torch()
+    ptrs = []
+    for S, n in zip(S_list, n_sel_list):
+        ptrs.append(_ptr(S, torch.int32, "S").value if int(n) > 0 else None)
+    arr = (C.c_void_p * stack.L)(*ptrs)
+    ns = (C.c_int * stack.L)(*[int(n) for n in n_sel_list])
+    _check(load().si_stack_plan(stack.handle, arr, ns, _stream(stream)))
+
+
+def si_sparse_ffn_decode_stack(stack: Stack, h, x_out=None, stream=None):
+    """One decode token through every layer of the stack: h (fp32 [d], read
+    and written) is the residual stream; x_out (optional bf16 [L][d]) gets each
+    layer's input."""
+    torch = _torch()
+    _check(load().si_sparse_ffn_decode_stack(stack.handle, _ptr(h, torch.float32, "h"),
+                                             _bf16(x_out, "x_out") if x_out is not None else None,
+                                             _stream(stream)))
+    return h
 
 
 class SpaxLayer:

@@ -130,6 +130,21 @@ struct spax_layer {
     unsigned* tickets = nullptr;
 };
 
+// A decode stack: L packed layers (not owned) decoded one token at a time by
+// one launch (si_sparse_ffn_decode_stack).
+struct si_stack {
+    int device = 0;
+    int L = 0, d = 0;
+    si_layer* layers[si::kStackMaxLayers] = {};
+    long long pos_off[si::kStackMaxLayers + 1] = {};  // offsets of the plan copies in pos
+    int32_t* pos = nullptr;                  // plan copies of the computed sets (capacity sum of n_loaded)
+    si::StackLayerDesc* desc = nullptr;      // [L] device
+    si::StackLayerDesc* desc_host = nullptr; // [L] pinned host staging of desc
+    float* delta = nullptr;                  // [L][kDeltaCopies][d], zero between launches
+    unsigned* sync = nullptr;                // barrier counters, ticket, error word; zero between launches
+    bool planned = false;
+};
+
 namespace {
 
 int grow_part(float** part, long long* cap, int d, int B) {
@@ -810,6 +825,135 @@ int spax_ffn_decode(spax_layer* L, const uint16_t* Wg, const uint16_t* Wu, const
         cudaMemsetAsync(L->hist, 0, (si::kTierBins + 1) * sizeof(unsigned), st);  // leave it clean
         return rc;
     }
+    return SI_OK;
+}
+
+}  // extern "C"
+
+namespace {
+
+void destroy_stack(si_stack* K) {
+    if (!K) return;
+    dfree(K->pos);
+    dfree(K->desc);
+    dfree(K->delta);
+    dfree(K->sync);
+    if (K->desc_host) cudaFreeHost(K->desc_host);
+    delete K;
+}
+
+}  // namespace
+
+extern "C" {
+
+// ------------------------------------------------------- a7: decode stack
+
+int si_stack_create(si_layer* const* layers, int L, si_stack** out) {
+    if (!out) return fail(SI_ERR_INVALID_ARG, "out is NULL");
+    *out = nullptr;
+    if (!layers) return fail(SI_ERR_INVALID_ARG, "NULL pointer");
+    if (L < 1 || L > si::kStackMaxLayers) return fail(SI_ERR_INVALID_ARG, "need 1 <= L <= 64");
+    for (int l = 0; l < L; ++l)
+        if (!layers[l]) return fail(SI_ERR_INVALID_ARG, "NULL layer handle");
+    const int d = layers[0]->d;
+    for (int l = 1; l < L; ++l)
+        if (layers[l]->d != d) return fail(SI_ERR_INVALID_ARG, "every layer of a stack must have the same d");
+    if (si::sparse_decode_stack_stages(d) < 8)
+        return fail(SI_ERR_UNSUPPORTED, "the decode stack supports d = 256, 512, 1024, 2048 or 3072");
+    si_stack* K = new si_stack();
+    SI_CK(cudaGetDevice(&K->device));
+    K->L = L;
+    K->d = d;
+    for (int l = 0; l < L; ++l) {
+        K->layers[l] = layers[l];
+        K->pos_off[l + 1] = K->pos_off[l] + layers[l]->n_loaded;
+    }
+    int rc;
+    if ((rc = dalloc(&K->pos, (size_t)K->pos_off[L], "stack plan copies")) ||
+        (rc = dalloc(&K->desc, (size_t)L, "stack layer table")) ||
+        (rc = dalloc(&K->delta, (size_t)L * si::kDeltaCopies * d, "stack layer sums")) ||
+        (rc = dalloc(&K->sync, (size_t)si::stack_sync_words(L), "stack barrier counters"))) {
+        destroy_stack(K);
+        return rc;
+    }
+    if (cudaMallocHost(reinterpret_cast<void**>(&K->desc_host), sizeof(si::StackLayerDesc) * L) != cudaSuccess) {
+        (void)cudaGetLastError();
+        K->desc_host = nullptr;
+        destroy_stack(K);
+        return fail(SI_ERR_OOM, "cudaMallocHost failed for the stack layer table");
+    }
+    cudaError_t e = cudaMemset(K->delta, 0, sizeof(float) * (size_t)L * si::kDeltaCopies * d);
+    if (e == cudaSuccess) e = cudaMemset(K->sync, 0, sizeof(unsigned) * (size_t)si::stack_sync_words(L));
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) {
+        destroy_stack(K);
+        return cuda_fail(e, "si_stack_create");
+    }
+    *out = K;
+    return SI_OK;
+}
+
+int si_stack_plan(si_stack* K, const int32_t* const* S, const int* n_sel, void* stream) {
+    if (!K || !S || !n_sel) return fail(SI_ERR_INVALID_ARG, "NULL pointer");
+    bool same = K->planned;
+    for (int l = 0; l < K->L; ++l) {
+        if (n_sel[l] < 0 || n_sel[l] > K->layers[l]->n_loaded)
+            return fail(SI_ERR_INVALID_ARG, "need 0 <= n_sel[l] <= n_loaded of layer l");
+        if (n_sel[l] > 0 && !S[l]) return fail(SI_ERR_INVALID_ARG, "NULL computed set");
+        same = same && K->desc_host[l].n == n_sel[l];
+    }
+    cudaStream_t st = (cudaStream_t)stream;
+    if (!same) {
+        // the layer table changes: it goes to the device by a stream-ordered copy
+        // from the pinned staging table, which an earlier copy may still read
+        if (capturing(st)) return fail(SI_ERR_INVALID_ARG, "the set sizes changed; plan once before capture");
+        SI_CK(cudaStreamSynchronize(st));
+        for (int l = 0; l < K->L; ++l) {
+            si::StackLayerDesc D;
+            D.packed = K->layers[l]->packed;
+            D.pos = K->pos + K->pos_off[l];
+            D.n = n_sel[l];
+            D.n_records = K->layers[l]->n_pad;
+            K->desc_host[l] = D;
+        }
+        SI_CK(cudaMemcpyAsync(K->desc, K->desc_host, sizeof(si::StackLayerDesc) * K->L, cudaMemcpyHostToDevice,
+                              st));
+    }
+    // the sets themselves: stream-ordered device copies (capturable)
+    for (int l = 0; l < K->L; ++l)
+        if (n_sel[l] > 0)
+            SI_CK(cudaMemcpyAsync(K->pos + K->pos_off[l], S[l], sizeof(int32_t) * (size_t)n_sel[l],
+                                  cudaMemcpyDeviceToDevice, st));
+    K->planned = true;
+    return SI_OK;
+}
+
+int si_sparse_ffn_decode_stack(si_stack* K, float* h, uint16_t* x_out, void* stream) {
+    if (!K || !h) return fail(SI_ERR_INVALID_ARG, "NULL pointer");
+    if (!K->planned) return fail(SI_ERR_INVALID_ARG, "call si_stack_plan before decoding");
+    if ((reinterpret_cast<uintptr_t>(h) & 15u) || (reinterpret_cast<uintptr_t>(x_out) & 15u))
+        return fail(SI_ERR_INVALID_ARG, "h and x_out must be 16-byte aligned");
+    unsigned* err = nullptr;
+    int rc = err_word(&err);
+    if (rc) return rc;
+    si::StackParams P = {};
+    P.layers = K->desc;
+    P.L = K->L;
+    P.d = K->d;
+    P.R = si::sparse_decode_stack_stages(K->d);
+    P.h = h;
+    P.x_out = x_out;
+    P.delta = K->delta;
+    P.sync = K->sync;
+    P.err = err;
+    SI_CK(si::launch_sparse_decode_stack(P, (cudaStream_t)stream));
+    return SI_OK;
+}
+
+int si_stack_destroy(si_stack* K) {
+    if (!K) return SI_OK;
+    cudaDeviceSynchronize();
+    destroy_stack(K);
     return SI_OK;
 }
 

@@ -29,64 +29,11 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "ring.cuh"
 
 namespace cg = cooperative_groups;
 
 namespace si {
-
-constexpr int kConsWarps = 8;
-constexpr int kConsThreads = kConsWarps * 32;
-constexpr int kDecThreads = kConsThreads + 32;
-
-__host__ __device__ constexpr int round_up(int x, int m) { return (x + m - 1) / m * m; }
-
-// Shared-memory layout of the streaming kernels (host and device agree).
-struct RingLayout {
-    int off_full, off_empty, off_aux, off_x, off_ring, stage, R, total;
-};
-
-__host__ __device__ inline RingLayout ring_layout(int R, int stage_bytes, int aux_bytes, int x_bytes) {
-    RingLayout L;
-    L.R = R;
-    L.stage = round_up(stage_bytes, 128);
-    L.off_full = 0;
-    L.off_empty = 8 * R;
-    L.off_aux = round_up(16 * R, 128);
-    L.off_x = L.off_aux + round_up(aux_bytes, 128);
-    L.off_ring = L.off_x + round_up(x_bytes, 128);
-    L.total = L.off_ring + R * L.stage;
-    return L;
-}
-
-// Producer loop of the ring kernels whose records are picked by an index
-// list (idx[0, cnt), each in [0, limit)): the warp loads the indices 32 at a
-// time, with the next block's load in flight while this block is issued, and
-// lane 0 issues record i into stage i % R once that stage's previous fill has
-// been released. An index out of range is flagged and replaced by 0. Called
-// by the whole producer warp.
-template <class IssueF>
-__device__ __forceinline__ void produce_by_index(const int32_t* __restrict__ idx, int cnt, int limit, int R,
-                                                 uint64_t* empty, unsigned* err, unsigned site, IssueF issue) {
-    const int lane = threadIdx.x & 31;
-    int pn = lane < cnt ? __ldcg(idx + lane) : 0;
-    for (int base = 0; base < cnt; base += 32) {
-        int p = pn;
-        pn = base + 32 + lane < cnt ? __ldcg(idx + base + 32 + lane) : 0;
-        const bool bad = base + lane < cnt && (p < 0 || p >= limit);
-        if (bad) p = 0;
-        if (__any_sync(0xFFFFFFFFu, bad) && lane == 0) atomicOr(err, SI_DEVERR_COUNT);
-        const int m = cnt - base < 32 ? cnt - base : 32;
-        for (int k = 0; k < m; ++k) {
-            const int pk = __shfl_sync(0xFFFFFFFFu, p, k);
-            if (lane == 0) {
-                const int i = base + k, s = i % R;
-                if (i >= R) mbar_wait(&empty[s], (uint32_t)((i / R - 1) & 1), err, site);
-                issue(i, s, pk);
-            }
-        }
-    }
-    __syncwarp();
-}
 
 // Cluster-level then grid-level reduction of the per-CTA partials ypart[BD]
 // (shared memory) into y[BD]. Must be called by every thread of every CTA.
@@ -431,25 +378,33 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_sparse_decode(SparseDecodePa
 }
 
 // Batch-1 decode with decoupled warps: neuron i belongs to warp i % 8 and ring
-// stage i % R (R a multiple of 8, so a warp always consumed the previous fill
-// of its own stages). Each warp computes a = silu(g.x) * (u.x) for its neuron
-// and accumulates a * down into its own register partial of y; there is no
+// stage i % R. Each warp computes a = silu(g.x) * (u.x) for its neuron and
+// accumulates a * down into its own register partial of y; there is no
 // CTA-wide barrier in the main loop, so a slow record stalls one warp only.
 // x is staged once per CTA in shared memory after the dependency wait; the
 // producer starts streaming as soon as the barriers exist.
+// R need not be a multiple of 8, so consecutive fills of a stage belong to
+// different warps and a parity wait alone could be answered by a fill two
+// phases old: the producer writes the record number into the stage's slot
+// before issuing its copy (only possible once the previous fill was released)
+// and a consumer waits for its number to appear before the parity wait.
+constexpr int kB1MaxStages = 32;  // stages of the batch-1 ring (their record numbers sit in the aux area)
+
 template <int MAXC>
 __global__ void __launch_bounds__(kDecThreads, 1) k_sparse_decode_b1(SparseDecodeParams P) {
     extern __shared__ __align__(1024) uint8_t smem[];
     const int d = P.d;
     // x is staged once per CTA in shared memory (one L2 read of x per CTA
     // rather than one per warp)
-    const RingLayout L = ring_layout(P.R, 6 * d, 0, 2 * d);
+    const RingLayout L = ring_layout(P.R, 6 * d, 4 * kB1MaxStages, 2 * d);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.off_full);
     uint64_t* empty = reinterpret_cast<uint64_t*>(smem + L.off_empty);
+    int* seq = reinterpret_cast<int*>(smem + L.off_aux);  // record number of each stage's latest fill
     const uint4* s_x = reinterpret_cast<const uint4*>(smem + L.off_x);
     uint8_t* ring = smem + L.off_ring;
     const int R = L.R;
-    if (R < 1) {  // the host never launches without stages; refuse rather than divide by zero
+    // the host never launches a ring shorter than the eight warp partials need
+    if (R < kConsWarps || R > kB1MaxStages) {
         if (threadIdx.x == 0) atomicOr(P.err, SI_DEVERR_COUNT);
         return;
     }
@@ -464,6 +419,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_sparse_decode_b1(SparseDecod
     constexpr int XJ = 8 * MAXC;  // 16-byte chunks of a row per lane (c = lane + 32 j)
     const int nch = d / 8;
 
+    for (int s = threadIdx.x; s < R; s += blockDim.x) seq[s] = -1;
     if (threadIdx.x == 0) {
         for (int s = 0; s < R; ++s) {
             mbar_init(&full[s], 1);
@@ -491,7 +447,8 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_sparse_decode_b1(SparseDecod
         }
         const uint64_t pol = policy_evict_first();
         produce_by_index(P.pos + lo, cnt, P.n_records, R, empty, P.err, kSiteDecode | kSiteEmpty,
-                         [&](int, int s, int p) {
+                         [&](int i, int s, int p) {
+                             *reinterpret_cast<volatile int*>(seq + s) = i;
                              mbar_arrive_expect_tx(&full[s], rec_bytes);
                              bulk_g2s_hint(ring + (size_t)s * L.stage, P.packed + (size_t)p * 3 * d, rec_bytes,
                                            &full[s], pol);
@@ -509,6 +466,15 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_sparse_decode_b1(SparseDecod
             for (int e = 0; e < 8; ++e) acc[j][e] = 0.0f;
         for (int i = warp; i < cnt; i += kConsWarps) {
             const int s = i % R;
+            if (*reinterpret_cast<volatile int*>(seq + s) != i) {
+                const long long t0 = cycles();
+                while (*reinterpret_cast<volatile int*>(seq + s) != i) {
+                    if (cycles() - t0 > kWaitLimitCycles) {
+                        if (lane == 0) atomicOr(P.err, SI_DEVERR_WAIT_TIMEOUT | kSiteDecode | kSiteFull);
+                        break;
+                    }
+                }
+            }
             mbar_wait(&full[s], (uint32_t)((i / R) & 1), P.err, kSiteDecode | kSiteFull);
             const uint4* st = reinterpret_cast<const uint4*>(ring + (size_t)s * L.stage);
             float ga[4] = {0.f, 0.f, 0.f, 0.f}, ua[4] = {0.f, 0.f, 0.f, 0.f};
@@ -537,10 +503,12 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_sparse_decode_b1(SparseDecod
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[s]);
         }
-        // Warp partial -> the warp's own first ring stage (free: the warp has
-        // consumed every record of its stages), no barrier needed before it.
-        // Layout per warp: for chunk j, the lanes' first halves (4 floats each)
-        // then their second halves, so the stores are bank-conflict free.
+        // Warp partial -> ring stage `warp`, once every warp has consumed all
+        // of its records (the producer has issued its last record by then, so
+        // no stage is refilled). Layout per warp: for chunk j, the lanes'
+        // first halves (4 floats each) then their second halves, so the
+        // stores are bank-conflict free.
+        named_bar_sync(1, kConsThreads);
         float4* wst = reinterpret_cast<float4*>(ring + (size_t)warp * L.stage);
 #pragma unroll
         for (int j = 0; j < XJ; ++j) {
@@ -1569,7 +1537,7 @@ cudaError_t launch_sd1(SparseDecodeParams& P, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
     if ((e = allow_max_smem(kern)) != cudaSuccess) return e;
-    const size_t smem = (size_t)ring_layout(P.R, 6 * P.d, 0, 2 * P.d).total;
+    const size_t smem = (size_t)ring_layout(P.R, 6 * P.d, 4 * kB1MaxStages, 2 * P.d).total;
     void* args[] = {&P};
     return launch_clustered(kern, sms > 2 * kSpareSms ? sms - kSpareSms : sms, 1, smem, st, args, /*pdl=*/true);
 }
@@ -1594,9 +1562,8 @@ int decode_max_partial_floats(int d, int B) {
 
 int sparse_decode_b1_stages(int d) {
     const int stage = round_up(6 * d, 128);
-    int R = (kSmemBudget - 512 - round_up(2 * d, 128)) / stage;
-    if (R > 32) R = 32;
-    R = (R / kConsWarps) * kConsWarps;
+    int R = (kSmemBudget - ring_layout(kB1MaxStages, 0, 4 * kB1MaxStages, 2 * d).total) / stage;
+    if (R > kB1MaxStages) R = kB1MaxStages;
     // warp w's partial (blocks of 32 chunks: round_up(d, 256) floats) reuses
     // its stage w, then the CTA partial stage 0
     return (R >= kConsWarps && stage >= round_up(d, 256) * 4) ? R : 0;

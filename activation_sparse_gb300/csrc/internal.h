@@ -101,6 +101,44 @@ cudaError_t launch_spax_encode(const uint16_t* Wd, int d, int N, int bits, int g
 // api.cu: sets the message si_last_error_string() returns on this thread
 void set_error_message(const char* msg);
 
+// One layer of a decode stack: the packed records of a handle and the copy of
+// its computed set that si_stack_plan made.
+struct StackLayerDesc {
+    const uint16_t* packed;   // [n_records][3][d] bf16
+    const int32_t* pos;       // n ascending packed positions
+    int n;
+    int n_records;
+};
+
+constexpr int kStackMaxLayers = 64;
+// Layer sums: kDeltaCopies copies of [d] per layer (CTA b adds into copy
+// b % kDeltaCopies). Grid barrier of layer l: kBarLines counters, each in its
+// own 128-byte line (kLineWords words); then the exit ticket and the launch's
+// error word, each in its own line.
+constexpr int kDeltaCopies = 4;
+constexpr int kBarLines = 16;
+constexpr int kLineWords = 32;
+__host__ __device__ inline int stack_bar_word(int l, int k) { return (l * kBarLines + k) * kLineWords; }
+__host__ __device__ inline int stack_ticket_word(int L) { return L * kBarLines * kLineWords; }
+__host__ __device__ inline int stack_lerr_word(int L) { return (L * kBarLines + 1) * kLineWords; }
+__host__ __device__ inline int stack_sync_words(int L) { return (L * kBarLines + 2) * kLineWords; }
+
+struct StackParams {
+    const StackLayerDesc* layers;  // [L], device
+    int L, d, R;
+    float* h;                 // [d] residual stream: read at entry, written at exit
+    uint16_t* x_out;          // optional [L][d]: the bf16 input each layer used
+    float* delta;             // [L][kDeltaCopies][d] per-layer output sums, zero on entry (the kernel
+                              // re-zeroes them)
+    unsigned* sync;           // [stack_sync_words(L)] barrier counters, exit ticket, the launch's error
+                              // word; zero on entry (the kernel re-zeroes them)
+    unsigned* err;            // device error word (the launch's failures are moved here at exit)
+};
+
+// stack.cu
+int sparse_decode_stack_stages(int d);
+cudaError_t launch_sparse_decode_stack(const StackParams& P, cudaStream_t st);
+
 // noalloc.cu: device address of the no-allocation entry point's reported
 // error word on the current device (looked up once per device; allocates nothing)
 int noalloc_error_word(unsigned** out);

@@ -107,8 +107,9 @@ int si_sparse_layers(int L, int first, int last, uint8_t *sparse, int *n_sparse)
 #define SI_DEVERR_RANGE 4u          /* a decode partial exceeded the fixed-point accumulator's range (|y| >= 2^23) */
 /* With SI_DEVERR_WAIT_TIMEOUT, bits 8-15 name the kernel whose wait ran out
  * (1 sparse decode, 2 dense activation pass, 3 tiered down-projection,
- * 4 activation GEMM) and bits 16-19 the barrier (1 stage full, 2 stage empty,
- * 3 stage full in the down-projection phase, 4 accumulator ready). */
+ * 4 activation GEMM, 5 decode stack) and bits 16-19 the barrier (1 stage
+ * full, 2 stage empty, 3 stage full in the down-projection phase,
+ * 4 accumulator ready, 5 grid barrier between layers). */
 int si_device_error(uint32_t *code, int clear);
 
 /* --------------------------------------------------- a1: profiler score */
@@ -309,6 +310,46 @@ int si_sparse_ffn_decode_residual(si_layer *layer, const int32_t *S, int n_sel, 
  * later calls are unaffected (their waits watch only their own launch). */
 int si_sparse_ffn_decode_noalloc(const uint16_t *packed, int n_records, int d, const int32_t *S,
                                  int n_sel, const uint16_t *x, float *y, void *stream);
+
+/* Decode stack: one launch per decode token over L sparse FFN layers.
+ * [SI] section 5 computes, at every decode step, each layer's FFN on that
+ * layer's selected neurons only, the layers one after another. In the pages'
+ * models (Llama, Qwen) a layer's FFN reads the RMS-normalised residual stream
+ * and adds its output back to it; for a stack of FFN layers (unit norm gain):
+ *     for l = 0 .. L-1:  x_l = bf16(h / sqrt(mean(h^2) + 1e-5));
+ *                        h += sum over p in S_l of a_p(x_l) * down_p
+ * (h in fp32, the mean over the d elements, round to nearest even; a_p and
+ * down_p as in si_sparse_ffn_decode). The
+ * whole token is one cooperative grid, one CTA per SM: the selected records
+ * of layer l+1 stream into the ring while layer l's partial sums are added
+ * up across the grid, so the weight stream does not stop at layer
+ * boundaries. The sum over a layer's CTAs uses float atomics: repeated calls
+ * can differ in the last bits (as si_sparse_ffn_decode_residual).
+ *
+ * si_stack_create: layers (host array of L handles, 1 <= L <= 64, all of the
+ *   same d, d in {256, 512, 1024, 2048, 3072}, else SI_ERR_UNSUPPORTED) are borrowed, not owned: they must
+ *   outlive the stack. Allocates (synchronous; not during capture).
+ * si_stack_plan: the computed sets, S (host array of L device pointers, each
+ *   int32 [n_sel[l]] ascending packed positions of layer l, as the selection
+ *   calls write them) and n_sel (host, L counts, 0 <= n_sel[l] <= n_loaded),
+ *   are copied into the stack by stream-ordered device copies; the caller may
+ *   reuse S afterwards. When the counts differ from the previous plan's, the
+ *   call first synchronises the stream and uploads the stack's layer table
+ *   (then it must not run during capture); with the same counts it only
+ *   enqueues the copies and may be captured.
+ * si_sparse_ffn_decode_stack: h fp32 [d] (16-byte aligned) holds the residual
+ *   stream; it is read at the start and receives h after layer L-1. x_out
+ *   (optional, may be NULL; 16-byte aligned) bf16 [L][d] receives each layer's
+ *   input x_l. Needs a plan; calls of one stack go on one stream (they share
+ *   its scratch). An index outside a layer's records sets SI_DEVERR_COUNT and
+ *   reads record 0; a grid barrier that runs out sets SI_DEVERR_WAIT_TIMEOUT
+ *   with kernel id 5 and barrier kind 5 (see si_device_error).
+ * si_stack_destroy frees the stack (synchronises the device first). */
+typedef struct si_stack si_stack;
+int si_stack_create(si_layer *const *layers, int L, si_stack **out);
+int si_stack_plan(si_stack *stack, const int32_t *const *S, const int *n_sel, void *stream);
+int si_sparse_ffn_decode_stack(si_stack *stack, float *h, uint16_t *x_out, void *stream);
+int si_stack_destroy(si_stack *stack);
 
 /* ------------------------------------------------------------- SpAx */
 

@@ -74,6 +74,7 @@ def _declare(L):
     L.oracle_spax_tiers.argtypes = [_f32p, i, i, i, _i32p, _i32p]
     L.oracle_spax_tiers.restype = i
     L.oracle_spax_down.argtypes = [_f32p, i, i, _u16p, _u8p, _f32p, i, i, _i32p, i, _i32p, i, _f64p]
+    L.oracle_bf16_round_array.argtypes = [_f32p, i, _u16p]
 
 
 def _c(a, dt):
@@ -201,6 +202,44 @@ def sparse_ffn(Wg, Wu, Wd, loaded, S, x):
     y = np.zeros(d, np.float64)
     lib().oracle_sparse_ffn(Wg, Wu, Wd, d, N, loaded, S, S.shape[0], x, y)
     return y
+
+
+def bf16_round(f):
+    """bf16 bit patterns (uint16) of float32 values, round to nearest even."""
+    f = _c(np.asarray(f, dtype=np.float32).ravel(), np.float32)
+    out = np.zeros(f.shape[0], np.uint16)
+    lib().oracle_bf16_round_array(f, f.shape[0], out)
+    return out
+
+
+NORM_EPS = 1e-5  # RMS norm epsilon of a stack layer's input (Llama 3.2's value)
+
+
+def rms_norm_bf16(h):
+    """bf16 bits of h / sqrt(mean(h^2) + eps): computed in float64, rounded to
+    float32, then to bf16 (round to nearest even)."""
+    hh = np.asarray(h, dtype=np.float64)
+    r = 1.0 / np.sqrt(np.mean(hh * hh) + NORM_EPS)
+    return bf16_round((hh * r).astype(np.float32))
+
+
+def sparse_ffn_stack(h, layers):
+    """One decode token through a stack of sparse FFN layers on one residual
+    stream. SelectInfer section 5 computes each layer's FFN on its selected
+    neurons, the layers in order; in the pages' models (Llama, Qwen) each FFN
+    reads the RMS-normalised residual stream and adds its output back to it
+    (unit norm gain here):
+        for each layer l:  x_l = bf16(h / sqrt(mean(h^2) + eps));  h = h + FFN_l(x_l)
+    h: float [d] (kept in float64 here); layers: list of (Wg, Wu, Wd, loaded,
+    S) with S the layer's selected packed positions. Returns (h after the
+    last layer, float64 [d]; the inputs x_l, uint16 [L][d] bf16 bits)."""
+    hh = np.array(h, dtype=np.float64)
+    xs = []
+    for Wg, Wu, Wd, loaded, S in layers:
+        x = rms_norm_bf16(hh)
+        xs.append(x)
+        hh = hh + sparse_ffn(Wg, Wu, Wd, loaded, S, x)
+    return hh, np.stack(xs) if xs else np.zeros((0, hh.shape[0]), np.uint16)
 
 
 def dense_act(Wg, Wu, x):

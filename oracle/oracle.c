@@ -36,6 +36,10 @@
  *   oracle_spax_down       dense numpy product when top = 100% / mid = 100%
  *   oracle_swiglu          closed-form silu values; with spax_down, the dense
  *                          activations when every input channel is top tier
+ *   oracle_bf16_round      the definition's properties on every kind of
+ *                          input (exact values, ties both ways, halfway
+ *                          carries into the exponent, signs, inf) and the
+ *                          nearest-value property on random floats
  */
 #include <math.h>
 #include <stdint.h>
@@ -366,6 +370,35 @@ void oracle_sparse_ffn(const uint16_t *Wg, const uint16_t *Wu, const uint16_t *W
         y[j] = acc;
     }
     free(a);
+}
+
+/* ------------------------------------------------- a7 decode stack input */
+
+/* bf16 value of a float32, rounded to nearest with ties to even: the input a
+ * layer of an FFN-only stack reads from the fp32 residual stream (the decode
+ * steps of SelectInfer section 5 run the layers one after another; with no
+ * attention or norm between the FFNs, layer l+1 reads h + FFN_l(x_l)).
+ * Written from the definition: of the two bf16 values around f (f with its low
+ * 16 bits cleared, and that plus one bf16 step away from zero), the nearer
+ * one; on an exact tie, the one whose last kept bit is 0. Inf stays inf; NaN
+ * stays a NaN. */
+uint16_t oracle_bf16_round(float f)
+{
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    if ((u & 0x7F800000u) == 0x7F800000u) {           /* inf or NaN */
+        if (u & 0x007FFFFFu) return (uint16_t)((u >> 16) | 0x0040u);
+        return (uint16_t)(u >> 16);
+    }
+    uint32_t lower = u >> 16;                          /* truncated toward zero */
+    uint32_t rest = u & 0xFFFFu;                       /* the dropped bits */
+    if (rest > 0x8000u || (rest == 0x8000u && (lower & 1u))) lower += 1u;
+    return (uint16_t)lower;
+}
+
+void oracle_bf16_round_array(const float *f, int n, uint16_t *out)
+{
+    for (int i = 0; i < n; ++i) out[i] = oracle_bf16_round(f[i]);
 }
 
 /* a_n(x) for every neuron of a layer (dense gate/up pass that the SpAx

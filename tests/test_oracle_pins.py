@@ -455,3 +455,144 @@ def test_spax_gate_up_special_cases():
     a8, _, _ = oracle.spax_gate_up(x, Wg, Wu, 0.0, 1.0, bits=8)
     ref = oracle.dense_act(Wg, Wu, x)
     assert np.abs(a8 - ref).max() <= 0.05 * np.abs(ref).max()
+
+
+# --------------------------------------------------------- bf16 rounding
+
+
+def _bf16_of(bits16):
+    return float((np.asarray([bits16], np.uint32) << 16).view(np.float32)[0])
+
+
+def test_bf16_round_fixed_cases():
+    one = 0x3F800000
+    f = lambda u: np.asarray([u], np.uint32).view(np.float32)[0]
+    cases = [
+        (one, 0x3F80),                 # exact
+        (one + 0x8000, 0x3F80),        # 1 + 2^-8: a tie, the kept bit is 0 -> stays
+        (one + 0x18000, 0x3F82),       # 1 + 3 * 2^-8: a tie, the kept bit is 1 -> up
+        (one + 0x8001, 0x3F81),        # just above the tie -> up
+        (one + 0x7FFF, 0x3F80),        # just below the tie -> down
+        (0x3FFF8000, 0x4000),          # a tie that carries into the exponent (-> 2.0)
+        (0xBF808000, 0xBF80),          # negative tie to even
+        (0xBF818000, 0xBF82),          # negative tie, odd -> away from zero
+        (0x7F800000, 0x7F80),          # inf
+        (0xFF800000, 0xFF80),          # -inf
+        (0x00000001, 0x0000),          # the smallest subnormal -> +0
+        (0x00018000, 0x0002),          # subnormal tie, odd -> up
+    ]
+    for u, want in cases:
+        got = int(oracle.bf16_round(np.array([f(u)], np.float32))[0])
+        assert got == want, (hex(u), hex(got), hex(want))
+    nan = oracle.bf16_round(np.array([np.nan], np.float32))[0]
+    assert math.isnan(_bf16_of(nan))
+
+
+def test_bf16_round_is_the_nearest_bf16():
+    # every finite float32 rounds to the nearer of the two bf16 values around
+    # it (distances in float64), an exact tie to the one with an even last bit
+    rng = np.random.default_rng(5)
+    bits = rng.integers(0, 2 ** 32, size=20000, dtype=np.uint64).astype(np.uint32)
+    bits = bits[(bits & 0x7F800000) != 0x7F800000]
+    f = bits.view(np.float32)
+    got = oracle.bf16_round(f).astype(np.uint32)
+    lo = bits >> 16
+    hi = lo + 1
+    vf = f.astype(np.float64)
+    vlo = (lo << 16).view(np.float32).astype(np.float64)
+    vhi = (hi << 16).view(np.float32).astype(np.float64)
+    dlo, dhi = np.abs(vf - vlo), np.abs(vhi - vf)
+    want = np.where(dlo < dhi, lo, np.where(dhi < dlo, hi, np.where(lo % 2 == 0, lo, hi)))
+    # a value above the largest finite bf16 that is nearer to it stays finite;
+    # one at or past the midpoint to 2^128 rounds to inf (hi = 0x7F80 there)
+    assert np.array_equal(got, want)
+
+
+# -------------------------------------------------------- decode stack
+
+
+def _tiny_layer():
+    one = int(synth.to_bf16_bits(np.array([1.0], np.float32))[0])
+    Wg = np.array([[one, 0]], np.uint16)      # g = x0
+    Wu = np.array([[0, one]], np.uint16)      # u = x1
+    Wd = np.array([[one], [0]], np.uint16)    # the output goes to h0 only
+    return Wg, Wu, Wd, np.array([0], np.int32), np.array([0], np.int32)
+
+
+def _silu(z):
+    return z * (1.0 + math.tanh(z / 2.0)) / 2.0     # z * sigmoid(z) by the tanh identity
+
+
+def test_sparse_ffn_stack_two_layers_closed_form():
+    # d = 2, one neuron: g = x0, u = x1, the output goes to h0 only.
+    # Each layer reads x = bf16(float32(h / sqrt(mean(h^2) + 1e-5))).
+    lay = _tiny_layer()
+    h, xs = oracle.sparse_ffn_stack(np.array([2.0, 1.0]), [lay, lay])
+    h0 = [2.0, 1.0]
+    want_x = []
+    for _ in range(2):
+        r = 1.0 / math.sqrt((h0[0] ** 2 + h0[1] ** 2) / 2.0 + 1e-5)
+        xb = synth.to_bf16_bits(np.array([h0[0] * r, h0[1] * r]))
+        want_x.append([int(v) for v in xb])
+        xf = synth.bf16_bits_to_f32(xb).astype(np.float64)
+        h0 = [h0[0] + _silu(xf[0]) * xf[1], h0[1]]
+    assert [[int(v) for v in row] for row in xs] == want_x
+    # the first input by hand: r = 1/sqrt(2.50001) = 0.632454..., 2r = 1.264908
+    # lies between the bf16 values 1.265625 (0x3FA2) and 1.2578125 (0x3FA1),
+    # nearer the first; r lies between 0.6328125 (0x3F22) and 0.62890625
+    # (0x3F21), nearer the first
+    assert want_x[0] == [0x3FA2, 0x3F22]
+    assert abs(h[0] - h0[0]) <= 1e-12 and h[1] == 1.0
+    # an oracle that skipped the bf16 rounding of the second layer's input
+    # (or its normalisation) would land measurably elsewhere
+    x1 = synth.bf16_bits_to_f32(np.array(want_x[0], np.uint16)).astype(np.float64)
+    h1 = 2.0 + _silu(x1[0]) * x1[1]
+    r1 = 1.0 / math.sqrt((h1 ** 2 + 1.0) / 2.0 + 1e-5)
+    assert abs(h1 + _silu(h1 * r1) * r1 - h[0]) > 1e-4
+    assert abs(h1 + _silu(h1) * 1.0 - h[0]) > 1e-2
+
+
+def test_sparse_ffn_stack_reduces_to_one_layer_and_composes():
+    d, N = 96, 160
+    rng_layers = []
+    for l in range(3):
+        Wg, Wu, Wd = synth.layer_weights(70, l, d, N)
+        s = synth.lognormal_absact(70 + l, 1, N)[0]
+        loaded, st = oracle.rank_loaded(s, s, 0.8, 0.2)
+        S = oracle.select(synth.lognormal_absact(80 + l, 8, len(loaded)), 8, 1, len(loaded), st, 16,
+                          oracle.cnt(0.5, N))[0]
+        rng_layers.append((Wg, Wu, Wd, loaded, S))
+    h0 = synth.normal(71, 0, 0, d)
+    # one layer: h + FFN(bf16(h / rms(h)))
+    h1, xs = oracle.sparse_ffn_stack(h0, rng_layers[:1])
+    x0 = synth.to_bf16_bits(h0 / np.sqrt(np.mean(h0 ** 2) + 1e-5))
+    assert np.array_equal(xs[0], x0)
+    Wg, Wu, Wd, loaded, S = rng_layers[0]
+    assert np.allclose(h1, h0 + oracle.sparse_ffn(Wg, Wu, Wd, loaded, S, x0), rtol=0, atol=1e-12)
+    # three layers = one, then the other two on its output
+    h3, xs3 = oracle.sparse_ffn_stack(h0, rng_layers)
+    h3b, xs3b = oracle.sparse_ffn_stack(h1, rng_layers[1:])
+    assert np.array_equal(h3, h3b) and np.array_equal(xs3[1:], xs3b)
+    # the layers do not commute (each reads the stream the previous one wrote)
+    h3r, _ = oracle.sparse_ffn_stack(h0, rng_layers[::-1])
+    assert np.max(np.abs(h3r - h3)) > 1e-6
+
+
+def test_sparse_ffn_stack_empty_sets_leave_h():
+    d, N = 64, 80
+    Wg, Wu, Wd = synth.layer_weights(72, 0, d, N)
+    loaded = np.arange(N, dtype=np.int32)
+    h0 = synth.normal(73, 0, 0, d)
+    h, xs = oracle.sparse_ffn_stack(h0, [(Wg, Wu, Wd, loaded, np.zeros(0, np.int32))] * 4)
+    assert np.array_equal(h, h0)
+    x0 = synth.to_bf16_bits(h0 / np.sqrt(np.mean(h0 ** 2) + 1e-5))
+    assert all(np.array_equal(x, x0) for x in xs)
+
+
+def test_rms_norm_input_scale_invariance():
+    # the layer input does not change when h is scaled by a power of two
+    # (the 1e-5 epsilon aside, which a large stream makes negligible)
+    h = synth.normal(74, 0, 0, 512) * 100.0
+    assert np.array_equal(oracle.rms_norm_bf16(h), oracle.rms_norm_bf16(h * 4.0))
+    x = synth.bf16_bits_to_f32(oracle.rms_norm_bf16(h)).astype(np.float64)
+    assert abs(np.sqrt(np.mean(x ** 2)) - 1.0) < 4e-3   # unit RMS up to bf16 rounding
