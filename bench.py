@@ -161,10 +161,10 @@ class ClockSampler:
 
 
 def kernel_source_hash():
-    """Hash of the decode kernels' sources; a DRAM-traffic figure taken with
-    other sources is not reported."""
+    """Hash of the sources of the batch-1 decode kernel and the dense pass;
+    a DRAM-traffic figure taken with other sources is not reported."""
     h = hashlib.sha256()
-    for f in ("decode.cu", "ring.cuh", "common.cuh", "stack.cu"):
+    for f in ("decode.cu", "ring.cuh", "common.cuh"):
         with open(os.path.join(ROOT, "activation_sparse_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
