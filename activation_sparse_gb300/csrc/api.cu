@@ -626,9 +626,12 @@ int spax_encode(const uint16_t* Wd, int d, int N, int bits, int group, spax_laye
     if (!out) return fail(SI_ERR_INVALID_ARG, "out is NULL");
     *out = nullptr;
     if (!Wd) return fail(SI_ERR_INVALID_ARG, "NULL pointer");
-    if (bits != 2 && bits != 4 && bits != 8) return fail(SI_ERR_UNSUPPORTED, "codes are 2, 4 or 8 bits wide");
+    if (bits != 2 && bits != 3 && bits != 4 && bits != 8)
+        return fail(SI_ERR_UNSUPPORTED, "codes are 2, 3, 4 or 8 bits wide");
     if (group < 8 || (group & (group - 1)) || d < 64 || d % 64 || d % group)
         return fail(SI_ERR_INVALID_ARG, "need group a power of two >= 8, d % 64 == 0, d % group == 0");
+    if (bits == 3 && d % 128)
+        return fail(SI_ERR_INVALID_ARG, "3-bit codes need d % 128 == 0 (records of whole 16-byte units)");
     if (d > 4096) return fail(SI_ERR_UNSUPPORTED, "tiered decode supports d <= 4096");
     if (N < 1 || N > 32768) return fail(SI_ERR_INVALID_ARG, "need 1 <= N <= 32768");
     cudaStream_t st = (cudaStream_t)stream;

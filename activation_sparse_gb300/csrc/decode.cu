@@ -10,8 +10,8 @@
 //                      sequences that selected it).
 //  k_dense_act         SpAx dense gate/up pass: a[n] for every neuron.
 //  k_tiered_down       SpAx three-tier down-projection (abstract, Fig. 2/3):
-//                      top columns in bf16, middle columns rebuilt from 2-, 4-
-//                      or 8-bit codes (min + q * scale), the rest never read.
+//                      top columns in bf16, middle columns rebuilt from 2-, 3-,
+//                      4- or 8-bit codes (min + q * scale), the rest never read.
 //
 // Common structure (warp-specialised, one CTA per SM):
 //   * the producer warp streams whole records into a ring of shared-memory
@@ -23,8 +23,8 @@
 //   * cross-CTA sum of y: 64-bit fixed-point atomics with a ticketed final
 //     conversion (batch-1 overwrite; deterministic), float atomics into y
 //     (batch-1 residual form), or cluster reduction through distributed
-//     shared memory plus a ticketed fixed-order final pass (batch B and
-//     tiered down; deterministic).
+//     shared memory plus a ticketed fixed-order final pass over float4
+//     columns (batch B and tiered down; deterministic).
 #include <cooperative_groups.h>
 
 #include "common.cuh"
@@ -34,53 +34,6 @@
 namespace cg = cooperative_groups;
 
 namespace si {
-
-// Cluster-level then grid-level reduction of the per-CTA partials ypart[BD]
-// (shared memory) into y[BD]. Must be called by every thread of every CTA.
-__device__ void cluster_ticket_reduce(float* ypart, int BD, float* __restrict__ part, unsigned* tickets,
-                                      float* __restrict__ y) {
-    __shared__ unsigned s_last;
-    cg::cluster_group cl = cg::this_cluster();
-    const unsigned C = cl.num_blocks();
-    const unsigned r = cl.block_rank();
-    const unsigned ncl = gridDim.x / C;
-    const unsigned cid = blockIdx.x / C;
-    cl.sync();
-    const int per = (BD + (int)C - 1) / (int)C;
-    const int s0 = (int)r * per;
-    const int s1 = min(BD, s0 + per);
-    for (int idx = s0 + (int)threadIdx.x; idx < s1; idx += blockDim.x) {
-        float v = 0.0f;
-        for (unsigned c = 0; c < C; ++c) v += cl.map_shared_rank(ypart, c)[idx];
-        __stcg(part + (size_t)cid * BD + idx, v);
-    }
-    __threadfence();
-    cl.sync();  // no CTA leaves while a peer still reads its shared memory
-    if (threadIdx.x == 0) {
-        __threadfence();
-        const unsigned t = atomicAdd(tickets + r, 1u);
-        s_last = (t == ncl - 1) ? 1u : 0u;
-    }
-    __syncthreads();
-    if (s_last) {
-        __threadfence();
-        for (int idx = s0 + (int)threadIdx.x; idx < s1; idx += blockDim.x) {
-            // eight loads in flight, summed in cluster order (deterministic)
-            float v = 0.0f;
-            unsigned k = 0;
-            for (; k + 8 <= ncl; k += 8) {
-                float t[8];
-#pragma unroll
-                for (int q = 0; q < 8; ++q) t[q] = __ldcg(part + (size_t)(k + q) * BD + idx);
-#pragma unroll
-                for (int q = 0; q < 8; ++q) v += t[q];
-            }
-            for (; k < ncl; ++k) v += __ldcg(part + (size_t)k * BD + idx);
-            y[idx] = v;
-        }
-        if (threadIdx.x == 0) tickets[r] = 0u;
-    }
-}
 
 // Cluster arrive / wait halves (all threads of every CTA in the cluster).
 __device__ __forceinline__ void cluster_arrive() {
@@ -374,7 +327,9 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_sparse_decode(SparseDecodePa
         }
     }
     __syncthreads();
-    cluster_ticket_reduce(reinterpret_cast<float*>(ring), B * d, P.part, P.tickets, P.y);
+    // float4 columns, each summed over the clusters by one thread of the last
+    // cluster (fixed cluster order: deterministic)
+    cluster_ticket_reduce4(reinterpret_cast<float*>(ring), B * d, P.part, P.tickets, P.y);
 }
 
 // Batch-1 decode with decoupled warps: neuron i belongs to warp i % 8 and ring
@@ -1329,6 +1284,12 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_tiered_down(TieredDownParams
                             mac(acc[j][5], __byte_perm(q.y, 0x4B000000u, 0x7441));
                             mac(acc[j][6], __byte_perm(q.y, 0x4B000000u, 0x7442));
                             mac(acc[j][7], __byte_perm(q.y, 0x4B000000u, 0x7443));
+                        } else if constexpr (BITS == 3) {
+                            // 24 bits per chunk, in bytes 3c .. 3c + 2; element e at bits 3e .. 3e + 2
+                            const uint8_t* b3 = st + 3 * c;
+                            const uint32_t q = (uint32_t)b3[0] | ((uint32_t)b3[1] << 8) | ((uint32_t)b3[2] << 16);
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) mac(acc[j][e], 0x4B000000u | ((q >> (3 * e)) & 7u));
                         } else {
                             // BITS == 2: sixteen bits per chunk, element e at bits 2e, 2e + 1
                             const uint32_t q = reinterpret_cast<const uint16_t*>(st)[c];
@@ -1520,6 +1481,7 @@ cudaError_t launch_sd(SparseDecodeParams& P, cudaStream_t st, int* grid_out) {
     if (e != cudaSuccess) return e;
     if (grid_out) *grid_out = grid;
     if (P.part_floats < (long long)(grid / cluster) * B * P.d) return cudaErrorInvalidValue;
+    if ((B * P.d) % (4 * cluster)) return cudaErrorInvalidValue;  // float4 slices per cluster rank
     void* args[] = {&P};
     return launch_clustered(kern, grid, cluster, smem, st, args);
 }
@@ -1548,7 +1510,9 @@ cudaError_t launch_sd1(SparseDecodeParams& P, cudaStream_t st) {
 int sparse_decode_stages(int d, int B) {
     const int fixed = ring_layout(0, 6 * d, 2 * kConsWarps * B * 4, B * d * 2).total;
     const int stage = round_up(6 * d, 128);
-    int R = (kSmemBudget - fixed - 256) / stage;
+    // the cluster reduction's static shared memory (a float4 per thread) comes
+    // out of the same 227 KB
+    int R = (kSmemBudget - (int)sizeof(float4) * kDecThreads - fixed - 256) / stage;
     if (R > 32) R = 32;
     return R;
 }
@@ -1668,6 +1632,7 @@ cudaError_t launch_tiered_down(TieredDownParams P, cudaStream_t st) {
     const bool wide = P.d > 2048;
     switch (P.bits) {
         case 2: return wide ? launch_tiered<2, 2>(P, smem, st) : launch_tiered<1, 2>(P, smem, st);
+        case 3: return wide ? launch_tiered<2, 3>(P, smem, st) : launch_tiered<1, 3>(P, smem, st);
         case 4: return wide ? launch_tiered<2, 4>(P, smem, st) : launch_tiered<1, 4>(P, smem, st);
         case 8: return wide ? launch_tiered<2, 8>(P, smem, st) : launch_tiered<1, 8>(P, smem, st);
         default: return cudaErrorInvalidValue;

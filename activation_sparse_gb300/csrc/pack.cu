@@ -9,8 +9,8 @@
 //  k_down_norms    ||Wd[:, n]||_2 per packed neuron, for the weight-aware
 //                  salience |a_n| * ||Wd[:, n]||_2 (WiSparse abstract).
 //  k_spax_encode   SpAx offline encoding (Fig. 2, Fig. 3): per column and
-//                  per row group, float32 min / max / scale and 2-, 4- or
-//                  8-bit codes, plus a column-major bf16 copy of Wd so that a top-tier
+//                  per row group, float32 min / max / scale and 2-, 3-, 4-
+//                  or 8-bit codes, plus a column-major bf16 copy of Wd so that a top-tier
 //                  column is one contiguous read. A column's codes and its
 //                  (scale, min) pairs form one record, so a middle-tier
 //                  column is one contiguous read too.
@@ -62,7 +62,9 @@ template <int BITS>
 __global__ void __launch_bounds__(256) k_spax_encode(const uint16_t* __restrict__ Wd, int d, int N, int group,
                                                     int ngp, uint16_t* __restrict__ WdT,
                                                     uint8_t* __restrict__ recs, int rec_bytes) {
-    constexpr int EPB = 8 / BITS;            // codes per byte
+    // codes per store unit: one byte (2-, 4-, 8-bit codes) or, for 3-bit
+    // codes, eight codes in three bytes (a code may straddle two bytes)
+    constexpr int EPU = BITS == 3 ? 8 : 8 / BITS;
     constexpr int QMAX = (1 << BITS) - 1;
     extern __shared__ __align__(16) uint16_t s_tile[];  // [group][33]
     const int n0 = blockIdx.x * 32;
@@ -89,10 +91,10 @@ __global__ void __launch_bounds__(256) k_spax_encode(const uint16_t* __restrict_
             mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
         }
         const float scale = __fdiv_rn(__fsub_rn(mx, mn), (float)QMAX);
-        for (int r = EPB * tx; r < group; r += 32 * EPB) {
-            uint32_t byte = 0u;
+        for (int r = EPU * tx; r < group; r += 32 * EPU) {
+            uint32_t word = 0u;
 #pragma unroll
-            for (int h = 0; h < EPB; ++h) {
+            for (int h = 0; h < EPU; ++h) {
                 const uint16_t hb = s_tile[(r + h) * 33 + cc];
                 WdT[(size_t)n * d + r0 + r + h] = hb;
                 const float w = __uint_as_float((uint32_t)hb << 16);
@@ -103,9 +105,15 @@ __global__ void __launch_bounds__(256) k_spax_encode(const uint16_t* __restrict_
                     v = (int)floorf(t);
                     v = v < 0 ? 0 : (v > QMAX ? QMAX : v);
                 }
-                byte |= (uint32_t)v << (h * BITS);
+                word |= (uint32_t)v << (h * BITS);
             }
-            recs[(size_t)n * rec_bytes + (r0 + r) / EPB] = (uint8_t)byte;
+            // element i at bit i * BITS of the column's little-endian stream
+            uint8_t* dst = recs + (size_t)n * rec_bytes + (size_t)(r0 + r) * BITS / 8;
+            dst[0] = (uint8_t)word;
+            if constexpr (BITS == 3) {
+                dst[1] = (uint8_t)(word >> 8);
+                dst[2] = (uint8_t)(word >> 16);
+            }
         }
         if (tx == 0) {
             float* prm = reinterpret_cast<float*>(recs + (size_t)n * rec_bytes + (size_t)d * BITS / 8);
@@ -155,6 +163,10 @@ cudaError_t launch_spax_encode(const uint16_t* Wd, int d, int N, int bits, int g
         case 2:
             if ((e = allow_max_smem(k_spax_encode<2>)) != cudaSuccess) return e;
             k_spax_encode<2><<<grid, 256, smem, st>>>(Wd, d, N, group, ngp, WdT, recs, rec_bytes);
+            break;
+        case 3:
+            if ((e = allow_max_smem(k_spax_encode<3>)) != cudaSuccess) return e;
+            k_spax_encode<3><<<grid, 256, smem, st>>>(Wd, d, N, group, ngp, WdT, recs, rec_bytes);
             break;
         case 4:
             if ((e = allow_max_smem(k_spax_encode<4>)) != cudaSuccess) return e;

@@ -657,7 +657,7 @@ def spax_in_selected_set(si, torch, dev, stream, W, enc, seed, layers=4, toks=64
 
 
 def spax_code_widths(si, torch, dev, stream, W, seed, layers=4, toks=64):
-    """The same SpAx layer-token with 2-, 4- and 8-bit middle-tier codes, on the
+    """The same SpAx layer-token with 2-, 3-, 4- and 8-bit middle-tier codes, on the
     first `layers` layers of the stack: microseconds per layer-token and the
     selected bytes (dense gate/up + bf16 top + b-bit records) per second."""
     w = synth.WORKLOADS["llama3.1-8b-spax"]
@@ -667,7 +667,7 @@ def spax_code_widths(si, torch, dev, stream, W, seed, layers=4, toks=64):
     y = torch.empty((toks, layers, w.d), dtype=torch.float32, device=dev)
     a = torch.empty((layers, w.N), dtype=torch.float32, device=dev)
     out = {}
-    for bits in (2, 4, 8):
+    for bits in (2, 3, 4, 8):
         enc = []
         for l in range(layers):
             _, _, Wd = gpu_weights(torch, seed, l, w.d, w.N, w.sigma, dev)

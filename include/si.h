@@ -360,12 +360,15 @@ int si_stack_destroy(si_stack *stack);
  * min + q * scale. The handle keeps a column-major bf16 copy of Wd (top tier,
  * one contiguous column per neuron) and, per column, one record of
  * rec = d*bits/8 + 8*ng_pad bytes (ng_pad = d/group rounded up to even): the
- * codes (element i at bit offset i*bits, little-endian: element 2i in the
- * low nibble of byte i for bits = 4), then ng_pad fp32 (scale, min) pairs,
- * so a middle-tier column is one contiguous read.
+ * codes (one bit stream per column: element i in bits i*bits .. i*bits +
+ * bits - 1, bit k being bit k % 8 of byte k / 8; element 2i in the low
+ * nibble of byte i for bits = 4, and 3-bit codes straddle bytes), then
+ * ng_pad fp32 (scale, min) pairs, so a middle-tier column is one contiguous
+ * read.
  *   Wd bf16 [d x N]. Synchronous (allocates, enqueues, waits).
- * Requires bits 2, 4 or 8 (SI_ERR_UNSUPPORTED otherwise), group a power of
- * two >= 8 dividing d, d % 64 == 0, d <= 4096. */
+ * Requires bits 2, 3, 4 or 8 (SI_ERR_UNSUPPORTED otherwise), group a power
+ * of two >= 8 dividing d, d % 64 == 0 (d % 128 == 0 for bits = 3),
+ * d <= 4096. */
 int spax_encode(const uint16_t *Wd, int d, int N, int bits, int group, spax_layer **out,
                 void *stream);
 

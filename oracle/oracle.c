@@ -428,12 +428,14 @@ void oracle_swiglu(const double *g, const double *u, int n, double *a)
  *   scale  = (mx - mn) / (2^bits - 1)            (float32)
  *   q      = clamp(floor((w - mn) / scale + 0.5), 0, 2^bits - 1), q = 0 when scale == 0
  *   w^     = mn + q * scale.
- * codes: [N x d*bits/8] bytes, element 2i in the low nibble for bits = 4
- * (generally: element i at bit offset (i*bits) % 8 of byte (i*bits)/8, bits
- * in {2, 4, 8}); params: [N x d/group x 2] float32 = (scale, min). */
+ * codes: [N x d*bits/8] bytes holding each column's codes as one bit stream,
+ * element i in bits i*bits .. i*bits + bits - 1, bit k of the stream being
+ * bit k % 8 of byte k / 8 (so element 2i sits in the low nibble of byte i for
+ * bits = 4, and a 3-bit code can straddle two bytes); bits in {2, 3, 4, 8},
+ * d*bits a multiple of 8; params: [N x d/group x 2] float32 = (scale, min). */
 int oracle_spax_encode(const uint16_t *Wd, int d, int N, int bits, int group, uint8_t *codes, float *params)
 {
-    if (!(bits == 2 || bits == 4 || bits == 8) || group <= 0 || d % group) return -1;
+    if (!(bits == 2 || bits == 3 || bits == 4 || bits == 8) || group <= 0 || d % group || (d * bits) % 8) return -1;
     int ng = d / group, qmax = (1 << bits) - 1;
     size_t cb = (size_t)d * bits / 8;
     memset(codes, 0, cb * (size_t)N);
@@ -459,8 +461,10 @@ int oracle_spax_encode(const uint16_t *Wd, int d, int N, int bits, int group, ui
                     if (q < 0) q = 0;
                     if (q > qmax) q = qmax;
                 }
-                size_t bit = (size_t)i * bits;
-                codes[(size_t)n * cb + bit / 8] |= (uint8_t)(q << (bit % 8));
+                for (int k = 0; k < bits; ++k) {
+                    size_t bit = (size_t)i * bits + k;
+                    codes[(size_t)n * cb + bit / 8] |= (uint8_t)(((q >> k) & 1) << (bit % 8));
+                }
             }
         }
     return 0;
@@ -496,7 +500,6 @@ void oracle_spax_down(const float *a, int N, int d, const uint16_t *Wd, const ui
 {
     int ng = d / group;
     size_t cb = (size_t)d * bits / 8;
-    uint32_t qmask = (1u << bits) - 1u;
     #pragma omp parallel for schedule(static)
     for (int j = 0; j < d; ++j) {
         double acc = 0.0;
@@ -505,10 +508,13 @@ void oracle_spax_down(const float *a, int N, int d, const uint16_t *Wd, const ui
             acc += (double)a[n] * bf(Wd[(size_t)j * N + n]);
         }
         int g = j / group;
-        size_t bit = (size_t)j * bits;
         for (int i = 0; i < k_mid; ++i) {
             int n = mid[i];
-            uint32_t q = ((uint32_t)codes[(size_t)n * cb + bit / 8] >> (bit % 8)) & qmask;
+            uint32_t q = 0;
+            for (int k = 0; k < bits; ++k) {
+                size_t bit = (size_t)j * bits + k;
+                q |= (uint32_t)((codes[(size_t)n * cb + bit / 8] >> (bit % 8)) & 1u) << k;
+            }
             double scale = params[((size_t)n * ng + g) * 2 + 0];
             double mn = params[((size_t)n * ng + g) * 2 + 1];
             acc += (double)a[n] * (mn + (double)q * scale);

@@ -68,7 +68,9 @@ def test_validation_before_cuda(si):
     assert lib.si_pack_loaded(p, p, p, 64, 10, p, p, 0.5, 0.6, C.byref(h), None) == si.SI_ERR_INVALID_ARG
     assert lib.si_sparse_ffn_decode(None, p, 1, 1, p, p, None) == si.SI_ERR_INVALID_ARG
     assert lib.si_select_from_absact(None, p, 8, 1, 1, 1, 0.4, p, None, None, None) == si.SI_ERR_INVALID_ARG
-    assert lib.spax_encode(p, 256, 10, 3, 128, C.byref(h), None) == si.SI_ERR_UNSUPPORTED
+    assert lib.spax_encode(p, 256, 10, 5, 128, C.byref(h), None) == si.SI_ERR_UNSUPPORTED
+    # 3-bit records are whole 16-byte units only when d % 128 == 0
+    assert lib.spax_encode(p, 192, 10, 3, 64, C.byref(h), None) == si.SI_ERR_INVALID_ARG
     assert lib.spax_encode(p, 256, 10, 4, 100, C.byref(h), None) == si.SI_ERR_INVALID_ARG
     assert lib.si_merge_scores(None, None, 1, 4, p, None) == si.SI_ERR_INVALID_ARG
     assert lib.si_layer_destroy(None) == si.SI_OK

@@ -39,7 +39,8 @@ def llama8b_layer():
 
 @pytest.mark.parametrize("d,N,group,bits", [(256, 64, 128, 4), (4096, 14336, 128, 4), (512, 300, 64, 4),
                                             (128, 5, 8, 4), (256, 64, 128, 8), (512, 300, 64, 2),
-                                            (128, 5, 8, 2), (4096, 14336, 128, 8), (1024, 700, 32, 2)])
+                                            (128, 5, 8, 2), (4096, 14336, 128, 8), (1024, 700, 32, 2),
+                                            (4096, 14336, 128, 3), (256, 64, 128, 3), (128, 5, 8, 3)])
 def test_spax_encode_bit_exact(si, d, N, group, bits, llama8b_layer):
     if (d, N) == (4096, 14336):
         _, _, Wd = llama8b_layer
@@ -69,7 +70,8 @@ def signed_acts(seed, N, ties=False):
                                                  (1000, 1.0, 0.0, False, 4), (1000, 0.0, 1.0, True, 4),
                                                  (1000, 0.0, 0.0, False, 4), (77, 0.4, 0.6, True, 4),
                                                  (14336, 0.3, 0.3, False, 8), (14336, 0.3, 0.3, True, 2),
-                                                 (1000, 0.0, 1.0, True, 8), (1000, 0.2, 0.8, False, 2)])
+                                                 (1000, 0.0, 1.0, True, 8), (1000, 0.2, 0.8, False, 2),
+                                                 (14336, 0.3, 0.3, False, 3), (1000, 0.0, 1.0, True, 3)])
 def test_spax_tiers_and_down(si, N, top, mid, ties, bits):
     d = 256 if N != 14336 else 4096
     _, _, Wd = synth.layer_weights(52, 0, d, N)
@@ -133,7 +135,7 @@ def test_spax_dense_act(si, d, N, llama8b_layer):
     assert rel_err(a.numpy(), ref) <= 1e-5
 
 
-@pytest.mark.parametrize("bits", [4, 8, 2])
+@pytest.mark.parametrize("bits", [4, 8, 2, 3])
 def test_spax_ffn_decode_full_token(si, llama8b_layer, bits):
     """One Llama-3.1-8B layer token: dense gate/up, 30% bf16 / 30% b-bit / 40% skipped."""
     Wg, Wu, Wd = llama8b_layer
@@ -172,7 +174,8 @@ def test_spax_dense_act_repeated_calls(si, llama8b_layer):
 
 
 @pytest.mark.parametrize("d,N,frac,top,mid,bits", [(4096, 14336, 0.4, 0.3, 0.3, 4), (256, 1000, 0.5, 0.5, 0.5, 2),
-                                                  (256, 1000, 0.05, 0.2, 0.3, 8), (256, 1000, 0.0, 0.3, 0.3, 4)])
+                                                  (256, 1000, 0.05, 0.2, 0.3, 8), (256, 1000, 0.0, 0.3, 0.3, 4),
+                                                  (256, 1000, 0.5, 0.3, 0.4, 3)])
 def test_spax_select_decode(si, d, N, frac, top, mid, bits, llama8b_layer):
     """SelectInfer x SpAx: gate/up only on a selected set, tiers inside it
     (fractions of the set), the down-projection over its top and middle

@@ -327,18 +327,25 @@ def test_spax_encode_constant_and_ramp_groups():
     assert np.all(params[1, :, 0] == 0.0) and np.all(params[1, :, 1] == np.float32(-1.25))
 
 
+def _codes_of(codes, d, bits):
+    # element i of a column: bits i*bits .. i*bits+bits-1 of the column's
+    # little-endian bit stream, read through a Python integer
+    out = np.zeros((codes.shape[0], d), np.int64)
+    for n in range(codes.shape[0]):
+        stream = int.from_bytes(bytes(codes[n]), "little")
+        for i in range(d):
+            out[n, i] = (stream >> (i * bits)) & ((1 << bits) - 1)
+    return out
+
+
 def test_spax_encode_other_widths():
     d, N = 128, 3
     _, _, Wd = synth.layer_weights(12, 0, d, N)
-    for bits in (2, 8):
+    for bits in (2, 3, 8):
         codes, params = oracle.spax_encode(Wd, bits, 64)
         assert codes.shape == (N, d * bits // 8)
-        qmax = (1 << bits) - 1
         w = f32(Wd)
-        per = 8 // bits
-        q = np.zeros((N, d), np.int64)
-        for k in range(per):
-            q[:, k::per] = (codes >> (k * bits)) & qmax
+        q = _codes_of(codes, d, bits)
         for n in range(N):
             for g in range(2):
                 scale, mn = params[n, g]
@@ -596,3 +603,22 @@ def test_rms_norm_input_scale_invariance():
     assert np.array_equal(oracle.rms_norm_bf16(h), oracle.rms_norm_bf16(h * 4.0))
     x = synth.bf16_bits_to_f32(oracle.rms_norm_bf16(h)).astype(np.float64)
     assert abs(np.sqrt(np.mean(x ** 2)) - 1.0) < 4e-3   # unit RMS up to bf16 rounding
+
+
+def test_spax_encode_3bit_ramp_layout():
+    # a group whose values are exactly mn + q*scale for q = 0..7 (scale = 1/8):
+    # the codes are the ramp itself, and the stream packs element i at bits
+    # 3i..3i+2, so 8 codes fill 3 bytes and codes straddle byte boundaries
+    d, N, group = 16, 1, 8
+    vals = np.array([0.0, 0.125, 0.25, 0.375, 0.5, 0.625, 0.75, 0.875] * 2)
+    Wd = bf16(vals.reshape(d, N))
+    codes, params = oracle.spax_encode(Wd, 3, group)
+    assert codes.shape == (1, 6)
+    ramp = sum(q << (3 * q) for q in range(8))        # 0b111110101100011010001000
+    want = list(ramp.to_bytes(3, "little")) * 2
+    assert [int(b) for b in codes[0]] == want
+    assert np.allclose(params[0, :, 0], 0.125) and np.allclose(params[0, :, 1], 0.0)
+    # the decoder reads the same stream back: mid tier only, a = 1 -> y = w exactly
+    y = oracle.spax_down(np.ones(N, np.float32), Wd, codes, params, np.zeros(0, np.int32),
+                         np.zeros(1, np.int32), bits=3, group=group)
+    assert np.array_equal(y, vals)
