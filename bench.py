@@ -786,16 +786,13 @@ def cpu_baseline_spax(w, tokens=4, seed=12):
                       "extrapolated to %d layers" % (tokens, w.L), "extrapolated": True}
 
 
-def run_reference(args, world, rank):
-    """The reference arm: the CPU oracle as it stands, on the host cores, on the
-    headline workload; each step is a bounded sample (one layer-token of each of
-    layers {0, L/2, L-1}) whose measured time is reported as ms_per_step."""
-    if rank != 0:
-        return
+def reference_sample(w, seed=21):
+    """The reference arm's bounded sample on workload w: one decode token of the
+    oracle's sparse FFN on each of layers {0, L/2, L-1}. Returns (step, layer-
+    tokens per step, description, cores); step() runs one sample and returns
+    its wall time in seconds."""
     import oracle
-    w = HEAD
-    t_all = time.perf_counter()
-    rng = np.random.default_rng(21)
+    rng = np.random.default_rng(seed)
     layers = sorted({0, w.L // 2, w.L - 1})
     data = []
     for l in layers:
@@ -807,23 +804,35 @@ def run_reference(args, world, rank):
         n_sel = oracle.cnt(w.phi, w.N)
         S = oracle.select(rng.random((64, len(loaded))).astype(np.float32), 64, 1, len(loaded), st, 256, n_sel)
         data.append((Wg, Wu, Wd, loaded, S[0]))
+    xs = _cpu_bf16(rng, (len(layers), w.d))
 
     def step():
-        for Wg, Wu, Wd, loaded, S in data:
-            oracle.sparse_ffn(Wg, Wu, Wd, loaded, S, _cpu_bf16(rng, (w.d,)))
-
-    for _ in range(args.warmup):
-        step()
-    times = []
-    for _ in range(args.steps):
         t0 = time.perf_counter()
-        step()
-        times.append(time.perf_counter() - t0)
-    per_lt = statistics.median(times) / len(layers)
-    value = 1.0 / (w.L * per_lt)
+        for (Wg, Wu, Wd, loaded, S), x in zip(data, xs):
+            oracle.sparse_ffn(Wg, Wu, Wd, loaded, S, x)
+        return time.perf_counter() - t0
+
     cores = oracle.num_threads()
     desc = ("oracle sparse_ffn, one decode token on each of layers %s of the %d-layer stack per step "
             "(%d OpenMP threads); tokens/s extrapolated to the full stack" % (layers, w.L, cores))
+    return step, len(layers), desc, cores
+
+
+def run_reference(args, world, rank):
+    """The reference arm: the CPU oracle as it stands, on the host cores, on the
+    headline workload; each step is a bounded sample whose measured time is
+    reported as ms_per_step, the full-step figure under its own key."""
+    if rank != 0:
+        return
+    import oracle
+    w = HEAD
+    t_all = time.perf_counter()
+    step, n_lt, desc, cores = reference_sample(w)
+    for _ in range(args.warmup):
+        step()
+    times = [step() for _ in range(args.steps)]
+    per_lt = statistics.median(times) / n_lt
+    value = 1.0 / (w.L * per_lt)
     out = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "tokens/s", "n_gpus": world,
            "steps": args.steps, "warmup": args.warmup,
            "ms_per_step": round(statistics.mean(times) * 1e3, 3),

@@ -30,11 +30,11 @@ def _worker(rank, world, port, q):
     s = bench.sum_over_ranks(256.0, world)
     bench.barrier(world)
     # reference arm: rank 0 alone prints one JSON line; the other ranks do nothing
-    bench.cpu_sample = lambda budget: (10.0, "fake sample", 1, 1)
+    # a sample of 3 layer-tokens that takes 0.3 s per step
+    bench.reference_sample = lambda w: ((lambda: 0.3), 3, "fake sample", 1)
     buf = io.StringIO()
     with redirect_stdout(buf):
-        bench.run_reference(bench.main.__globals__["argparse"].Namespace(warmup=0, steps=2, cpu_seconds=0.1),
-                            world, rank)
+        bench.run_reference(bench.main.__globals__["argparse"].Namespace(warmup=0, steps=2), world, rank)
     q.put((rank, m, s, buf.getvalue()))
     dist.destroy_process_group()
 
@@ -54,5 +54,7 @@ def test_two_rank_aggregation_gloo():
     assert m0 == m1 == 3.0           # the slowest rank's time
     assert s0 == s1 == 512.0         # units processed by all ranks
     line = json.loads(out0.strip())
-    assert line["impl"] == "reference" and line["n_gpus"] == 2 and line["value"] == 10.0
+    assert line["impl"] == "reference" and line["n_gpus"] == 2
+    assert line["value"] == round(3 / (28 * 0.3), 4)          # 3 layer-tokens in 0.3 s, 28 layers per token
+    assert line["ms_per_step"] == 300.0                        # the measured time of a step's sample
     assert out1 == ""
