@@ -15,6 +15,7 @@ from ._binding import (  # noqa: F401
     si_decode_plan, si_expand_clusters, si_sparse_ffn_decode, si_sparse_ffn_decode_residual, si_sparse_ffn_decode_noalloc,
     Stack, si_stack_create, si_stack_plan, si_sparse_ffn_decode_stack,
     spax_encode, spax_dense_act, spax_tiered_down, spax_ffn_decode, spax_select_decode,
+    spax_encode_rows, spax_gate_up, spax_all_decode,
     SI_OK, SI_ERR_INVALID_ARG, SI_ERR_CUDA, SI_ERR_OOM, SI_ERR_UNSUPPORTED, SI_ERR_DEVICE,
 )
 

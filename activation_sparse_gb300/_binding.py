@@ -56,6 +56,8 @@ SIGNATURES = {
     "spax_tiered_down": (_i, [_vp, _vp, _d, _d, _vp, _vp, _vp, _vp]),
     "spax_ffn_decode": (_i, [_vp, _vp, _vp, _vp, _d, _d, _vp, _vp, _vp]),
     "spax_select_decode": (_i, [_vp, _vp, _vp, _vp, _i, _vp, _d, _d, _vp, _vp, _vp]),
+    "spax_gate_up": (_i, [_vp, _vp, _vp, _d, _d, _vp, _vp, _vp, _vp]),
+    "spax_all_decode": (_i, [_vp, _vp, _vp, _vp, _d, _d, _d, _d, _vp, _vp, _vp]),
 }
 
 _lib = None
@@ -430,5 +432,33 @@ def spax_ffn_decode(layer: SpaxLayer, Wg, Wu, x, top_frac, mid_frac, y, a_out=No
     torch = _torch()
     _check(load().spax_ffn_decode(layer.handle, _bf16(Wg, "Wg"), _bf16(Wu, "Wu"), _bf16(x, "x"), float(top_frac),
                                   float(mid_frac), _ptr(y, torch.float32, "y"),
+                                  _ptr(a_out, torch.float32, "a_out"), _stream(stream)))
+    return y
+
+
+def spax_encode_rows(W, bits=4, group=128, stream=None) -> SpaxLayer:
+    """Encodes a gate or up matrix W [N x d] for spax_gate_up: its columns
+    (input channels) get the records, with groups along the N neurons."""
+    N, d = W.shape
+    h = C.c_void_p()
+    _check(load().spax_encode(_bf16(W, "W"), N, d, int(bits), int(group), C.byref(h), _stream(stream)))
+    return SpaxLayer(h)
+
+
+def spax_gate_up(gate: SpaxLayer, up: SpaxLayer, x, top_frac, mid_frac, a, top_idx=None, mid_idx=None, stream=None):
+    """a = silu(g) * u with g, u tiered over the input channels by |x|."""
+    torch = _torch()
+    _check(load().spax_gate_up(gate.handle, up.handle, _bf16(x, "x"), float(top_frac), float(mid_frac),
+                               _ptr(a, torch.float32, "a"), _ptr(top_idx, torch.int32, "top_idx"),
+                               _ptr(mid_idx, torch.int32, "mid_idx"), _stream(stream)))
+    return a
+
+
+def spax_all_decode(down: SpaxLayer, gate: SpaxLayer, up: SpaxLayer, x, in_top, in_mid, top_frac, mid_frac, y,
+                    a_out=None, stream=None):
+    """One SpAx-ALL FFN token: gate/up tiers by |x|, then the down tiers by |a|."""
+    torch = _torch()
+    _check(load().spax_all_decode(down.handle, gate.handle, up.handle, _bf16(x, "x"), float(in_top), float(in_mid),
+                                  float(top_frac), float(mid_frac), _ptr(y, torch.float32, "y"),
                                   _ptr(a_out, torch.float32, "a_out"), _stream(stream)))
     return y

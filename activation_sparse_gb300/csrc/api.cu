@@ -632,7 +632,7 @@ int spax_encode(const uint16_t* Wd, int d, int N, int bits, int group, spax_laye
         return fail(SI_ERR_INVALID_ARG, "need group a power of two >= 8, d % 64 == 0, d % group == 0");
     if (bits == 3 && d % 128)
         return fail(SI_ERR_INVALID_ARG, "3-bit codes need d % 128 == 0 (records of whole 16-byte units)");
-    if (d > 4096) return fail(SI_ERR_UNSUPPORTED, "tiered decode supports d <= 4096");
+    if (d > 32768) return fail(SI_ERR_UNSUPPORTED, "need d <= 32768");
     if (N < 1 || N > 32768) return fail(SI_ERR_INVALID_ARG, "need 1 <= N <= 32768");
     cudaStream_t st = (cudaStream_t)stream;
     if (capturing(st)) return fail(SI_ERR_INVALID_ARG, "spax_encode allocates; not allowed during capture");
@@ -737,6 +737,7 @@ int tier_counts(const spax_layer* L, double top_frac, double mid_frac, long long
 // must hold the tier histogram of a (the kernel re-zeroes it).
 int tiered_core(spax_layer* L, const float* a, long long k_top, long long k_mid, float* y, int32_t* top_out,
                 int32_t* mid_out, cudaStream_t st) {
+    if (L->d > 4096) return fail(SI_ERR_UNSUPPORTED, "the tiered down-projection supports d <= 4096");
     unsigned* err = nullptr;
     int rc = err_word(&err);
     if (rc) return rc;
@@ -957,6 +958,83 @@ int si_stack_destroy(si_stack* K) {
     if (!K) return SI_OK;
     cudaDeviceSynchronize();
     destroy_stack(K);
+    return SI_OK;
+}
+
+}  // extern "C"
+
+namespace {
+
+// The gate/up tiers by |x| into a (and, when hist is given, the down
+// projection's tier histogram of a).
+int gate_up_core(const spax_layer* G, const spax_layer* U, const uint16_t* x, double top_frac, double mid_frac,
+                 float* a, int32_t* top_idx, int32_t* mid_idx, unsigned* hist, int32_t* slab, cudaStream_t st) {
+    if (!G || !U || !x || !a) return fail(SI_ERR_INVALID_ARG, "NULL pointer");
+    // an encoded gate/up matrix: rows = neurons (handle d), columns = input channels (handle N)
+    if (G->d != U->d || G->N != U->N || G->bits != U->bits || G->group != U->group)
+        return fail(SI_ERR_INVALID_ARG, "gate and up encodings must have the same shape, bits and group");
+    const int N = G->d, d = G->N;
+    if (N % 4 || G->group % 4) return fail(SI_ERR_INVALID_ARG, "need N % 4 == 0");
+    if (d > 8192) return fail(SI_ERR_UNSUPPORTED, "gate/up tiers support d <= 8192 input channels");
+    if (!(top_frac >= 0.0 && mid_frac >= 0.0 && top_frac + mid_frac <= 1.0))
+        return fail(SI_ERR_INVALID_ARG, "tier fractions must be >= 0 with top + mid <= 1");
+    const long long k_top = count_of(top_frac, d), k_mid = count_of(mid_frac, d);
+    if (k_top + k_mid > d) return fail(SI_ERR_INVALID_ARG, "top + mid tiers exceed the channels");
+    unsigned* err = nullptr;
+    int rc = err_word(&err);
+    if (rc) return rc;
+    si::GateUpTierParams P = {};
+    P.WgT = G->WdT;
+    P.WuT = U->WdT;
+    P.gcodes = G->codes;
+    P.ucodes = U->codes;
+    P.rec_bytes = G->rec_bytes;
+    P.bits = G->bits;
+    P.group = G->group;
+    P.d = d;
+    P.N = N;
+    P.x = x;
+    P.k_top = (int)k_top;
+    P.k_mid = (int)k_mid;
+    P.a = a;
+    P.hist = hist;
+    P.slab = hist ? slab : nullptr;
+    P.top_out = top_idx;
+    P.mid_out = mid_idx;
+    P.S = si::spax_gate_up_slice(N);
+    P.err = err;
+    if (P.S < 4) return fail(SI_ERR_CUDA, "cannot query the device");
+    SI_CK(si::launch_spax_gate_up(P, st));
+    return SI_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int spax_gate_up(const spax_layer* gate, const spax_layer* up, const uint16_t* x, double top_frac, double mid_frac,
+                 float* a, int32_t* top_idx, int32_t* mid_idx, void* stream) {
+    return gate_up_core(gate, up, x, top_frac, mid_frac, a, top_idx, mid_idx, nullptr, nullptr, (cudaStream_t)stream);
+}
+
+int spax_all_decode(spax_layer* down, const spax_layer* gate, const spax_layer* up, const uint16_t* x,
+                    double in_top_frac, double in_mid_frac, double top_frac, double mid_frac, float* y,
+                    float* a_out, void* stream) {
+    if (!down || !gate || !up || !y) return fail(SI_ERR_INVALID_ARG, "NULL pointer");
+    if (down->N != gate->d || down->d != gate->N)
+        return fail(SI_ERR_INVALID_ARG, "the down encoding's columns must be the gate/up encodings' rows");
+    long long k_top = 0, k_mid = 0;
+    int rc = tier_counts(down, top_frac, mid_frac, &k_top, &k_mid);
+    if (rc) return rc;
+    cudaStream_t st = (cudaStream_t)stream;
+    float* a = a_out ? a_out : down->a;
+    // the gate/up pass builds the down tiers' histogram of a as it writes it
+    if ((rc = gate_up_core(gate, up, x, in_top_frac, in_mid_frac, a, nullptr, nullptr, down->hist, down->slab, st)))
+        return rc;
+    if ((rc = tiered_core(down, a, k_top, k_mid, y, nullptr, nullptr, st))) {
+        cudaMemsetAsync(down->hist, 0, (si::kTierBins + 1) * sizeof(unsigned), st);  // leave it clean
+        return rc;
+    }
     return SI_OK;
 }
 

@@ -77,6 +77,31 @@ struct TieredDownParams {
     int aux_floats;           // per-CTA buffer: activations in the first half, columns in the second
 };
 
+// SpAx tiers on the gate/up projections by |x| (spax_in.cu). Channel j of the
+// gate (up) weights is column j of Wg (Wu): WgT [d][N] bf16 holds the columns
+// contiguously, gcodes [d] the per-channel records (N*bits/8 code bytes, then
+// ngp (scale, min) pairs for groups of `group` consecutive neurons).
+struct GateUpTierParams {
+    const uint16_t* WgT;
+    const uint16_t* WuT;
+    const uint8_t* gcodes;
+    const uint8_t* ucodes;
+    int rec_bytes, bits, group;
+    int d, N;                 // input channels, neurons
+    const uint16_t* x;        // [d] bf16
+    int k_top, k_mid;         // channel tiers
+    float* a;                 // [N] out
+    unsigned* hist;           // optional tier histogram of a (kTierBins + 1 words, zero on entry)
+    int32_t* slab;            // optional member lists of hist
+    int32_t* top_out;         // optional [k_top] channel lists, ascending
+    int32_t* mid_out;         // optional [k_mid]
+    int S;                    // neurons per CTA (multiple of 4, <= 128)
+    unsigned* err;
+};
+int spax_gate_up_slice(int N);
+size_t spax_gate_up_smem(int d, int S);
+cudaError_t launch_spax_gate_up(const GateUpTierParams& P, cudaStream_t st);
+
 // select.cu
 cudaError_t launch_topk_alpha(const float* absA, int ld, int n, int T, int B, int alpha, uint32_t* counts,
                               uint32_t* topmask, cudaStream_t st);

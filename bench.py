@@ -595,6 +595,7 @@ def run_spax(si, torch, dev, stream, args, toks=64):
                                "note": "token time per layer minus the dense pass's time per layer"},
            "token_roofline_frac": round(byts / per_tok / 1e9 / hbm_peak, 4)}
     out["e2e"] = spax_e2e(si, torch, dev, stream, enc, W, w, args)
+    out["all"] = spax_all(si, torch, dev, stream, W, enc, seed)
     out["in_selected_set"] = spax_in_selected_set(si, torch, dev, stream, W, enc, seed)
     out["code_widths"] = spax_code_widths(si, torch, dev, stream, W, seed)
     for e in enc:
@@ -602,6 +603,56 @@ def run_spax(si, torch, dev, stream, args, toks=64):
     del W, enc, x, y, a
     torch.cuda.empty_cache()
     return out
+
+
+def spax_all(si, torch, dev, stream, W, enc, seed, layers=8, toks=64, in_top=0.3, in_mid=0.3):
+    """SpAx-ALL for the FFN on the first `layers` layers: tiers on the gate/up
+    projections by |x| (input channels, 30 % bf16 / 30 % 4-bit codes) then the
+    down tiers by |a|; k_spax_gate_up's own roofline from a gate/up-only graph."""
+    w = synth.WORKLOADS["llama3.1-8b-spax"]
+    hbm_peak, _, _, kind = peaks()
+    gates, ups = [], []
+    for l in range(layers):
+        gates.append(si.spax_encode_rows(W[l][0], w.bits, w.group))
+        ups.append(si.spax_encode_rows(W[l][1], w.bits, w.group))
+    x = gpu_tokens(torch, seed, 403, toks * layers, w.d, dev).view(toks, layers, w.d)
+    y = torch.empty((toks, layers, w.d), dtype=torch.float32, device=dev)
+    a = torch.empty((layers, w.N), dtype=torch.float32, device=dev)
+
+    def run():
+        for t in range(toks):
+            for l in range(layers):
+                si.spax_all_decode(enc[l], gates[l], ups[l], x[t, l], in_top, in_mid, w.top_frac, w.mid_frac,
+                                   y[t, l], a[l])
+
+    def gate_up_only():
+        for t in range(toks):
+            for l in range(layers):
+                si.spax_gate_up(gates[l], ups[l], x[t, l], in_top, in_mid, a[l])
+
+    g, gg = graph_of(torch, stream, run), graph_of(torch, stream, gate_up_only)
+    ms = statistics.median(replay_ms(torch, g, stream) for _ in range(3))
+    gu_ms = statistics.median(replay_ms(torch, gg, stream) for _ in range(3))
+    assert si.si_device_error() == 0
+    for e in gates + ups:
+        e.close()
+    kt, km = si.si_count(in_top, w.d), si.si_count(in_mid, w.d)
+    ngp_n = -(-(w.N // w.group) // 2) * 2
+    gu_bytes = kt * w.N * 2 * 2 + km * 2 * (w.N * w.bits // 8 + 8 * (w.N // w.group))
+    k_top, k_mid = si.si_count(w.top_frac, w.N), si.si_count(w.mid_frac, w.N)
+    ngp = -(-(w.d // w.group) // 2) * 2
+    down_bytes = k_top * 2 * w.d + k_mid * (w.d * w.bits // 8 + 8 * ngp)
+    us = ms * 1e3 / (toks * layers)
+    gu_us = gu_ms * 1e3 / (toks * layers)
+    del ngp_n
+    return {"layers": layers, "tokens": toks, "in_top_frac": in_top, "in_mid_frac": in_mid,
+            "us_per_layer_token": round(us, 2), "bytes_per_layer_token": gu_bytes + down_bytes,
+            "hbm_gbs": round((gu_bytes + down_bytes) / us / 1e3, 1),
+            "frac": round((gu_bytes + down_bytes) / us / 1e3 / hbm_peak, 4),
+            "tokens_per_s_32_layers": round(1e6 / (us * w.L), 2),
+            "gate_up_roofline": {"kernel": "k_spax_gate_up", "bound": "hbm", "achieved": round(gu_bytes / gu_us / 1e3, 1),
+                                 "peak": hbm_peak, "unit": "GB/s", "frac": round(gu_bytes / gu_us / 1e3 / hbm_peak, 4),
+                                 "peak_source": kind, "bytes_per_launch": gu_bytes, "launch_us": round(gu_us, 3)}}
 
 
 def spax_e2e(si, torch, dev, stream, enc, W, w, args, toks=16):
@@ -922,8 +973,8 @@ def run_profile_case(args):
     layer, as the headline runs it), decode1b (Llama3.2-1B layer), batch8
     (k_sparse_decode<8>, Qwen2.5-3B layer), prefill (k_act_gemm, 1024-token
     prompt, Llama3.2-3B layer), stack (k_sparse_decode_stack, 4 Llama3.2-3B
-    layers), dense (k_dense_act) and tiered (k_tiered_down) on a Llama-3.1-8B
-    layer. Prints one JSON line with the CUDA-event time per launch."""
+    layers), dense (k_dense_act), tiered (k_tiered_down) and gateup
+    (k_spax_gate_up, channel tiers 30 % / 30 %) on a Llama-3.1-8B layer. Prints one JSON line with the CUDA-event time per launch."""
     import torch
     import activation_sparse_gb300 as si
     dev = torch.device("cuda", 0)
@@ -968,8 +1019,14 @@ def run_profile_case(args):
         a = torch.empty(w.N, dtype=torch.float32, device=dev)
         y = torch.empty(w.d, dtype=torch.float32, device=dev)
         si.spax_dense_act(Wg, Wu, x, a)
-        fn = (lambda: si.spax_dense_act(Wg, Wu, x, a)) if case == "dense" else \
-             (lambda: si.spax_tiered_down(enc, a, w.top_frac, w.mid_frac, y))
+        if case == "gateup":
+            gate, upe = si.spax_encode_rows(Wg, w.bits, w.group), si.spax_encode_rows(Wu, w.bits, w.group)
+            keep += [gate, upe]
+            fn = lambda: si.spax_gate_up(gate, upe, x, 0.3, 0.3, a)  # noqa: E731
+        elif case == "dense":
+            fn = lambda: si.spax_dense_act(Wg, Wu, x, a)  # noqa: E731
+        else:
+            fn = lambda: si.spax_tiered_down(enc, a, w.top_frac, w.mid_frac, y)  # noqa: E731
     for _ in range(args.warmup):
         fn()
     torch.cuda.synchronize()
@@ -993,7 +1050,8 @@ def main(argv=None):
     ap.add_argument("--headline-only", action="store_true", help="skip the other workloads' objects")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--out-dir", default=None, help="directory for the clock samples (optional)")
-    ap.add_argument("--profile-case", choices=["decode", "decode1b", "batch8", "prefill", "stack", "dense", "tiered"],
+    ap.add_argument("--profile-case", choices=["decode", "decode1b", "batch8", "prefill", "stack", "dense", "tiered",
+                                               "gateup"],
                     default=None, help="run only a few launches of one kernel (for ncu captures)")
     args = ap.parse_args(argv)
     if args.profile_case:

@@ -368,7 +368,8 @@ int si_stack_destroy(si_stack *stack);
  *   Wd bf16 [d x N]. Synchronous (allocates, enqueues, waits).
  * Requires bits 2, 3, 4 or 8 (SI_ERR_UNSUPPORTED otherwise), group a power
  * of two >= 8 dividing d, d % 64 == 0 (d % 128 == 0 for bits = 3),
- * d <= 4096. */
+ * d <= 32768; the tiered down-projection calls need d <= 4096 (an encoding
+ * of Wg / Wu for spax_gate_up has d = N neurons). */
 int spax_encode(const uint16_t *Wd, int d, int N, int bits, int group, spax_layer **out,
                 void *stream);
 
@@ -427,6 +428,36 @@ int spax_ffn_decode(spax_layer *layer, const uint16_t *Wg, const uint16_t *Wu,
 int spax_select_decode(spax_layer *layer, const uint16_t *Wg, const uint16_t *Wu, const int32_t *rows,
                        int n_rows, const uint16_t *x, double top_frac, double mid_frac, float *y,
                        float *a_out, void *stream);
+
+/* SpAx tiers on the gate/up projections by |x| ([SPAX] Table 1 "ALL":
+ * every offloaded projection tiered; the FFN part adds gate and up to the
+ * down projection; Table 2 "SpAx-ALL"). Input channel j (column j of Wg and
+ * of Wu) is ranked by |x_j| (ties to the lower index): the k_top =
+ * si_count(top_frac, d) largest are read in bf16, the next k_mid =
+ * si_count(mid_frac, d) are rebuilt from their own b-bit codes (Fig. 3), the
+ * rest are skipped:
+ *   g = sum_{j in top} x_j Wg[:, j] + sum_{j in mid} x_j w^_j,  u likewise,
+ *   a[n] = silu(g[n]) * u[n].
+ * gate / up: made by spax_encode on Wg / Wu read as [N x d] matrices
+ * (spax_encode(Wg, N, d, bits, group, ...): rows = neurons, columns = input
+ * channels), same shape, bits and group; N % 4 == 0, d <= 8192.
+ *   x bf16 [d]; a fp32 [N] (written); top_idx / mid_idx (optional, may be
+ *   NULL) int32 [k_top] / [k_mid] receive the channel tiers, ascending.
+ * Requires top_frac, mid_frac >= 0, top_frac + mid_frac <= 1. */
+int spax_gate_up(const spax_layer *gate, const spax_layer *up, const uint16_t *x, double top_frac,
+                 double mid_frac, float *a, int32_t *top_idx, int32_t *mid_idx, void *stream);
+
+/* One SpAx-ALL decode token for the FFN ([SPAX] Table 1 "ALL"): spax_gate_up
+ * with the input-channel fractions in_top_frac / in_mid_frac, then
+ * spax_tiered_down on its a with top_frac / mid_frac over the N neurons (two
+ * kernels; the gate/up pass also counts the down tiers' histogram).
+ *   down: spax_encode of Wd [d x N] (d <= 4096); gate / up as for
+ *   spax_gate_up, with rows = the down encoding's columns (N) and columns =
+ *   its rows (d). y fp32 [d] (overwritten, deterministic); a_out (optional)
+ *   fp32 [N] receives a. Calls on one down handle go on one stream. */
+int spax_all_decode(spax_layer *down, const spax_layer *gate, const spax_layer *up, const uint16_t *x,
+                    double in_top_frac, double in_mid_frac, double top_frac, double mid_frac, float *y,
+                    float *a_out, void *stream);
 
 #ifdef __cplusplus
 }

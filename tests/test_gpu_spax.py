@@ -212,3 +212,69 @@ def test_spax_select_decode(si, d, N, frac, top, mid, bits, llama8b_layer):
     ref2 = oracle.spax_down(a_ref, Wd, codes, params, rt2, rm2, bits=bits)
     assert rel_err(y.numpy(), ref2) <= TOL
     layer.close()
+
+
+# ------------------------------------------- tiers on gate/up by |x| ("ALL")
+
+
+def _tie_heavy_x(seed, d, levels=12):
+    # bf16 inputs whose magnitudes take few values: many ties at the tier boundaries
+    u = synth.uniform(seed, 0, 0, d)
+    v = (np.floor(u * levels) - levels / 2 + 0.5) / 4.0
+    return synth.to_bf16_bits(v)
+
+
+@pytest.mark.parametrize("d,N,top,mid,bits,ties", [(4096, 14336, 0.3, 0.3, 4, False), (4096, 14336, 0.2, 0.5, 2, True),
+                                                   (256, 512, 0.3, 0.3, 8, False), (256, 512, 0.25, 0.5, 3, True),
+                                                   (256, 512, 1.0, 0.0, 4, False), (256, 512, 0.0, 1.0, 4, True),
+                                                   (256, 512, 0.0, 0.0, 4, False), (512, 1024, 0.1, 0.0, 4, True)])
+def test_spax_gate_up_tiers(si, d, N, top, mid, bits, ties, llama8b_layer):
+    """Channel tiers by |x| bit-exact against the oracle (ties to the lower
+    index); a = silu(g) * u within 1e-5 of max|a| (fp32 sums of bf16 products
+    and of rebuilt weights)."""
+    if (d, N) == (4096, 14336):
+        Wg, Wu, _ = llama8b_layer
+    else:
+        Wg, Wu, _ = synth.layer_weights(60, 0, d, N)
+    x = _tie_heavy_x(61, d) if ties else synth.tokens(62, 0, synth.T_DECODE, 1, d)[0]
+    gate = si.spax_encode_rows(dev_bf16(Wg), bits, 128)
+    upe = si.spax_encode_rows(dev_bf16(Wu), bits, 128)
+    k_top, k_mid = si.si_count(top, d), si.si_count(mid, d)
+    a = Guarded((N,), torch().float32, fill=float("nan"))
+    t_out = Guarded((max(k_top, 1),), torch().int32, fill=-1)
+    m_out = Guarded((max(k_mid, 1),), torch().int32, fill=-1)
+    si.spax_gate_up(gate, upe, dev_bf16(x), top, mid, a.t, t_out.t if k_top else None, m_out.t if k_mid else None)
+    got = a.numpy()
+    ref, rt, rm = oracle.spax_gate_up(x, Wg, Wu, top, mid, bits=bits, group=128)
+    assert np.array_equal(t_out.numpy()[:k_top], rt)
+    assert np.array_equal(m_out.numpy()[:k_mid], rm)
+    scale = max(np.max(np.abs(ref)), 1e-30)
+    assert np.max(np.abs(got - ref)) <= 1e-5 * scale
+    gate.close()
+    upe.close()
+
+
+def test_spax_all_decode_llama8b(si, llama8b_layer):
+    """One SpAx-ALL token (Llama-3.1-8B layer): channel tiers 30 % / 30 % by |x|
+    on gate/up, then neuron tiers 30 % / 30 % by |a| on the down projection;
+    y within the FFN tolerance of the oracle's token."""
+    Wg, Wu, Wd = llama8b_layer
+    d, N = 4096, 14336
+    gate = si.spax_encode_rows(dev_bf16(Wg), 4, 128)
+    upe = si.spax_encode_rows(dev_bf16(Wu), 4, 128)
+    down = si.spax_encode(dev_bf16(Wd), 4, 128)
+    codes, params = oracle.spax_encode(Wd, 4, 128)
+    for tok in range(2):   # twice: the down tiers' histogram is left clean for the next token
+        x = synth.tokens(63, tok, synth.T_DECODE, 1, d)[0]
+        y = Guarded((d,), torch().float32, fill=float("nan"))
+        a = Guarded((N,), torch().float32, fill=float("nan"))
+        si.spax_all_decode(down, gate, upe, dev_bf16(x), 0.3, 0.3, 0.3, 0.3, y.t, a.t)
+        a_ref, _, _ = oracle.spax_gate_up(x, Wg, Wu, 0.3, 0.3)
+        assert np.max(np.abs(a.numpy() - a_ref)) <= 1e-5 * np.max(np.abs(a_ref))
+        a32 = a_ref.astype(np.float32)
+        rt, rm = oracle.spax_tiers(a32, si.si_count(0.3, N), si.si_count(0.3, N))
+        y_ref = oracle.spax_down(a32, Wd, codes, params, rt, rm)
+        assert rel_err(y.numpy(), y_ref) <= TOL
+    down.close()
+    gate.close()
+    upe.close()
