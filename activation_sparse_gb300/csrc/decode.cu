@@ -511,9 +511,13 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_sparse_decode_b1(SparseDecod
 
 // --------------------------------------------------------------- dense act
 
+constexpr int kDensePfRows = 256;   // rows per CTA up to which the prefetch ranks them
+constexpr int kDensePfMargin = 2;   // extra ranks prefetched on each side of a tier boundary
+
 template <int MAXC>
 __global__ void __launch_bounds__(kDecThreads, 1) k_dense_act(DenseActParams P) {
     extern __shared__ __align__(1024) uint8_t smem[];
+    __shared__ float s_pf[kDensePfRows];  // this CTA's a values, for the optional prefetch
     const int d = P.d;
     const RingLayout L = ring_layout(P.R, 4 * d, 0, d * 2);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.off_full);
@@ -613,6 +617,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_dense_act(DenseActParams P) 
             if (lane == 0) {
                 const float av = swiglu(g, u);
                 P.a[row(i)] = av;
+                if (i < kDensePfRows) s_pf[i] = av;
                 mbar_arrive(&empty[s]);
                 if (P.hist) {
                     if (P.slab) {
@@ -627,6 +632,25 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_dense_act(DenseActParams P) 
             }
         }
         if (lane == 0 && pend_pos < (uint32_t)kSlabCap) P.slab[(size_t)pend_bin * kSlabCap + pend_pos] = pend_n;
+    }
+    if (!P.pf_WdT || cnt > kDensePfRows) return;  // the same decision in every thread
+    __syncthreads();
+    // local rank of each row's |a| (ties to the lower row), against this CTA's
+    // share of each tier, widened by kDensePfMargin ranks on both sides
+    const int total_rows = P.rows ? P.n_rows : P.N;
+    const int T = (int)(((long long)P.pf_k_top * cnt + total_rows / 2) / total_rows);
+    const int M = (int)(((long long)P.pf_k_mid * cnt + total_rows / 2) / total_rows);
+    for (int t = threadIdx.x; t < cnt; t += blockDim.x) {
+        const uint32_t kt = abs_key(s_pf[t]);
+        int rank = 0;
+        for (int j = 0; j < cnt; ++j) {
+            const uint32_t kj = abs_key(s_pf[j]);
+            rank += (kj > kt) || (kj == kt && j < t);
+        }
+        const size_t n = (size_t)row(t);
+        if (P.pf_k_top > 0 && rank < T + kDensePfMargin) prefetch_l2(P.pf_WdT + n * d, row_bytes);
+        if (P.pf_k_mid > 0 && rank >= T - kDensePfMargin && rank < T + M + kDensePfMargin)
+            prefetch_l2(P.pf_codes + n * (size_t)P.pf_rec_bytes, (uint32_t)P.pf_rec_bytes);
     }
 }
 
@@ -668,7 +692,11 @@ __global__ void __launch_bounds__(256) k_abs_hist(const float* __restrict__ a, i
 // give the exact key `thr` and how many keys equal to it are taken. The
 // CTA then counts the members of each tier in index order and takes its
 // window of ranks of both tiers (balanced over the CTAs).
-constexpr int kTDW = kDecThreads / 32;  // warps of the tiered kernel
+constexpr int kTdThreads = 256;          // threads of the tiered kernel: eight warps
+constexpr int kTDW = kTdThreads / 32;    // warps of the tiered kernel
+constexpr int kTdSplit = 1;              // warps that share a record, each a slice of its rows
+constexpr int kTdPairs = kTDW / kTdSplit;  // record streams (one per group of kTdSplit warps)
+constexpr int kTdSlots = 16;             // records in flight per stream at most (one barrier pair each)
 
 // Exclusive scan over the CTA's warps of two per-warp counts (the same value
 // in every lane of a warp); gives the warp's offsets and the CTA totals.
@@ -779,10 +807,10 @@ __device__ __forceinline__ void tier_windows(const TieredDownParams& P, ValF ava
     // keys are read eight at a time ahead of the atomics (which the compiler
     // cannot move loads across); 0xFFFFFFFF pads past the end and matches no bin
     if (act[0] || act[1])
-        for (int i0 = tid; i0 < N; i0 += 8 * kDecThreads) {
+        for (int i0 = tid; i0 < N; i0 += 8 * kTdThreads) {
             uint32_t kv[8];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) kv[u] = i0 + u * kDecThreads < N ? key(i0 + u * kDecThreads) : 0xFFFFFFFFu;
+            for (int u = 0; u < 8; ++u) kv[u] = i0 + u * kTdThreads < N ? key(i0 + u * kTdThreads) : 0xFFFFFFFFu;
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
                 const uint32_t top = kv[u] >> kTierShift, b = (kv[u] >> 9) & 2047u;
@@ -797,10 +825,10 @@ __device__ __forceinline__ void tier_windows(const TieredDownParams& P, ValF ava
     for (int i = tid; i < 2 * kTierBins; i += blockDim.x) (&s_hist[0][0])[i] = 0u;
     __syncthreads();
     if (act[0] || act[1])
-        for (int i0 = tid; i0 < N; i0 += 8 * kDecThreads) {
+        for (int i0 = tid; i0 < N; i0 += 8 * kTdThreads) {
             uint32_t kv[8];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) kv[u] = i0 + u * kDecThreads < N ? key(i0 + u * kDecThreads) : 0xFFFFFFFFu;
+            for (int u = 0; u < 8; ++u) kv[u] = i0 + u * kTdThreads < N ? key(i0 + u * kTdThreads) : 0xFFFFFFFFu;
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
                 const uint32_t b = kv[u] & 511u;
@@ -986,8 +1014,24 @@ __device__ bool tier_own_range(const TieredDownParams& P, const float* s_a, int*
     if (P.slab && !zero_bin && h0 <= (uint32_t)kSlabCap && h1 <= (uint32_t)kSlabCap && h0 + h1 <= (uint32_t)cap) {
         C = h0 + h1;
         const uint32_t b0 = act[0] ? d0[0] : d0[1];  // the first list's bin
-        for (uint32_t c = (uint32_t)tid; c < C; c += blockDim.x)
-            cand[c] = __ldcg(P.slab + (c < h0 ? (size_t)b0 * kSlabCap + c : (size_t)d0[1] * kSlabCap + (c - h0)));
+        auto slot = [&](uint32_t c) -> size_t {
+            return c < h0 ? (size_t)b0 * kSlabCap + c : (size_t)d0[1] * kSlabCap + (c - h0);
+        };
+        // eight loads in flight per thread before any store (C <= 2 * kSlabCap:
+        // one round trip for up to 8 * 288 candidates)
+        for (uint32_t c0 = (uint32_t)tid; c0 < C; c0 += 8u * blockDim.x) {
+            int v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const uint32_t c = c0 + (uint32_t)u * blockDim.x;
+                v[u] = c < C ? __ldcg(P.slab + slot(c)) : 0;
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const uint32_t c = c0 + (uint32_t)u * blockDim.x;
+                if (c < C) cand[c] = v[u];
+            }
+        }
         __syncthreads();
     } else {
         uint32_t n = 0u;
@@ -1083,30 +1127,58 @@ __device__ bool tier_own_range(const TieredDownParams& P, const float* s_a, int*
     return true;
 }
 
+// Shared-memory layout of the tiered kernel: per record stream kTdSlots
+// "full" and "empty" barriers, the activation / column buffer, then the ring
+// (ring_bytes, the CTA's sum of y in its last 4d bytes).
+__host__ __device__ inline int td_off_aux() { return round_up(16 * kTdPairs * kTdSlots, 128); }
+__host__ __device__ inline int td_off_ring(int aux_floats) { return td_off_aux() + round_up(aux_floats * 4, 128); }
+
+// The eight 4-bit codes of a 32-bit word (element i at bits 4i) as the floats
+// 1 + q / 16 (exact: q sits in the top mantissa bits of 1.0f), in element
+// pairs: element 2m is the low nibble of byte m, 2m + 1 the high one.
+__device__ __forceinline__ void codes4_unit(uint32_t q, float2 (&w)[4]) {
+    const uint32_t lo = ((q << 3) & 0x78787878u) | 0x80808080u;  // byte m: 0x80 | low nibble << 3
+    const uint32_t hi = ((q >> 1) & 0x78787878u) | 0x80808080u;  // byte m: 0x80 | high nibble << 3
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+        const uint32_t sel = 0x7044u | ((uint32_t)m << 8);  // bytes: 0, 0, lo/hi byte m, 0x3F
+        w[m] = make_float2(__uint_as_float(__byte_perm(lo, 0x3F000000u, sel)),
+                           __uint_as_float(__byte_perm(hi, 0x3F000000u, sel)));
+    }
+}
+
 // SpAx tiered down-projection (abstract, Fig. 2; middle columns rebuilt from
 // their codes as in Fig. 3): y = sum over Top of a_n Wd[:, n] + sum over Mid
-// of a_n (min_g + q * scale_g). Each CTA takes an even share of both tier
-// lists. Record i of the CTA (its top columns first, then its middle ones)
-// goes to consumer warp i % 8 and ring stage i % R, R a multiple of 8, so a
-// stage always belongs to one warp; each warp keeps its own partial of y in
-// registers (lane l holds chunks l + 32 j of 8 columns). The partials meet
-// in shared memory at the end and the CTAs' sums are reduced through the
-// cluster and a fixed-order final pass (deterministic).
-template <int MAXC, int BITS>
-__global__ void __launch_bounds__(kDecThreads, 1) k_tiered_down(TieredDownParams P) {
+// of a_n (min_g + q * scale_g). Each CTA takes its own index range (or an
+// even share of both tier lists), its top columns first, then its middle
+// ones. Record i goes to stream i % S (S = 8 / kTdSplit streams of kTdSplit
+// warps): each warp of the stream reads it, a slice of the d rows each (lane
+// l: chunks l + 32 j of 8 rows of the slice). The stream's first warp issues
+// the stream's copies into the stream's own byte ring, records back to back
+// at their own size (a bf16 column 2d bytes, a code record rec_bytes), and
+// reuses bytes once every warp of the stream has released them. The
+// streams' partials meet in shared memory at the end (summed in stream
+// order) and the CTAs' sums are reduced through the cluster and a
+// fixed-order final pass (deterministic). FULL: d == 2048 * MAXC, every
+// lane's chunks exist (no bounds checks in the per-record code).
+template <int MAXC, int BITS, bool FULL>
+__global__ void __launch_bounds__(kTdThreads, 1) k_tiered_down(TieredDownParams P) {
     extern __shared__ __align__(1024) uint8_t smem[];
     const int d = P.d;
     const int mid_bytes = P.rec_bytes;  // d * BITS / 8 code bytes, then ngp (scale, min) pairs
-    const RingLayout L = ring_layout(P.R, 2 * d, P.aux_floats * 4, 0);
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.off_full);
-    uint64_t* empty = reinterpret_cast<uint64_t*>(smem + L.off_empty);
-    float* s_av = reinterpret_cast<float*>(smem + L.off_aux);
-    uint8_t* ring = smem + L.off_ring;
-    const int R = L.R;
-    // the host never launches a ring without warp-owned stages or without room
-    // for the eight warp partials and the CTA sum; refuse one
-    if (R < kConsWarps || R % kConsWarps ||
-        (long long)R * L.stage < (long long)kConsWarps * ((d + 255) / 256) * 1024 + 4LL * d) {
+    uint64_t* full_all = reinterpret_cast<uint64_t*>(smem);
+    uint64_t* empty_all = full_all + kTdPairs * kTdSlots;
+    float* s_av = reinterpret_cast<float*>(smem + td_off_aux());
+    uint8_t* ring = smem + td_off_ring(P.aux_floats);
+    const int ring_bytes = P.ring_bytes;
+    // each stream's ring (records only; the CTA sum of y follows them)
+    const int RP = ((ring_bytes - 4 * d) / kTdPairs) / 128 * 128;
+    float* ycta = reinterpret_cast<float*>(ring + ring_bytes) - d;
+    // a stream's ring holds one record of either kind, the streams' partials
+    // and the CTA sum fit the ring, a slice's chunks fit 8 * MAXC / kTdSplit
+    // per lane; refuse a launch where they do not (the host never makes one)
+    if (RP < 2 * d || RP < mid_bytes || (mid_bytes & 15) || (d % (8 * kTdSplit)) || d > 2048 * MAXC ||
+        (FULL && d != 2048 * MAXC) || (long long)ring_bytes < (4LL * kTdPairs + 4) * d) {
         if (threadIdx.x == 0) atomicOr(P.err, SI_DEVERR_COUNT);
         return;
     }
@@ -1118,13 +1190,11 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_tiered_down(TieredDownParams
     const int m1 = (int)((long long)P.k_mid * (blockIdx.x + 1) / gridDim.x);
     const int n0 = (int)((long long)P.N * blockIdx.x / gridDim.x);
     const int n1 = (int)((long long)P.N * (blockIdx.x + 1) / gridDim.x);
-    constexpr int XJ = 8 * MAXC;  // 16-byte chunks of a bf16 column per lane
-    const int nch = d / 8;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < R; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1);
+        for (int b = 0; b < kTdPairs * kTdSlots; ++b) {
+            mbar_init(&full_all[b], 1);
+            mbar_init(&empty_all[b], kTdSplit);
         }
         fence_mbar_init();
     }
@@ -1141,8 +1211,9 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_tiered_down(TieredDownParams
     int* s_col = reinterpret_cast<int*>(s_av + P.aux_floats / 2);
     // a is staged in the ring when it fits (the ring is idle until streaming):
     // one bulk copy when a is 16-byte aligned and sized, else vector loads
+    const int RB = kTdPairs * RP;
     float* s_a = reinterpret_cast<float*>(ring);
-    const bool staged = (long long)N * 4 <= (long long)R * L.stage;
+    const bool staged = (long long)N * 4 <= (long long)RB;
     const bool bulk = staged && (N % 4) == 0 && (reinterpret_cast<uintptr_t>(P.a) & 15) == 0;
     if (bulk && tid == 0) {
         mbar_init(&s_stage_bar, 1);
@@ -1161,7 +1232,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_tiered_down(TieredDownParams
     bool own = false;
     if (staged && !P.top_out && !P.mid_out) {
         const long long off = ((long long)N * 4 + 15) / 16 * 16;
-        const long long cap = ((long long)R * L.stage - off) / 4;
+        const long long cap = ((long long)RB - off) / 4;
         own = tier_own_range(P, s_a, reinterpret_cast<int*>(ring + off), (int)(cap < N ? cap : N), n0, n1, s_col,
                              s_av, s_hist, s_w, s_state, s_n);
         __syncthreads();
@@ -1187,165 +1258,190 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_tiered_down(TieredDownParams
     }
     __syncthreads();  // the records are in place and the staged keys are no longer read
 
-    if (warp == kConsWarps) {
-        // kIssueLanes lanes issue the copies, lane l the records l, l + 8, ...
-        // (R is a multiple of 8, so every stage is filled by one lane, in
-        // order): one lane alone cannot keep the small middle-column copies
-        // flowing.
-        constexpr int kIssueLanes = 8;
-        if (lane < kIssueLanes) {
-            const uint64_t pol = policy_evict_first();
-            for (int i = lane; i < nrec; i += kIssueLanes) {
-                const int s = i % R;
-                if (i >= R) mbar_wait(&empty[s], (uint32_t)((i / R - 1) & 1), P.err, kSiteTiered | kSiteEmpty);
-                uint8_t* dst = ring + (size_t)s * L.stage;
-                int ci = s_col[i];
-                if (ci < 0 || ci >= P.N) {  // never read outside the encoded buffers
-                    atomicOr(P.err, SI_DEVERR_COUNT);
-                    ci = 0;
-                }
-                const size_t col = (size_t)ci;
-                if (i < ntop) {
-                    mbar_arrive_expect_tx(&full[s], (uint32_t)(2 * d));
-                    bulk_g2s_hint(dst, P.WdT + col * d, (uint32_t)(2 * d), &full[s], pol);
-                } else {
-                    mbar_arrive_expect_tx(&full[s], (uint32_t)mid_bytes);
-                    bulk_g2s_hint(dst, P.codes + col * P.rec_bytes, (uint32_t)P.rec_bytes, &full[s], pol);
+    constexpr int JH = 8 * MAXC / kTdSplit;  // chunks per lane in a slice
+    const int pair = warp / kTdSplit, half = warp % kTdSplit;  // stream, slice
+    const int nch = d / 8, hch = nch / kTdSplit;  // chunks of a column, of a slice
+    const int cbase = half * hch;                 // this warp's first chunk
+    float2 acc[JH][4];
+    float amin[JH];
+#pragma unroll
+    for (int j = 0; j < JH; ++j) {
+        amin[j] = 0.0f;
+#pragma unroll
+        for (int m = 0; m < 4; ++m) acc[j][m] = make_float2(0.0f, 0.0f);
+    }
+    {
+        uint8_t* reg = ring + (size_t)pair * RP;
+        uint64_t* full = full_all + pair * kTdSlots;
+        uint64_t* empty = empty_all + pair * kTdSlots;
+        const int nw = nrec > pair ? (nrec - pair + kTdPairs - 1) / kTdPairs : 0;  // the stream's records
+        const int gshift = 31 - __clz(P.group);  // group is a power of two (checked by the host)
+        auto rec_size = [&](int k) -> uint32_t {
+            return pair + kTdPairs * k < ntop ? (uint32_t)(2 * d) : (uint32_t)mid_bytes;
+        };
+        // Placement in the stream's ring: a running position and offset; a
+        // record that would run past the ring's end starts at its beginning.
+        // Issuer and consumers replay the same sequence.
+        struct Cursor {
+            uint32_t mono, off;  // monotonic byte position, its offset in the ring
+        };
+        auto place = [&](Cursor& c, uint32_t sz) -> uint32_t {
+            if (c.off + sz > (uint32_t)RP) {
+                c.mono += (uint32_t)RP - c.off;
+                c.off = 0u;
+            }
+            const uint32_t at = c.off;
+            c.mono += sz;
+            c.off += sz;
+            return at;
+        };
+        const bool issuer = half == 0 && lane == 0;
+        const uint64_t pol = policy_evict_first();
+        Cursor head = {0u, 0u}, rel = {0u, 0u}, cons = {0u, 0u};
+        int ki = 0, jr = 0;  // records issued, records known released (issuer only)
+        for (int k = 0; k < nw; ++k) {
+            if (issuer) {
+                while (ki < nw) {
+                    const uint32_t sz = rec_size(ki);
+                    Cursor h2 = head;
+                    const uint32_t at = place(h2, sz);
+                    const bool fits = ki - jr < kTdSlots && (jr == ki || h2.mono - rel.mono <= (uint32_t)RP);
+                    if (fits) {
+                        const int i = pair + kTdPairs * ki;
+                        int ci = s_col[i];
+                        if (ci < 0 || ci >= N) {  // never read outside the encoded buffers
+                            atomicOr(P.err, SI_DEVERR_COUNT);
+                            ci = 0;
+                        }
+                        const size_t col = (size_t)ci;
+                        const void* src = i < ntop ? static_cast<const void*>(P.WdT + col * d)
+                                                   : static_cast<const void*>(P.codes + col * (size_t)P.rec_bytes);
+                        mbar_arrive_expect_tx(&full[ki % kTdSlots], sz);
+                        bulk_g2s_hint(reg + at, src, sz, &full[ki % kTdSlots], pol);
+                        head = h2;
+                        ++ki;
+                        continue;
+                    }
+                    if (jr >= k) break;  // nothing this warp has consumed is still unreleased
+                    // record jr: this warp is done with it; take its release when
+                    // the stream's other warps have released it too (wait only if
+                    // record k itself still needs the room)
+                    const uint32_t par = (uint32_t)((jr / kTdSlots) & 1);
+                    if (ki > k) {
+                        if (!mbar_test_wait(&empty[jr % kTdSlots], par)) break;
+                    } else if (!mbar_wait(&empty[jr % kTdSlots], par, P.err, kSiteTiered | kSiteEmpty)) {
+                        break;
+                    }
+                    place(rel, rec_size(jr));
+                    ++jr;
                 }
             }
-        }
-        __syncwarp();
-    } else {
-        // amin: the middle columns' a * min terms, equal over a chunk; kept apart
-        // only where registers allow (nine warps leave 168 per thread)
-        constexpr bool kSepMin = (MAXC == 1);
-        float acc[XJ][8], amin[XJ];
-#pragma unroll
-        for (int j = 0; j < XJ; ++j) {
-            amin[j] = 0.0f;
-#pragma unroll
-            for (int e = 0; e < 8; ++e) acc[j][e] = 0.0f;
-        }
-        const int gshift = 31 - __clz(P.group);  // group is a power of two (checked by the host)
-        for (int i = warp; i < nrec; i += kConsWarps) {
-            const int s = i % R;
-            mbar_wait(&full[s], (uint32_t)((i / R) & 1), P.err, kSiteTiered | kSiteFull);
-            const uint8_t* st = ring + (size_t)s * L.stage;
+            const int i = pair + kTdPairs * k;
+            const uint32_t at = place(cons, rec_size(k));
+            mbar_wait(&full[k % kTdSlots], (uint32_t)((k / kTdSlots) & 1), P.err, kSiteTiered | kSiteFull);
+            const uint8_t* st = reg + at;
             const float av = s_av[i];
             if (i < ntop) {
+                const float2 a2 = make_float2(av, av);
 #pragma unroll
-                for (int j = 0; j < XJ; ++j) {
+                for (int j = 0; j < JH; ++j) {
                     const int c = lane + 32 * j;
-                    if (c < nch) {
+                    if (FULL || c < hch) {
                         float f[8];
-                        unpack8(reinterpret_cast<const uint4*>(st)[c], f);
+                        unpack8(reinterpret_cast<const uint4*>(st)[cbase + c], f);
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) acc[j][e] = fmaf(av, f[e], acc[j][e]);
+                        for (int m = 0; m < 4; ++m) acc[j][m] = __ffma2_rn(a2, make_float2(f[2 * m], f[2 * m + 1]), acc[j][m]);
                     }
                 }
             } else {
                 const float2* prm = reinterpret_cast<const float2*>(st + (d * BITS) / 8);
 #pragma unroll
-                for (int j = 0; j < XJ; ++j) {
+                for (int j = 0; j < JH; ++j) {
                     const int c = lane + 32 * j;
-                    if (c < nch) {
-                        const float2 sm = prm[(8 * c) >> gshift];  // (scale, min)
-                        const float c1 = av * sm.x, c0 = av * sm.y;
-                        if constexpr (kSepMin) amin[j] += c0;
-                        // acc += c1 * code (+ c0 unless it is kept apart); a code
-                        // arrives as the float bits of 2^23 + code, exact for
-                        // codes below 2^23, and 2^23 is subtracted
-                        auto mac = [&](float& acc_e, uint32_t word) {
-                            const float qf = __uint_as_float(word) - 8388608.0f;
-                            if constexpr (kSepMin) acc_e = fmaf(c1, qf, acc_e);
-                            else acc_e = fmaf(c1, qf, acc_e + c0);
-                        };
-                        // the eight codes of chunk c: element i at bit i * BITS
+                    if (FULL || c < hch) {
+                        const int cc = cbase + c;
+                        const float2 sm = prm[(8 * cc) >> gshift];  // (scale, min)
                         if constexpr (BITS == 4) {
-                            // elements 0,2,4,6 in the low nibbles, 1,3,5,7 in the high ones
-                            const uint32_t q = reinterpret_cast<const uint32_t*>(st)[c];
-                            const uint32_t lo = q & 0x0F0F0F0Fu, hi = (q >> 4) & 0x0F0F0F0Fu;
-                            mac(acc[j][0], __byte_perm(lo, 0x4B000000u, 0x7440));
-                            mac(acc[j][1], __byte_perm(hi, 0x4B000000u, 0x7440));
-                            mac(acc[j][2], __byte_perm(lo, 0x4B000000u, 0x7441));
-                            mac(acc[j][3], __byte_perm(hi, 0x4B000000u, 0x7441));
-                            mac(acc[j][4], __byte_perm(lo, 0x4B000000u, 0x7442));
-                            mac(acc[j][5], __byte_perm(hi, 0x4B000000u, 0x7442));
-                            mac(acc[j][6], __byte_perm(lo, 0x4B000000u, 0x7443));
-                            mac(acc[j][7], __byte_perm(hi, 0x4B000000u, 0x7443));
-                        } else if constexpr (BITS == 8) {
-                            // one byte per element
-                            const uint2 q = reinterpret_cast<const uint2*>(st)[c];
-                            mac(acc[j][0], __byte_perm(q.x, 0x4B000000u, 0x7440));
-                            mac(acc[j][1], __byte_perm(q.x, 0x4B000000u, 0x7441));
-                            mac(acc[j][2], __byte_perm(q.x, 0x4B000000u, 0x7442));
-                            mac(acc[j][3], __byte_perm(q.x, 0x4B000000u, 0x7443));
-                            mac(acc[j][4], __byte_perm(q.y, 0x4B000000u, 0x7440));
-                            mac(acc[j][5], __byte_perm(q.y, 0x4B000000u, 0x7441));
-                            mac(acc[j][6], __byte_perm(q.y, 0x4B000000u, 0x7442));
-                            mac(acc[j][7], __byte_perm(q.y, 0x4B000000u, 0x7443));
-                        } else if constexpr (BITS == 3) {
-                            // 24 bits per chunk, in bytes 3c .. 3c + 2; element e at bits 3e .. 3e + 2
-                            const uint8_t* b3 = st + 3 * c;
-                            const uint32_t q = (uint32_t)b3[0] | ((uint32_t)b3[1] << 8) | ((uint32_t)b3[2] << 16);
+                            // codes as 1 + q / 16: a (min + q scale) = 16 a scale (1 + q / 16) + a (min - 16 scale)
+                            const float c1 = (16.0f * av) * sm.x;
+                            amin[j] += fmaf(av, sm.y, -c1);
+                            const float2 c2 = make_float2(c1, c1);
+                            float2 w[4];
+                            codes4_unit(reinterpret_cast<const uint32_t*>(st)[cc], w);
 #pragma unroll
-                            for (int e = 0; e < 8; ++e) mac(acc[j][e], 0x4B000000u | ((q >> (3 * e)) & 7u));
+                            for (int m = 0; m < 4; ++m) acc[j][m] = __ffma2_rn(c2, w[m], acc[j][m]);
                         } else {
-                            // BITS == 2: sixteen bits per chunk, element e at bits 2e, 2e + 1
-                            const uint32_t q = reinterpret_cast<const uint16_t*>(st)[c];
+                            const float c1 = av * sm.x;
+                            amin[j] = fmaf(av, sm.y, amin[j]);
+                            // a code arrives as the float bits of 2^23 + code,
+                            // exact for codes below 2^23, and 2^23 is subtracted
+                            uint32_t wd[8];
+                            if constexpr (BITS == 8) {
+                                // one byte per element
+                                const uint2 q = reinterpret_cast<const uint2*>(st)[cc];
 #pragma unroll
-                            for (int e = 0; e < 8; ++e) mac(acc[j][e], 0x4B000000u | ((q >> (2 * e)) & 3u));
+                                for (int e = 0; e < 4; ++e) {
+                                    wd[e] = __byte_perm(q.x, 0x4B000000u, 0x7440u | (uint32_t)e);
+                                    wd[4 + e] = __byte_perm(q.y, 0x4B000000u, 0x7440u | (uint32_t)e);
+                                }
+                            } else if constexpr (BITS == 3) {
+                                // 24 bits per chunk, in bytes 3c .. 3c + 2; element e at bits 3e .. 3e + 2
+                                const uint8_t* b3 = st + 3 * cc;
+                                const uint32_t q = (uint32_t)b3[0] | ((uint32_t)b3[1] << 8) | ((uint32_t)b3[2] << 16);
+#pragma unroll
+                                for (int e = 0; e < 8; ++e) wd[e] = 0x4B000000u | ((q >> (3 * e)) & 7u);
+                            } else {
+                                // BITS == 2: sixteen bits per chunk, element e at bits 2e, 2e + 1
+                                const uint32_t q = reinterpret_cast<const uint16_t*>(st)[cc];
+#pragma unroll
+                                for (int e = 0; e < 8; ++e) wd[e] = 0x4B000000u | ((q >> (2 * e)) & 3u);
+                            }
+                            const float2 c2 = make_float2(c1, c1);
+#pragma unroll
+                            for (int m = 0; m < 4; ++m)
+                                acc[j][m] = __ffma2_rn(c2, make_float2(__uint_as_float(wd[2 * m]) - 8388608.0f,
+                                                                       __uint_as_float(wd[2 * m + 1]) - 8388608.0f),
+                                                       acc[j][m]);
                         }
                     }
                 }
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[s]);
+            if (lane == 0) mbar_arrive(&empty[k % kTdSlots]);
         }
-        // All records consumed: warp w's partial goes to ring region w
-        // (round_up(d, 256) floats; for chunk j the lanes' first halves, then
-        // their second halves, so the stores are bank-conflict free), then
-        // each thread sums the eight partials of its float4 columns.
-        const int wstride = ((d + 255) / 256) * 64;  // float4s per warp region
-        named_bar_sync(1, kConsThreads);
-        float4* wst = reinterpret_cast<float4*>(ring) + (size_t)warp * wstride;
+    }
+    // All records consumed and every copy landed: the stream's partial goes
+    // to ring region `pair` (d floats; this warp writes its slice), then each
+    // thread sums its float4 columns over the streams in stream order.
+    __syncthreads();
+    {
+        float* part = reinterpret_cast<float*>(ring) + (size_t)pair * d;
 #pragma unroll
-        for (int j = 0; j < XJ; ++j) {
-            if constexpr (kSepMin)
-#pragma unroll
-                for (int e = 0; e < 8; ++e) acc[j][e] += amin[j];
-            if (32 * j < nch) {
-                wst[j * 64 + lane] = make_float4(acc[j][0], acc[j][1], acc[j][2], acc[j][3]);
-                wst[j * 64 + 32 + lane] = make_float4(acc[j][4], acc[j][5], acc[j][6], acc[j][7]);
+        for (int j = 0; j < JH; ++j) {
+            const int c = lane + 32 * j;
+            if (FULL || c < hch) {
+                float4* pc = reinterpret_cast<float4*>(part + 8 * (cbase + c));
+                pc[0] = make_float4(acc[j][0].x + amin[j], acc[j][0].y + amin[j], acc[j][1].x + amin[j],
+                                    acc[j][1].y + amin[j]);
+                pc[1] = make_float4(acc[j][2].x + amin[j], acc[j][2].y + amin[j], acc[j][3].x + amin[j],
+                                    acc[j][3].y + amin[j]);
             }
-        }
-        named_bar_sync(1, kConsThreads);
-        float4* part4 = reinterpret_cast<float4*>(ring);
-        float4 v[2 * MAXC];
-        constexpr int KV = 2 * MAXC;  // float4 columns per consumer thread
-#pragma unroll
-        for (int t = 0; t < KV; ++t) {
-            const int k = threadIdx.x + t * kConsThreads;
-            v[t] = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (k < d / 4) {
-                const int c = k >> 1, off = (c >> 5) * 64 + (k & 1) * 32 + (c & 31);
-#pragma unroll
-                for (int w = 0; w < kConsWarps; ++w) {
-                    const float4 u = part4[(size_t)w * wstride + off];
-                    v[t].x += u.x; v[t].y += u.y; v[t].z += u.z; v[t].w += u.w;
-                }
-            }
-        }
-        // the CTA sum goes to the tail of the ring, past the eight regions
-        float4* ysum = reinterpret_cast<float4*>(ring + (size_t)R * L.stage) - d / 4;
-#pragma unroll
-        for (int t = 0; t < KV; ++t) {
-            const int k = threadIdx.x + t * kConsThreads;
-            if (k < d / 4) ysum[k] = v[t];
         }
     }
     __syncthreads();
-    const float* ycta = reinterpret_cast<const float*>(ring + (size_t)R * L.stage) - d;
+    {
+        const float4* part4 = reinterpret_cast<const float4*>(ring);
+        for (int k = tid; k < d / 4; k += blockDim.x) {
+            float4 v = part4[k];
+#pragma unroll
+            for (int p = 1; p < kTdPairs; ++p) {
+                const float4 u = part4[(size_t)p * (d / 4) + k];
+                v.x += u.x; v.y += u.y; v.z += u.z; v.w += u.w;
+            }
+            reinterpret_cast<float4*>(ycta)[k] = v;
+        }
+    }
+    __syncthreads();
     cluster_ticket_reduce4(ycta, d, P.part, P.tickets, P.y);
     // every CTA read the histogram at its start; the last one to finish
     // re-zeroes it for the next token
@@ -1371,10 +1467,10 @@ constexpr int kSmemBudget = 227 * 1024 - 2048;  // dynamic budget, leaves room f
 // griddepcontrol.wait before it reads anything that grid may write).
 template <class K>
 cudaError_t launch_clustered(K kernel, int grid, int cluster, size_t smem, cudaStream_t st, void** args,
-                             bool pdl = false) {
+                             bool pdl = false, int threads = kDecThreads) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid, 1, 1);
-    cfg.blockDim = dim3(kDecThreads, 1, 1);
+    cfg.blockDim = dim3(threads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
     cudaLaunchAttribute attr[2];
@@ -1392,7 +1488,7 @@ cudaError_t launch_clustered(K kernel, int grid, int cluster, size_t smem, cudaS
 // Largest co-resident grid for a clustered streaming kernel: tries cluster
 // sizes 8, 4, 2 and keeps the one that puts the most CTAs on the GPU at once.
 template <class K>
-cudaError_t pick_grid(K kernel, size_t smem, int* grid, int* cluster) {
+cudaError_t pick_grid(K kernel, size_t smem, int* grid, int* cluster, int threads) {
     int dev = 0, sms = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -1406,7 +1502,7 @@ cudaError_t pick_grid(K kernel, size_t smem, int* grid, int* cluster) {
     for (int C = 16; C >= 2; C /= 2) {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3((sms / C) * C, 1, 1);
-        cfg.blockDim = dim3(kDecThreads, 1, 1);
+        cfg.blockDim = dim3(threads, 1, 1);
         cfg.dynamicSmemBytes = smem;
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -1446,7 +1542,7 @@ struct GridCache {
 };
 
 template <class K>
-cudaError_t cached_grid(K kernel, size_t smem, int* grid, int* cluster) {
+cudaError_t cached_grid(K kernel, size_t smem, int* grid, int* cluster, int threads = kDecThreads) {
     static thread_local GridCache cache[64];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -1458,7 +1554,7 @@ cudaError_t cached_grid(K kernel, size_t smem, int* grid, int* cluster) {
             *cluster = c.cluster;
             return cudaSuccess;
         }
-    e = pick_grid(kernel, smem, grid, cluster);
+    e = pick_grid(kernel, smem, grid, cluster, threads);
     if (e != cudaSuccess) return e;
     for (auto& c : cache)
         if (c.fn == nullptr) {
@@ -1593,27 +1689,24 @@ cudaError_t launch_dense_act(DenseActParams P, cudaStream_t st) {
     return launch_clustered(k_dense_act<1>, grid, 1, smem, st, args, /*pdl=*/true);
 }
 
-// Stages of the tiered ring: a multiple of the consumer-warp count (each
-// stage belongs to one warp), and enough ring for the eight warp partials
-// (round_up(d, 256) floats each) plus the CTA sum (d floats) at its tail.
-int tiered_down_stages(int d, int aux_floats) {
+// Bytes of the tiered kernel's ring: what is left of the shared memory after
+// the barriers and the activation buffer, the CTA sum of y (4d bytes) at its
+// end. 0 when a stream's share cannot hold one record of either kind, or the
+// ring the streams' partials and the CTA sum.
+int tiered_down_ring(int d, int aux_floats, int rec_bytes) {
     // the kernel's static shared memory (tier histograms, reduction scratch)
     // takes about 21 KB of the 227 KB
     constexpr int kTieredBudget = 227 * 1024 - 24 * 1024;
-    const int stage = round_up(2 * d, 128);
-    const long long need = (long long)kConsWarps * round_up(d, 256) * 4 + 4LL * d;
-    int R = (int)((need + stage - 1) / stage);  // at least the tail's bytes
-    if (R < 32) R = 32;                           // up to 32 stages of look-ahead
-    R = ((R + kConsWarps - 1) / kConsWarps) * kConsWarps;
-    while (R >= kConsWarps && ring_layout(R, 2 * d, aux_floats * 4, 0).total > kTieredBudget) R -= kConsWarps;
-    return (R >= kConsWarps && (long long)R * stage >= need) ? R : 0;
+    const int bytes = (kTieredBudget - td_off_ring(aux_floats)) / 1024 * 1024;
+    const int RP = ((bytes - 4 * d) / kTdPairs) / 128 * 128;
+    return (RP >= 2 * d && RP >= rec_bytes && bytes >= (4 * kTdPairs + 4) * d) ? bytes : 0;
 }
 
-template <int MAXC, int BITS>
+template <int MAXC, int BITS, bool FULL>
 cudaError_t launch_tiered(TieredDownParams& P, size_t smem, cudaStream_t st) {
-    auto kern = k_tiered_down<MAXC, BITS>;
+    auto kern = k_tiered_down<MAXC, BITS, FULL>;
     int grid = 0, cluster = 0;
-    cudaError_t e = cached_grid(kern, smem, &grid, &cluster);
+    cudaError_t e = cached_grid(kern, smem, &grid, &cluster, kTdThreads);
     if (e != cudaSuccess) return e;
     if (P.part_floats < (long long)(grid / cluster) * P.d) return cudaErrorInvalidValue;
     // per-CTA record counts (rank windows, or an own range of N / grid
@@ -1624,19 +1717,25 @@ cudaError_t launch_tiered(TieredDownParams& P, size_t smem, cudaStream_t st) {
     if (own > per) per = own;
     if (2 * per > P.aux_floats) return cudaErrorInvalidValue;
     void* args[] = {&P};
-    return launch_clustered(kern, grid, cluster, smem, st, args, /*pdl=*/true);
+    return launch_clustered(kern, grid, cluster, smem, st, args, /*pdl=*/true, kTdThreads);
 }
 
 cudaError_t launch_tiered_down(TieredDownParams P, cudaStream_t st) {
-    const size_t smem = (size_t)ring_layout(P.R, 2 * P.d, P.aux_floats * 4, 0).total;
-    const bool wide = P.d > 2048;
+    const size_t smem = (size_t)td_off_ring(P.aux_floats) + (size_t)P.ring_bytes;
+    // d = 2048 or 4096: every lane's chunks exist, no bounds checks
+    const bool wide = P.d > 2048, full = P.d == 2048 || P.d == 4096;
+#define SI_TIERED_CASE(B)                                                                  \
+    case B:                                                                                \
+        if (full) return wide ? launch_tiered<2, B, true>(P, smem, st) : launch_tiered<1, B, true>(P, smem, st); \
+        return wide ? launch_tiered<2, B, false>(P, smem, st) : launch_tiered<1, B, false>(P, smem, st);
     switch (P.bits) {
-        case 2: return wide ? launch_tiered<2, 2>(P, smem, st) : launch_tiered<1, 2>(P, smem, st);
-        case 3: return wide ? launch_tiered<2, 3>(P, smem, st) : launch_tiered<1, 3>(P, smem, st);
-        case 4: return wide ? launch_tiered<2, 4>(P, smem, st) : launch_tiered<1, 4>(P, smem, st);
-        case 8: return wide ? launch_tiered<2, 8>(P, smem, st) : launch_tiered<1, 8>(P, smem, st);
+        SI_TIERED_CASE(2)
+        SI_TIERED_CASE(3)
+        SI_TIERED_CASE(4)
+        SI_TIERED_CASE(8)
         default: return cudaErrorInvalidValue;
     }
+#undef SI_TIERED_CASE
 }
 
 cudaError_t launch_abs_hist(const float* a, int N, unsigned* hist, int32_t* slab, cudaStream_t st) {

@@ -54,13 +54,22 @@ struct DenseActParams {
     int n_rows;
     unsigned* err;
     int R;
+    // Optional L2 prefetch, at the end of each CTA, of the down records the
+    // tier choice that follows will most likely take: by the rank of |a|
+    // among the CTA's own rows, the bf16 columns of its share of the top
+    // tier and the code records of its share of the middle tier (a few more
+    // around each boundary). A hint only: results never depend on it.
+    const uint16_t* pf_WdT;   // [N][d] bf16 down columns, or null (no prefetch)
+    const uint8_t* pf_codes;  // [N] code records of pf_rec_bytes
+    int pf_rec_bytes;
+    int pf_k_top, pf_k_mid;   // tier sizes over all (listed) rows
 };
 
 struct TieredDownParams {
     const uint16_t* WdT;      // [N][d] bf16
     const uint8_t* codes;     // [N] records of rec_bytes: d*bits/8 code bytes, then ngp (scale, min) pairs
     int rec_bytes;
-    int bits;                 // code width: 2, 4 or 8
+    int bits;                 // code width: 2, 3, 4 or 8
     const float* a;           // [N]
     unsigned* hist;           // tier histogram of a (kTierBins + 1 words), re-zeroed by the kernel
     const int32_t* slab;      // optional per-bin member lists of hist (see kSlabCap)
@@ -73,7 +82,7 @@ struct TieredDownParams {
     long long part_floats;
     unsigned* tickets;
     unsigned* err;
-    int R;
+    int ring_bytes;           // shared-memory ring (split into one byte ring per warp)
     int aux_floats;           // per-CTA buffer: activations in the first half, columns in the second
 };
 
@@ -176,7 +185,7 @@ cudaError_t launch_sparse_decode(SparseDecodeParams P, int B, cudaStream_t st);
 int dense_act_stages(int d);
 cudaError_t launch_dense_act(DenseActParams P, cudaStream_t st);
 cudaError_t launch_abs_hist(const float* a, int N, unsigned* hist, int32_t* slab, cudaStream_t st);
-int tiered_down_stages(int d, int aux_floats);
+int tiered_down_ring(int d, int aux_floats, int rec_bytes);
 cudaError_t launch_tiered_down(TieredDownParams P, cudaStream_t st);
 int streaming_grid_upper_bound();
 
