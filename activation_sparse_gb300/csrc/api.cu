@@ -698,11 +698,8 @@ int spax_layer_destroy(spax_layer* L) {
 
 namespace {
 
-// With `pf` (and its tier sizes), the pass ends by prefetching into L2 the
-// down records of pf that the tiered kernel after it will most likely read.
 int dense_act_core(const uint16_t* Wg, const uint16_t* Wu, int d, int N, const uint16_t* x, float* a, unsigned* hist,
-                   int32_t* slab, cudaStream_t stream, const int32_t* rows = nullptr, int n_rows = 0,
-                   const spax_layer* pf = nullptr, long long pf_k_top = 0, long long pf_k_mid = 0) {
+                   int32_t* slab, cudaStream_t stream, const int32_t* rows = nullptr, int n_rows = 0) {
     if (!Wg || !Wu || !x || !a) return fail(SI_ERR_INVALID_ARG, "NULL pointer");
     if (d < 8 || d % 8 || N < 1) return fail(SI_ERR_INVALID_ARG, "need d % 8 == 0, N >= 1");
     if (d > 4096) return fail(SI_ERR_UNSUPPORTED, "dense activation pass supports d <= 4096");
@@ -721,13 +718,6 @@ int dense_act_core(const uint16_t* Wg, const uint16_t* Wu, int d, int N, const u
     P.rows = rows;
     P.n_rows = n_rows;
     P.err = err;
-    if (pf && pf->d == d && pf->N == N) {
-        P.pf_WdT = pf->WdT;
-        P.pf_codes = pf->codes;
-        P.pf_rec_bytes = pf->rec_bytes;
-        P.pf_k_top = (int)pf_k_top;
-        P.pf_k_mid = (int)pf_k_mid;
-    }
     P.R = si::dense_act_stages(d);
     if (P.R < 8) return fail(SI_ERR_UNSUPPORTED, "d too large for the activation ring");
     SI_CK(si::launch_dense_act(P, stream));
@@ -816,7 +806,7 @@ int spax_select_decode(spax_layer* L, const uint16_t* Wg, const uint16_t* Wu, co
         SI_CK(cudaMemsetAsync(y, 0, (size_t)L->d * sizeof(float), st));
         return SI_OK;
     }
-    int rc = dense_act_core(Wg, Wu, L->d, L->N, x, a, L->hist, L->slab, st, rows, n_rows, L, k_top, k_mid);
+    int rc = dense_act_core(Wg, Wu, L->d, L->N, x, a, L->hist, L->slab, st, rows, n_rows);
     if (rc) return rc;
     if ((rc = tiered_core(L, a, k_top, k_mid, y, nullptr, nullptr, st))) {
         cudaMemsetAsync(L->hist, 0, (si::kTierBins + 1) * sizeof(unsigned), st);  // leave it clean
@@ -834,7 +824,7 @@ int spax_ffn_decode(spax_layer* L, const uint16_t* Wg, const uint16_t* Wu, const
     cudaStream_t st = (cudaStream_t)stream;
     float* a = a_out ? a_out : L->a;
     // the dense pass builds the tier histogram of a as it writes it
-    if ((rc = dense_act_core(Wg, Wu, L->d, L->N, x, a, L->hist, L->slab, st, nullptr, 0, L, k_top, k_mid))) return rc;
+    if ((rc = dense_act_core(Wg, Wu, L->d, L->N, x, a, L->hist, L->slab, st))) return rc;
     if ((rc = tiered_core(L, a, k_top, k_mid, y, nullptr, nullptr, st))) {
         cudaMemsetAsync(L->hist, 0, (si::kTierBins + 1) * sizeof(unsigned), st);  // leave it clean
         return rc;

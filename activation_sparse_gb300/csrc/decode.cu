@@ -64,10 +64,19 @@ __device__ void cluster_ticket_reduce4(const float* ypart, int BD, float* __rest
     cluster_arrive();
     cluster_wait();
     for (int q = threadIdx.x; q < Q; q += blockDim.x) {
+        // the peers' values in rank order, up to eight loads in flight before
+        // the adds (the rank order of the sum is kept)
         float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int c = 0; c < C; ++c) {
-            const float4 t = reinterpret_cast<const float4*>(cl.map_shared_rank(ypart, c))[q0 + q];
-            v.x += t.x; v.y += t.y; v.z += t.z; v.w += t.w;
+        for (int c = 0; c < C; c += 8) {
+            float4 t[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                if (c + u < C) t[u] = reinterpret_cast<const float4*>(cl.map_shared_rank(ypart, c + u))[q0 + q];
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                if (c + u < C) {
+                    v.x += t[u].x; v.y += t[u].y; v.z += t[u].z; v.w += t[u].w;
+                }
         }
         __stcg(part4 + (size_t)cid * BD4 + q0 + q, v);
     }
@@ -332,6 +341,309 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_sparse_decode(SparseDecodePa
     cluster_ticket_reduce4(reinterpret_cast<float*>(ring), B * d, P.part, P.tickets, P.y);
 }
 
+// ------------------------------------------------ batch decode on tensor cores
+
+// Warp-level bf16 tensor-core pieces: ldmatrix of 8x8 b16 tiles from any
+// 16-byte-aligned row addresses (one per lane 0-15), and the m16n8k16 MMA
+// with fp32 accumulation.
+__device__ __forceinline__ void ldsm_x2(const void* row, uint32_t& r0, uint32_t& r1) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0, %1}, [%2];"
+                 : "=r"(r0), "=r"(r1)
+                 : "r"(smem_u32(row)));
+}
+__device__ __forceinline__ void ldsm_x4(const void* row, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(smem_u32(row)));
+}
+__device__ __forceinline__ void ldsm_x2_trans(const void* row, uint32_t& r0, uint32_t& r1) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0, %1}, [%2];"
+                 : "=r"(r0), "=r"(r1)
+                 : "r"(smem_u32(row)));
+}
+// d += A (16 x 16, rows a0..a3 as the fragment) * B (16 x 8), A's rows 8-15
+// and k 8-15 given as registers (zero where absent)
+__device__ __forceinline__ void mma_bf16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+    // a register-only operation: not volatile, so independent MMAs can be
+    // interleaved by the compiler
+    asm(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+    const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+// Shared-memory layout of the tensor-core batch decode: full / empty
+// barriers, the cross-warp sums of the gate and up products, a, then the
+// stages. A stage is one packed record (gate row, up row, down column) plus
+// 16 bytes, so that the same 16-byte row of eight consecutive records falls
+// in eight different bank groups (conflict-free ldmatrix).
+constexpr int kMmaBatch = 8;  // records per batch: a batch's stages are held until its down products are done
+struct MmaLayout {
+    int off_full, off_empty, off_red, off_a, off_ring, stage, R, total;
+};
+__host__ __device__ inline MmaLayout mma_layout(int R, int d) {
+    MmaLayout L;
+    L.R = R;
+    L.stage = round_up(6 * d, 128) + 16;
+    L.off_full = 0;
+    L.off_empty = 8 * R;
+    L.off_red = round_up(16 * R, 128);
+    L.off_a = L.off_red + kConsWarps * 128 * 4;
+    L.off_ring = L.off_a + round_up(8 * 8 * 4, 128);
+    L.total = L.off_ring + R * L.stage;
+    return L;
+}
+
+// Grid-wide sum of the CTAs' partials for a cooperative launch (every CTA
+// resident): each CTA stores its partial (BD floats in shared memory) to
+// part[blockIdx], arrives on ctr[0] and waits (bounded) until all G CTAs
+// have arrived; then it sums its slice of the BD floats over the G partials
+// in a fixed order (groups of threads take every ng-th partial, the group
+// sums are added in group order) and writes y. The last CTA to leave resets
+// ctr[0] and ctr[1] for the next launch. BD % 4 == 0.
+__device__ void grid_slice_reduce4(const float* ypart, int BD, float* __restrict__ part, unsigned* ctr,
+                                   float* __restrict__ y, unsigned* err, unsigned site) {
+    __shared__ float4 s_grp[kDecThreads];
+    __shared__ unsigned s_last;
+    const int G = (int)gridDim.x, BD4 = BD / 4;
+    float4* part4 = reinterpret_cast<float4*>(part);
+    const float4* yp4 = reinterpret_cast<const float4*>(ypart);
+    for (int k = threadIdx.x; k < BD4; k += blockDim.x) __stcg(part4 + (size_t)blockIdx.x * BD4 + k, yp4[k]);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        // release: the partial (ordered before this thread by the CTA barrier)
+        // is visible before the arrival; acquire: the others' partials after it
+        asm volatile("fence.acq_rel.gpu;" ::: "memory");
+        asm volatile("red.relaxed.gpu.global.add.u32 [%0], 1;" ::"l"(ctr) : "memory");
+        const long long t0 = cycles();
+        for (uint32_t it = 1;; ++it) {
+            unsigned v;
+            asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
+            if (v >= (unsigned)G) break;
+            if ((it & 255u) == 0) {
+                if (*reinterpret_cast<volatile unsigned*>(err) & SI_DEVERR_WAIT_TIMEOUT) break;
+                if (cycles() - t0 > kWaitLimitCycles) {
+                    atomicOr(err, SI_DEVERR_WAIT_TIMEOUT | site);
+                    break;
+                }
+            }
+        }
+    }
+    __syncthreads();
+    const int q0 = (int)((long long)BD4 * blockIdx.x / G), q1 = (int)((long long)BD4 * (blockIdx.x + 1) / G);
+    const int nq = q1 - q0;
+    auto sum_parts = [&](int q, int first, int step) {
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        int k = first;
+        for (; k + 7 * step < G; k += 8 * step) {
+            float4 t[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) t[u] = __ldcg(part4 + (size_t)(k + u * step) * BD4 + q);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                v.x += t[u].x; v.y += t[u].y; v.z += t[u].z; v.w += t[u].w;
+            }
+        }
+        for (; k < G; k += step) {
+            const float4 t = __ldcg(part4 + (size_t)k * BD4 + q);
+            v.x += t.x; v.y += t.y; v.z += t.z; v.w += t.w;
+        }
+        return v;
+    };
+    float4* y4 = reinterpret_cast<float4*>(y);
+    if (nq > 0 && nq <= (int)blockDim.x) {
+        const int ng = (int)blockDim.x / nq;
+        const int q = (int)threadIdx.x % nq, grp = (int)threadIdx.x / nq;
+        if (grp < ng) s_grp[grp * nq + q] = sum_parts(q0 + q, grp, ng);
+        __syncthreads();
+        if ((int)threadIdx.x < nq) {
+            float4 acc = s_grp[threadIdx.x];
+            for (int gg = 1; gg < ng; ++gg) {
+                const float4 t = s_grp[gg * nq + threadIdx.x];
+                acc.x += t.x; acc.y += t.y; acc.z += t.z; acc.w += t.w;
+            }
+            y4[q0 + threadIdx.x] = acc;
+        }
+    } else {
+        for (int q = q0 + (int)threadIdx.x; q < q1; q += blockDim.x) y4[q] = sum_parts(q, 0, 1);
+    }
+    __syncthreads();  // every read of the partials is done before leaving
+    if (threadIdx.x == 0) {
+        __threadfence();
+        s_last = (atomicAdd(ctr + 1, 1u) == (unsigned)G - 1) ? 1u : 0u;
+        if (s_last) {
+            ctr[0] = 0u;
+            ctr[1] = 0u;
+        }
+    }
+}
+
+// Batch-B decode (B <= 8 sequences over the union plan) on the tensor cores.
+// The CTA takes its records in batches of eight. Gate and up products in one
+// MMA per k-step: A's rows 0-7 are the batch's gate rows and rows 8-15 their
+// up rows, times x^T (N = the 8 sequences); K is split over the eight
+// consumer warps (warp w takes k in [w d / 8, (w + 1) d / 8), its x
+// fragments held in registers for the whole launch), and the warps' partial
+// sums meet in shared memory, added in warp order. a = silu(g) u where the
+// sequence selected the record, else 0. Down: warp w takes rows
+// [w d / 8, (w + 1) d / 8); the batch's down columns (ldmatrix.trans) enter
+// K twice, against a's leading bf16 term in k 0-7 and its remainder in
+// k 8-15, so one MMA per tile applies a to within 2^-18 |a| (fp32-level
+// products). The launch is cooperative (one CTA per SM,
+// all resident) and the CTA sums meet in a grid-wide slice reduction in a
+// fixed order (deterministic).
+// DT = d / 128: k-steps of 16 per warp slice and m-tiles of 16 rows per warp.
+template <int DT>
+__global__ void __launch_bounds__(kDecThreads, 1) k_sparse_decode_mma(SparseDecodeParams P, int B) {
+    extern __shared__ __align__(1024) uint8_t smem[];
+    constexpr int d = 128 * DT;
+    const MmaLayout L = mma_layout(P.R, d);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.off_full);
+    uint64_t* empty = reinterpret_cast<uint64_t*>(smem + L.off_empty);
+    float* s_red = reinterpret_cast<float*>(smem + L.off_red);  // [warp][gate 64 | up 64]
+    float* s_av = reinterpret_cast<float*>(smem + L.off_a);     // [record][sequence]
+    uint8_t* ring = smem + L.off_ring;
+    const int R = L.R;
+    // the host never launches fewer stages than a batch, another d or B > 8
+    if (R < kMmaBatch || P.d != d || B < 1 || B > 8) {
+        if (threadIdx.x == 0) atomicOr(P.err, SI_DEVERR_COUNT);
+        return;
+    }
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n = P.n_dev ? *P.n_dev : P.n_host;
+    const int lo = (int)((long long)n * blockIdx.x / gridDim.x);
+    const int hi = (int)((long long)n * (blockIdx.x + 1) / gridDim.x);
+    const int cnt = hi - lo;
+    const uint32_t rec_bytes = (uint32_t)(6 * d);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < R; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kConsWarps);
+        }
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    if (warp == kConsWarps) {
+        const uint64_t pol = policy_evict_first();
+        produce_by_index(P.pos + lo, cnt, P.n_records, R, empty, P.err, kSiteDecode | kSiteEmpty,
+                         [&](int, int s, int p) {
+                             mbar_arrive_expect_tx(&full[s], rec_bytes);
+                             bulk_g2s_hint(ring + (size_t)s * L.stage, P.packed + (size_t)p * 3 * d, rec_bytes,
+                                           &full[s], pol);
+                         });
+    } else {
+        const int g = lane >> 2, t = lane & 3;  // fragment row / column group
+        // x^T fragments of this warp's k-slice: b0b1 = x[g][k0 + 2t ..], b2b3 = x[g][k0 + 8 + 2t ..]
+        uint32_t xb[DT][2];
+        {
+            const uint32_t* xg = reinterpret_cast<const uint32_t*>(P.x + (size_t)(g < B ? g : 0) * d);
+#pragma unroll
+            for (int ks = 0; ks < DT; ++ks) {
+                const int k0 = warp * (d / 8) + 16 * ks;
+                xb[ks][0] = g < B ? __ldg(xg + (k0 + 2 * t) / 2) : 0u;
+                xb[ks][1] = g < B ? __ldg(xg + (k0 + 8 + 2 * t) / 2) : 0u;
+            }
+        }
+        float acc[DT][4];
+#pragma unroll
+        for (int mt = 0; mt < DT; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.0f;
+        const int nbat = (cnt + kMmaBatch - 1) / kMmaBatch;
+        for (int bt = 0; bt < nbat; ++bt) {
+            const int i0 = bt * kMmaBatch;
+            const int nb = min(kMmaBatch, cnt - i0);
+            // the sequence mask of this thread's record, read ahead of the products
+            const int rm = threadIdx.x >> 3;
+            const uint32_t pm = (threadIdx.x < 64 && rm < nb && P.pmask) ? __ldg(P.pmask + lo + i0 + rm) : 0xFFFFFFFFu;
+            for (int r = 0; r < nb; ++r) {
+                const int i = i0 + r;
+                mbar_wait(&full[i % R], (uint32_t)((i / R) & 1), P.err, kSiteDecode | kSiteFull);
+            }
+            // lanes 0-15 address record (lane & 7) (record 0 where the batch is short)
+            const int rr = (lane & 7) < nb ? (lane & 7) : 0;
+            const uint8_t* rec = ring + (size_t)((i0 + rr) % R) * L.stage;
+            const int half8 = (lane >> 3) & 1;  // second 8x8 tile of the pair
+            // gate (rows g) and up (rows g + 8): D[record][sequence] over this
+            // warp's k-slice. ldmatrix.x4 tiles: lanes 0-7 gate rows at k0,
+            // 8-15 up rows at k0, 16-23 gate rows at k0 + 8, 24-31 up rows at
+            // k0 + 8. Two accumulator chains (even and odd k-steps), so that
+            // consecutive MMAs do not wait on each other.
+            const uint8_t* gu = ring + (size_t)((i0 + ((lane & 7) < nb ? (lane & 7) : 0)) % R) * L.stage +
+                                (size_t)(((lane >> 3) & 1) * 2 * d) + (size_t)(((lane >> 4) & 1) * 8) * 2;
+            float cgu[2][4] = {};
+#pragma unroll
+            for (int ks = 0; ks < DT; ++ks) {
+                const int k0 = warp * (d / 8) + 16 * ks;
+                uint32_t a0, a1, a2, a3;
+                ldsm_x4(gu + (size_t)k0 * 2, a0, a1, a2, a3);
+                mma_bf16(cgu[ks & 1], a0, a1, a2, a3, xb[ks][0], xb[ks][1]);
+            }
+            float cg[1][2] = {{cgu[0][0] + cgu[1][0], cgu[0][1] + cgu[1][1]}};
+            float cu[1][2] = {{cgu[0][2] + cgu[1][2], cgu[0][3] + cgu[1][3]}};
+            // rows g (the records) of the fragments: sequences 2t, 2t + 1
+            *reinterpret_cast<float2*>(s_red + warp * 128 + g * 8 + 2 * t) = make_float2(cg[0][0], cg[0][1]);
+            *reinterpret_cast<float2*>(s_red + warp * 128 + 64 + g * 8 + 2 * t) = make_float2(cu[0][0], cu[0][1]);
+            named_bar_sync(1, kConsThreads);
+            if (threadIdx.x < 64) {
+                const int r = threadIdx.x >> 3, b = threadIdx.x & 7;
+                float gs = 0.0f, us = 0.0f;
+#pragma unroll
+                for (int w = 0; w < kConsWarps; ++w) {
+                    gs += s_red[w * 128 + threadIdx.x];
+                    us += s_red[w * 128 + 64 + threadIdx.x];
+                }
+                s_av[r * 8 + b] = (r < nb && b < B && ((pm >> b) & 1u)) ? swiglu(gs, us) : 0.0f;
+            }
+            named_bar_sync(1, kConsThreads);
+            // a as B fragments: k = 2t, 2t + 1 (records) -> (a[2t][g], a[2t + 1][g]),
+            // its leading bf16 term for k < 8 and the bf16 of the remainder for k >= 8
+            uint32_t bh, bl;
+            {
+                const float a0 = s_av[(2 * t) * 8 + g], a1 = s_av[(2 * t + 1) * 8 + g];
+                const float h0 = __bfloat162float(__float2bfloat16_rn(a0)), h1 = __bfloat162float(__float2bfloat16_rn(a1));
+                bh = pack_bf16(h0, h1);
+                bl = pack_bf16(a0 - h0, a1 - h1);
+            }
+            // down: Y[row][sequence] += Dn[row][record] a[record][sequence] over this warp's rows
+            const uint8_t* dn = rec + (size_t)4 * d + (size_t)(8 * half8) * 2;
+            // (the records' columns enter K twice: k 0-7 and k 8-15 both hold
+            // records 0-7, against a's two terms)
+#pragma unroll
+            for (int mt = 0; mt < DT; ++mt) {
+                uint32_t a0, a1;
+                ldsm_x2_trans(dn + (size_t)(warp * (d / 8) + 16 * mt) * 2, a0, a1);
+                mma_bf16(acc[mt], a0, a1, a0, a1, bh, bl);
+            }
+            __syncwarp();
+            if (lane == 0)
+                for (int r = 0; r < nb; ++r) mbar_arrive(&empty[(i0 + r) % R]);
+        }
+        named_bar_sync(1, kConsThreads);  // every consumer is done with the ring
+        float* ypart = reinterpret_cast<float*>(ring);
+#pragma unroll
+        for (int mt = 0; mt < DT; ++mt) {
+            const int m0 = warp * (d / 8) + 16 * mt;
+            if (2 * t < B) {
+                ypart[(size_t)(2 * t) * d + m0 + g] = acc[mt][0];
+                ypart[(size_t)(2 * t) * d + m0 + 8 + g] = acc[mt][2];
+            }
+            if (2 * t + 1 < B) {
+                ypart[(size_t)(2 * t + 1) * d + m0 + g] = acc[mt][1];
+                ypart[(size_t)(2 * t + 1) * d + m0 + 8 + g] = acc[mt][3];
+            }
+        }
+    }
+    __syncthreads();
+    grid_slice_reduce4(reinterpret_cast<float*>(ring), B * d, P.part, P.tickets, P.y, P.err, kSiteDecode | kSiteAccum);
+}
+
 // Batch-1 decode with decoupled warps: neuron i belongs to warp i % 8 and ring
 // stage i % R. Each warp computes a = silu(g.x) * (u.x) for its neuron and
 // accumulates a * down into its own register partial of y; there is no
@@ -511,13 +823,9 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_sparse_decode_b1(SparseDecod
 
 // --------------------------------------------------------------- dense act
 
-constexpr int kDensePfRows = 256;   // rows per CTA up to which the prefetch ranks them
-constexpr int kDensePfMargin = 2;   // extra ranks prefetched on each side of a tier boundary
-
 template <int MAXC>
 __global__ void __launch_bounds__(kDecThreads, 1) k_dense_act(DenseActParams P) {
     extern __shared__ __align__(1024) uint8_t smem[];
-    __shared__ float s_pf[kDensePfRows];  // this CTA's a values, for the optional prefetch
     const int d = P.d;
     const RingLayout L = ring_layout(P.R, 4 * d, 0, d * 2);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.off_full);
@@ -617,7 +925,6 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_dense_act(DenseActParams P) 
             if (lane == 0) {
                 const float av = swiglu(g, u);
                 P.a[row(i)] = av;
-                if (i < kDensePfRows) s_pf[i] = av;
                 mbar_arrive(&empty[s]);
                 if (P.hist) {
                     if (P.slab) {
@@ -632,25 +939,6 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_dense_act(DenseActParams P) 
             }
         }
         if (lane == 0 && pend_pos < (uint32_t)kSlabCap) P.slab[(size_t)pend_bin * kSlabCap + pend_pos] = pend_n;
-    }
-    if (!P.pf_WdT || cnt > kDensePfRows) return;  // the same decision in every thread
-    __syncthreads();
-    // local rank of each row's |a| (ties to the lower row), against this CTA's
-    // share of each tier, widened by kDensePfMargin ranks on both sides
-    const int total_rows = P.rows ? P.n_rows : P.N;
-    const int T = (int)(((long long)P.pf_k_top * cnt + total_rows / 2) / total_rows);
-    const int M = (int)(((long long)P.pf_k_mid * cnt + total_rows / 2) / total_rows);
-    for (int t = threadIdx.x; t < cnt; t += blockDim.x) {
-        const uint32_t kt = abs_key(s_pf[t]);
-        int rank = 0;
-        for (int j = 0; j < cnt; ++j) {
-            const uint32_t kj = abs_key(s_pf[j]);
-            rank += (kj > kt) || (kj == kt && j < t);
-        }
-        const size_t n = (size_t)row(t);
-        if (P.pf_k_top > 0 && rank < T + kDensePfMargin) prefetch_l2(P.pf_WdT + n * d, row_bytes);
-        if (P.pf_k_mid > 0 && rank >= T - kDensePfMargin && rank < T + M + kDensePfMargin)
-            prefetch_l2(P.pf_codes + n * (size_t)P.pf_rec_bytes, (uint32_t)P.pf_rec_bytes);
     }
 }
 
@@ -1617,7 +1905,9 @@ int decode_max_partial_floats(int d, int B) {
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-    return (sms / 2 + 1) * B * d;  // clusters have at least 2 CTAs
+    // one partial per CTA for the tensor-core batch kernel (one CTA per SM),
+    // one per cluster (at least 2 CTAs) otherwise
+    return (B > 1 ? sms : sms / 2 + 1) * B * d;
 }
 
 int sparse_decode_b1_stages(int d) {
@@ -1629,8 +1919,47 @@ int sparse_decode_b1_stages(int d) {
     return (R >= kConsWarps && stage >= round_up(d, 256) * 4) ? R : 0;
 }
 
+// Stages of the tensor-core batch decode for width d (at most 32; 0 when
+// fewer than one batch of records fits).
+int sparse_decode_mma_stages(int d) {
+    const MmaLayout L = mma_layout(0, d);
+    int R = (kSmemBudget - (int)sizeof(float4) * kDecThreads - L.off_ring - 256) / L.stage;
+    if (R > 32) R = 32;
+    return R >= kMmaBatch ? R : 0;
+}
+
+template <int DT>
+cudaError_t launch_sd_mma(SparseDecodeParams& P, int B, cudaStream_t st) {
+    auto kern = k_sparse_decode_mma<DT>;
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    if ((e = allow_max_smem(kern)) != cudaSuccess) return e;
+    if (P.part_floats < (long long)sms * B * P.d) return cudaErrorInvalidValue;
+    void* args[] = {&P, &B};
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(sms, 1, 1);  // one CTA per SM; the cooperative launch guarantees co-residency
+    cfg.blockDim = dim3(kDecThreads, 1, 1);
+    cfg.dynamicSmemBytes = (size_t)mma_layout(P.R, P.d).total;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelExC(&cfg, reinterpret_cast<const void*>(kern), args);
+}
+
 cudaError_t launch_sparse_decode(SparseDecodeParams P, int B, cudaStream_t st) {
     const bool wide = P.d > 2048;
+    // B > 1 at d = 1024 or 2048: the tensor-core kernel (wider d would not
+    // keep its x fragments and partial sums in the registers of a 9-warp CTA)
+    if (B >= 2 && B <= 8 && (P.d == 1024 || P.d == 2048)) {
+        SparseDecodeParams P2 = P;
+        P2.R = sparse_decode_mma_stages(P.d);
+        if (P2.R >= kMmaBatch) return P.d == 1024 ? launch_sd_mma<8>(P2, B, st) : launch_sd_mma<16>(P2, B, st);
+    }
     if (B == 1 && P.pmask == nullptr && (P.n_dev == nullptr || P.stable_plan)) {
         const int R1 = sparse_decode_b1_stages(P.d);
         if (R1 >= kConsWarps) {

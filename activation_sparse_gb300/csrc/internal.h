@@ -54,15 +54,6 @@ struct DenseActParams {
     int n_rows;
     unsigned* err;
     int R;
-    // Optional L2 prefetch, at the end of each CTA, of the down records the
-    // tier choice that follows will most likely take: by the rank of |a|
-    // among the CTA's own rows, the bf16 columns of its share of the top
-    // tier and the code records of its share of the middle tier (a few more
-    // around each boundary). A hint only: results never depend on it.
-    const uint16_t* pf_WdT;   // [N][d] bf16 down columns, or null (no prefetch)
-    const uint8_t* pf_codes;  // [N] code records of pf_rec_bytes
-    int pf_rec_bytes;
-    int pf_k_top, pf_k_mid;   // tier sizes over all (listed) rows
 };
 
 struct TieredDownParams {

@@ -68,6 +68,54 @@ def test_sparse_decode_parity(si, d, N, gamma, delta, phi, alpha, T, B, sigma):
     c.layer.close()
 
 
+MMA_CASES = [
+    # d, N, gamma, delta, phi, alpha, T, B, sigma: batches at d = 1024 and 2048 take the tensor-core kernel
+    (1024, 4096, 0.7, 0.2, 0.4, 256, 8, 8, 1.0),
+    (1024, 600, 0.9, 0.1, 0.3, 32, 4, 2, 1.0),           # a few records per CTA: short last batches
+    (2048, 11008, 0.8, 0.25, 0.5, 1024, 16, 5, 1.5),
+    (2048, 3000, 1.0, 0.0, 1.0, 64, 4, 8, 1.0),          # phi = 1: every sequence computes every neuron
+]
+
+
+@pytest.mark.parametrize("d,N,gamma,delta,phi,alpha,T,B,sigma", MMA_CASES)
+def test_batch_decode_tensor_core_path(si, d, N, gamma, delta, phi, alpha, T, B, sigma):
+    c = Case(si, d, N, gamma, delta, phi, alpha, T, B, sigma, seed=48)
+    S_dev = dev(c.S)
+    si.si_decode_plan(c.layer, S_dev, c.n_sel, B)
+    x = synth.tokens(49, 0, synth.T_DECODE, B, d)
+    ys = []
+    for _ in range(2):
+        y = Guarded((B, d), torch().float32, fill=float("nan"))
+        si.si_sparse_ffn_decode(c.layer, S_dev, c.n_sel, B, dev_bf16(x), y.t)
+        y.check()
+        ys.append(y.numpy())
+    assert np.array_equal(ys[0].view(np.uint32), ys[1].view(np.uint32))   # deterministic
+    for b in range(B):
+        ref = oracle.sparse_ffn(c.Wg, c.Wu, c.Wd, c.loaded, c.S[b], x[b])
+        assert rel_err(ys[0][b], ref) <= 2e-5, b
+    c.layer.close()
+
+
+def test_batch_decode_disjoint_sets(si):
+    # four sequences with disjoint computed sets: the union is four times a
+    # set and every record serves exactly one sequence
+    d, N, B = 2048, 4096, 4
+    c = Case(si, d, N, 0.9, 0.0, 0.2, 64, 4, 1, seed=50)
+    nl = len(c.loaded)
+    n = nl // (2 * B)
+    S = np.stack([np.arange(b, nl, B, dtype=np.int32)[:n] for b in range(B)])
+    S_dev = dev(S)
+    si.si_decode_plan(c.layer, S_dev, n, B)
+    x = synth.tokens(51, 0, synth.T_DECODE, B, d)
+    y = Guarded((B, d), torch().float32, fill=float("nan"))
+    si.si_sparse_ffn_decode(c.layer, S_dev, n, B, dev_bf16(x), y.t)
+    got = y.numpy()
+    for b in range(B):
+        ref = oracle.sparse_ffn(c.Wg, c.Wu, c.Wd, c.loaded, S[b], x[b])
+        assert rel_err(got[b], ref) <= 2e-5, b
+    c.layer.close()
+
+
 def test_sparse_decode_dense_limit_matches_library_dense_ffn(si):
     # every neuron loaded and computed: the output is the dense SwiGLU FFN (numpy)
     from scipy.special import expit
