@@ -650,7 +650,16 @@ int spax_encode(const uint16_t* Wd, int d, int N, int bits, int group, spax_laye
         (rc = dalloc(&L->hist, si::kTierBins + 1, "tier histogram")) ||
         (rc = dalloc(&L->slab, (size_t)si::kTierBins * si::kSlabCap, "tier member lists")) ||
         (rc = dalloc(&L->a, N, "activations")) ||
-        (rc = dalloc(&L->tickets, 16, "tickets")) || (rc = grow_part(&L->part, &L->part_floats, d, 1))) {
+        (rc = dalloc(&L->tickets, 16, "tickets"))) {
+        destroy_spax(L);
+        return rc;
+    }
+    L->part_floats = si::tiered_max_partial_floats(d);
+    if (L->part_floats <= 0) {
+        destroy_spax(L);
+        return fail(SI_ERR_CUDA, "cannot query the device for the tiered grid");
+    }
+    if ((rc = dalloc(&L->part, (size_t)L->part_floats, "tiered partials"))) {
         destroy_spax(L);
         return rc;
     }

@@ -406,9 +406,10 @@ __host__ __device__ inline MmaLayout mma_layout(int R, int d) {
 // have arrived; then it sums its slice of the BD floats over the G partials
 // in a fixed order (groups of threads take every ng-th partial, the group
 // sums are added in group order) and writes y. The last CTA to leave resets
-// ctr[0] and ctr[1] for the next launch. BD % 4 == 0.
+// ctr[0] and ctr[1] for the next launch. BD % 4 == 0. With `trigger` the
+// grid lets its dependents launch once all its CTAs have arrived.
 __device__ void grid_slice_reduce4(const float* ypart, int BD, float* __restrict__ part, unsigned* ctr,
-                                   float* __restrict__ y, unsigned* err, unsigned site) {
+                                   float* __restrict__ y, unsigned* err, unsigned site, bool trigger = false) {
     __shared__ float4 s_grp[kDecThreads];
     __shared__ unsigned s_last;
     const int G = (int)gridDim.x, BD4 = BD / 4;
@@ -436,6 +437,9 @@ __device__ void grid_slice_reduce4(const float* ypart, int BD, float* __restrict
         }
     }
     __syncthreads();
+    // every CTA of the grid is resident now: the next grid in the stream may
+    // begin (it cannot take an SM this grid still needs)
+    if (trigger) grid_launch_dependents();
     const int q0 = (int)((long long)BD4 * blockIdx.x / G), q1 = (int)((long long)BD4 * (blockIdx.x + 1) / G);
     const int nq = q1 - q0;
     auto sum_parts = [&](int q, int first, int step) {
@@ -1446,9 +1450,10 @@ __device__ __forceinline__ void codes4_unit(uint32_t q, float2 (&w)[4]) {
 // at their own size (a bf16 column 2d bytes, a code record rec_bytes), and
 // reuses bytes once every warp of the stream has released them. The
 // streams' partials meet in shared memory at the end (summed in stream
-// order) and the CTAs' sums are reduced through the cluster and a
-// fixed-order final pass (deterministic). FULL: d == 2048 * MAXC, every
-// lane's chunks exist (no bounds checks in the per-record code).
+// order) and the CTAs' sums in a grid-wide slice reduction in a fixed order
+// (deterministic; the launch is cooperative, one CTA per SM). FULL:
+// d == 2048 * MAXC, every lane's chunks exist (no bounds checks in the
+// per-record code).
 template <int MAXC, int BITS, bool FULL>
 __global__ void __launch_bounds__(kTdThreads, 1) k_tiered_down(TieredDownParams P) {
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -1492,7 +1497,6 @@ __global__ void __launch_bounds__(kTdThreads, 1) k_tiered_down(TieredDownParams 
     __shared__ unsigned s_last;
     __shared__ __align__(8) uint64_t s_stage_bar;
     __shared__ int s_n[2];
-    grid_launch_dependents();
     grid_dependency_wait();  // a and its tier histogram are the previous grids' output
     const int tid = threadIdx.x;
     const int N = P.N;
@@ -1730,7 +1734,7 @@ __global__ void __launch_bounds__(kTdThreads, 1) k_tiered_down(TieredDownParams 
         }
     }
     __syncthreads();
-    cluster_ticket_reduce4(ycta, d, P.part, P.tickets, P.y);
+    grid_slice_reduce4(ycta, d, P.part, P.tickets, P.y, P.err, kSiteTiered | kSiteAccum, /*trigger=*/true);
     // every CTA read the histogram at its start; the last one to finish
     // re-zeroes it for the next token
     if (threadIdx.x == 0) {
@@ -1901,6 +1905,13 @@ int sparse_decode_stages(int d, int B) {
     return R;
 }
 
+int tiered_max_partial_floats(int d) {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    return sms * d;  // one partial per CTA, one CTA per SM
+}
+
 int decode_max_partial_floats(int d, int B) {
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
@@ -2031,13 +2042,24 @@ int tiered_down_ring(int d, int aux_floats, int rec_bytes) {
     return (RP >= 2 * d && RP >= rec_bytes && bytes >= (4 * kTdPairs + 4) * d) ? bytes : 0;
 }
 
+// Cooperative launch (one CTA per SM, all resident: the grid-wide slice
+// reduction waits on every CTA), with programmatic stream serialization when
+// the runtime accepts the two together (probed once, outside stream capture).
+inline int& tiered_pdl_state() {
+    static int state = 0;  // 0 unknown, 1 cooperative + PDL accepted, 2 cooperative only
+    return state;
+}
+
 template <int MAXC, int BITS, bool FULL>
 cudaError_t launch_tiered(TieredDownParams& P, size_t smem, cudaStream_t st) {
     auto kern = k_tiered_down<MAXC, BITS, FULL>;
-    int grid = 0, cluster = 0;
-    cudaError_t e = cached_grid(kern, smem, &grid, &cluster, kTdThreads);
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (P.part_floats < (long long)(grid / cluster) * P.d) return cudaErrorInvalidValue;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    if ((e = allow_max_smem(kern)) != cudaSuccess) return e;
+    const int grid = sms;
+    if (P.part_floats < (long long)grid * P.d) return cudaErrorInvalidValue;
     // per-CTA record counts (rank windows, or an own range of N / grid
     // columns) must fit the activation buffer (activations in the first half
     // of the buffer, columns in the second)
@@ -2046,7 +2068,35 @@ cudaError_t launch_tiered(TieredDownParams& P, size_t smem, cudaStream_t st) {
     if (own > per) per = own;
     if (2 * per > P.aux_floats) return cudaErrorInvalidValue;
     void* args[] = {&P};
-    return launch_clustered(kern, grid, cluster, smem, st, args, /*pdl=*/true, kTdThreads);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.blockDim = dim3(kTdThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    int& state = tiered_pdl_state();
+    if (state == 0) {
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        if (cudaStreamIsCapturing(st, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone) {
+            cfg.numAttrs = 1;
+            return cudaLaunchKernelExC(&cfg, reinterpret_cast<const void*>(kern), args);
+        }
+        cfg.numAttrs = 2;
+        e = cudaLaunchKernelExC(&cfg, reinterpret_cast<const void*>(kern), args);
+        if (e == cudaSuccess) {
+            state = 1;
+            return e;
+        }
+        (void)cudaGetLastError();
+        state = 2;
+    }
+    cfg.numAttrs = state == 1 ? 2 : 1;
+    return cudaLaunchKernelExC(&cfg, reinterpret_cast<const void*>(kern), args);
 }
 
 cudaError_t launch_tiered_down(TieredDownParams P, cudaStream_t st) {
