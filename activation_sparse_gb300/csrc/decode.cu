@@ -520,6 +520,11 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_sparse_decode_mma(SparseDeco
         return;
     }
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // A stable plan (its records, masks and count) cannot be written by the
+    // grid before this one, so the ring fills while that grid finishes; x,
+    // y, the partials and the counters are touched only after the
+    // dependency wait. A fresh plan may be that grid's output: wait first.
+    if (!P.stable_plan) grid_dependency_wait();
     const int n = P.n_dev ? *P.n_dev : P.n_host;
     const int lo = (int)((long long)n * blockIdx.x / gridDim.x);
     const int hi = (int)((long long)n * (blockIdx.x + 1) / gridDim.x);
@@ -544,6 +549,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_sparse_decode_mma(SparseDeco
                                            &full[s], pol);
                          });
     } else {
+        if (P.stable_plan) grid_dependency_wait();  // x may be the previous grid's output
         const int g = lane >> 2, t = lane & 3;  // fragment row / column group
         // x^T fragments of this warp's k-slice: b0b1 = x[g][k0 + 2t ..], b2b3 = x[g][k0 + 8 + 2t ..]
         uint32_t xb[DT][2];
@@ -644,8 +650,9 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_sparse_decode_mma(SparseDeco
             }
         }
     }
-    __syncthreads();
-    grid_slice_reduce4(reinterpret_cast<float*>(ring), B * d, P.part, P.tickets, P.y, P.err, kSiteDecode | kSiteAccum);
+    __syncthreads();  // (the consumers' dependency wait orders every write below after the previous grid)
+    grid_slice_reduce4(reinterpret_cast<float*>(ring), B * d, P.part, P.tickets, P.y, P.err, kSiteDecode | kSiteAccum,
+                       /*trigger=*/true);
 }
 
 // Batch-1 decode with decoupled warps: neuron i belongs to warp i % 8 and ring
@@ -1930,6 +1937,37 @@ int sparse_decode_b1_stages(int d) {
     return (R >= kConsWarps && stage >= round_up(d, 256) * 4) ? R : 0;
 }
 
+// Cooperative launch (one CTA per SM, all resident: a grid-wide slice
+// reduction waits on every CTA), with programmatic stream serialization when
+// the runtime accepts the two together (probed once, outside stream capture;
+// during a capture before the probe, cooperative alone).
+cudaError_t launch_coop(const void* kern, cudaLaunchConfig_t cfg, void** args) {
+    static int state = 0;  // 0 unknown, 1 cooperative + PDL accepted, 2 cooperative only
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    if (state == 0) {
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        if (cudaStreamIsCapturing(cfg.stream, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone) {
+            cfg.numAttrs = 1;
+            return cudaLaunchKernelExC(&cfg, kern, args);
+        }
+        cfg.numAttrs = 2;
+        const cudaError_t e = cudaLaunchKernelExC(&cfg, kern, args);
+        if (e == cudaSuccess) {
+            state = 1;
+            return e;
+        }
+        (void)cudaGetLastError();
+        state = 2;
+    }
+    cfg.numAttrs = state == 1 ? 2 : 1;
+    return cudaLaunchKernelExC(&cfg, kern, args);
+}
+
 // Stages of the tensor-core batch decode for width d (at most 32; 0 when
 // fewer than one batch of records fits).
 int sparse_decode_mma_stages(int d) {
@@ -1954,12 +1992,7 @@ cudaError_t launch_sd_mma(SparseDecodeParams& P, int B, cudaStream_t st) {
     cfg.blockDim = dim3(kDecThreads, 1, 1);
     cfg.dynamicSmemBytes = (size_t)mma_layout(P.R, P.d).total;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeCooperative;
-    attr[0].val.cooperative = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelExC(&cfg, reinterpret_cast<const void*>(kern), args);
+    return launch_coop(reinterpret_cast<const void*>(kern), cfg, args);
 }
 
 cudaError_t launch_sparse_decode(SparseDecodeParams P, int B, cudaStream_t st) {
@@ -2042,14 +2075,6 @@ int tiered_down_ring(int d, int aux_floats, int rec_bytes) {
     return (RP >= 2 * d && RP >= rec_bytes && bytes >= (4 * kTdPairs + 4) * d) ? bytes : 0;
 }
 
-// Cooperative launch (one CTA per SM, all resident: the grid-wide slice
-// reduction waits on every CTA), with programmatic stream serialization when
-// the runtime accepts the two together (probed once, outside stream capture).
-inline int& tiered_pdl_state() {
-    static int state = 0;  // 0 unknown, 1 cooperative + PDL accepted, 2 cooperative only
-    return state;
-}
-
 template <int MAXC, int BITS, bool FULL>
 cudaError_t launch_tiered(TieredDownParams& P, size_t smem, cudaStream_t st) {
     auto kern = k_tiered_down<MAXC, BITS, FULL>;
@@ -2069,34 +2094,11 @@ cudaError_t launch_tiered(TieredDownParams& P, size_t smem, cudaStream_t st) {
     if (2 * per > P.aux_floats) return cudaErrorInvalidValue;
     void* args[] = {&P};
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.gridDim = dim3(grid, 1, 1);  // one CTA per SM; the cooperative launch guarantees co-residency
     cfg.blockDim = dim3(kTdThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
-    cudaLaunchAttribute attr[2];
-    attr[0].id = cudaLaunchAttributeCooperative;
-    attr[0].val.cooperative = 1;
-    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[1].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    int& state = tiered_pdl_state();
-    if (state == 0) {
-        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
-        if (cudaStreamIsCapturing(st, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone) {
-            cfg.numAttrs = 1;
-            return cudaLaunchKernelExC(&cfg, reinterpret_cast<const void*>(kern), args);
-        }
-        cfg.numAttrs = 2;
-        e = cudaLaunchKernelExC(&cfg, reinterpret_cast<const void*>(kern), args);
-        if (e == cudaSuccess) {
-            state = 1;
-            return e;
-        }
-        (void)cudaGetLastError();
-        state = 2;
-    }
-    cfg.numAttrs = state == 1 ? 2 : 1;
-    return cudaLaunchKernelExC(&cfg, reinterpret_cast<const void*>(kern), args);
+    return launch_coop(reinterpret_cast<const void*>(kern), cfg, args);
 }
 
 cudaError_t launch_tiered_down(TieredDownParams P, cudaStream_t st) {
