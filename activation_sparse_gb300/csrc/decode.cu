@@ -1457,10 +1457,9 @@ __device__ __forceinline__ void codes4_unit(uint32_t q, float2 (&w)[4]) {
 // at their own size (a bf16 column 2d bytes, a code record rec_bytes), and
 // reuses bytes once every warp of the stream has released them. The
 // streams' partials meet in shared memory at the end (summed in stream
-// order) and the CTAs' sums in a grid-wide slice reduction in a fixed order
-// (deterministic; the launch is cooperative, one CTA per SM). FULL:
-// d == 2048 * MAXC, every lane's chunks exist (no bounds checks in the
-// per-record code).
+// order) and the CTAs' sums are reduced through the cluster and a
+// fixed-order final pass (deterministic). FULL: d == 2048 * MAXC, every
+// lane's chunks exist (no bounds checks in the per-record code).
 template <int MAXC, int BITS, bool FULL>
 __global__ void __launch_bounds__(kTdThreads, 1) k_tiered_down(TieredDownParams P) {
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -1504,6 +1503,7 @@ __global__ void __launch_bounds__(kTdThreads, 1) k_tiered_down(TieredDownParams 
     __shared__ unsigned s_last;
     __shared__ __align__(8) uint64_t s_stage_bar;
     __shared__ int s_n[2];
+    grid_launch_dependents();
     grid_dependency_wait();  // a and its tier histogram are the previous grids' output
     const int tid = threadIdx.x;
     const int N = P.N;
@@ -1741,7 +1741,7 @@ __global__ void __launch_bounds__(kTdThreads, 1) k_tiered_down(TieredDownParams 
         }
     }
     __syncthreads();
-    grid_slice_reduce4(ycta, d, P.part, P.tickets, P.y, P.err, kSiteTiered | kSiteAccum, /*trigger=*/true);
+    cluster_ticket_reduce4(ycta, d, P.part, P.tickets, P.y);
     // every CTA read the histogram at its start; the last one to finish
     // re-zeroes it for the next token
     if (threadIdx.x == 0) {
@@ -2078,13 +2078,10 @@ int tiered_down_ring(int d, int aux_floats, int rec_bytes) {
 template <int MAXC, int BITS, bool FULL>
 cudaError_t launch_tiered(TieredDownParams& P, size_t smem, cudaStream_t st) {
     auto kern = k_tiered_down<MAXC, BITS, FULL>;
-    int dev = 0, sms = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    int grid = 0, cluster = 0;
+    cudaError_t e = cached_grid(kern, smem, &grid, &cluster, kTdThreads);
     if (e != cudaSuccess) return e;
-    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-    if ((e = allow_max_smem(kern)) != cudaSuccess) return e;
-    const int grid = sms;
-    if (P.part_floats < (long long)grid * P.d) return cudaErrorInvalidValue;
+    if (P.part_floats < (long long)(grid / cluster) * P.d) return cudaErrorInvalidValue;
     // per-CTA record counts (rank windows, or an own range of N / grid
     // columns) must fit the activation buffer (activations in the first half
     // of the buffer, columns in the second)
@@ -2093,12 +2090,7 @@ cudaError_t launch_tiered(TieredDownParams& P, size_t smem, cudaStream_t st) {
     if (own > per) per = own;
     if (2 * per > P.aux_floats) return cudaErrorInvalidValue;
     void* args[] = {&P};
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(grid, 1, 1);  // one CTA per SM; the cooperative launch guarantees co-residency
-    cfg.blockDim = dim3(kTdThreads, 1, 1);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = st;
-    return launch_coop(reinterpret_cast<const void*>(kern), cfg, args);
+    return launch_clustered(kern, grid, cluster, smem, st, args, /*pdl=*/true, kTdThreads);
 }
 
 cudaError_t launch_tiered_down(TieredDownParams P, cudaStream_t st) {

@@ -363,7 +363,13 @@ def run_selectinfer(si, torch, dev, stream, w, args, seed, *, steps, warmup, dec
     achieved = (token_bytes / w.L) / launch_s / 1e9
     gemm_flop = w.L * 4.0 * st.M * w.d * st.n_loaded
     gemm_tfs = gemm_flop / (gemm_ms / 1e3) / 1e12
-    kern = "k_sparse_decode_b1" if w.B == 1 else "k_sparse_decode<%d>" % w.B
+    # batches at d = 1024 / 2048 run on the tensor-core kernel (template: d / 128)
+    if w.B == 1:
+        kern = "k_sparse_decode_b1"
+    elif w.d in (1024, 2048):
+        kern = "k_sparse_decode_mma<%d>" % (w.d // 128)
+    else:
+        kern = "k_sparse_decode<%d>" % w.B
     traffic, traffic_src = recorded_traffic("%s@%s" % (kern, w.name))
     out = {
         "workload": w.name, "value": round(value, 2), "unit": "tokens/s",
@@ -971,7 +977,7 @@ def run_profile_case(args):
     """A few launches of one kernel on one full-size layer, for ncu captures.
     Cases: decode (k_sparse_decode_b1, residual form with a plan, Llama3.2-3B
     layer, as the headline runs it), decode1b (Llama3.2-1B layer), batch8
-    (k_sparse_decode<8>, Qwen2.5-3B layer), prefill (k_act_gemm, 1024-token
+    (k_sparse_decode_mma<16>, Qwen2.5-3B layer, 8 sequences), prefill (k_act_gemm, 1024-token
     prompt, Llama3.2-3B layer), stack (k_sparse_decode_stack, 4 Llama3.2-3B
     layers), dense (k_dense_act), tiered (k_tiered_down) and gateup
     (k_spax_gate_up, channel tiers 30 % / 30 %) on a Llama-3.1-8B layer. Prints one JSON line with the CUDA-event time per launch."""
