@@ -9,7 +9,7 @@ library and raises when it cannot be found or built.
 from ._binding import (  # noqa: F401
     SIGNATURES, SIError, Layer, SpaxLayer, load, lib_path,
     si_count, si_counts, si_packed_bytes, si_sparse_layers, si_device_error,
-    si_profile_scores, si_merge_scores, si_pack_loaded,
+    si_profile_scores, si_merge_scores, si_scores_save, si_scores_load, si_pack_loaded,
     si_select_dynamic, si_prefill_absact, si_select_from_absact,
     si_set_gemm_tile, si_gemm_tile_for, si_layer_set_salience, si_layer_norms,
     si_decode_plan, si_expand_clusters, si_sparse_ffn_decode, si_sparse_ffn_decode_residual, si_sparse_ffn_decode_noalloc,

@@ -28,6 +28,8 @@ SIGNATURES = {
     "si_device_error": (_i, [_u32p, _i]),
     "si_profile_scores": (_i, [_vp, _vp, _i, _i, _vp, _i, _vp, _vp]),
     "si_merge_scores": (_i, [C.POINTER(_vp), C.POINTER(_ll), _i, _i, _vp, _vp]),
+    "si_scores_save": (_i, [C.c_char_p, _vp, _i, _ll]),
+    "si_scores_load": (_i, [C.c_char_p, _vp, _i, _ip, C.POINTER(_ll)]),
     "si_pack_loaded": (_i, [_vp, _vp, _vp, _i, _i, _vp, _vp, _d, _d, C.POINTER(_vp), _vp]),
     "si_layer_info": (_i, [_vp, _ip, _ip, _ip, _ip, _ip]),
     "si_layer_buffers": (_i, [_vp, C.POINTER(_vp), C.POINTER(_vp), C.POINTER(_vp)]),
@@ -180,6 +182,28 @@ def si_merge_scores(score_list, token_counts, out, stream=None):
     _check(load().si_merge_scores(ptrs, toks, len(score_list), out.shape[0], _ptr(out, torch.float32, "out"),
                                   _stream(stream)))
     return out
+
+
+def si_scores_save(path, scores, token_count):
+    """Writes a score file: `scores` (fp32 [N], on any device) and the token
+    count they were summed over."""
+    import numpy as np
+    if hasattr(scores, "detach"):
+        scores = scores.detach().to("cpu")
+        scores = scores.numpy()
+    h = np.ascontiguousarray(scores, dtype=np.float32).reshape(-1)
+    _check(load().si_scores_save(os.fsencode(path), h.ctypes.data, int(h.size), int(token_count)))
+
+
+def si_scores_load(path):
+    """Reads a score file: (scores as a float32 numpy array [N], token count)."""
+    import numpy as np
+    n, t = C.c_int(), C.c_longlong()
+    L = load()
+    _check(L.si_scores_load(os.fsencode(path), None, 0, C.byref(n), C.byref(t)))
+    out = np.empty(n.value, dtype=np.float32)
+    _check(L.si_scores_load(os.fsencode(path), out.ctypes.data, int(out.size), C.byref(n), C.byref(t)))
+    return out, t.value
 
 
 class Layer:

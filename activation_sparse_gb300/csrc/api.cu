@@ -1,6 +1,8 @@
 // api.cu -- the C ABI declared in include/si.h: argument validation, handle
 // lifetime, scratch management and kernel launches. No arithmetic of the
 // method happens here; every step runs in the kernels.
+#include <vector>
+#include <cstdio>
 #include <cmath>
 #include <cstring>
 #include <mutex>
@@ -8,6 +10,19 @@
 
 #include "../../include/si.h"
 #include "internal.h"
+#include <nvtx3/nvToolsExt.h>
+
+namespace {
+// An NVTX range named after the entry point, open for the call (a pointer
+// check when no profiler is attached).
+struct NvtxRange {
+    explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+    NvtxRange(const NvtxRange&) = delete;
+    NvtxRange& operator=(const NvtxRange&) = delete;
+};
+}  // namespace
+#define SI_TRACE(name) NvtxRange si_trace_range_(name)
 
 namespace {
 
@@ -255,6 +270,7 @@ int si_counts(int N, double gamma, double delta, double phi, int* n_loaded, int*
 long long si_packed_bytes(int d, int n_loaded) { return 3LL * d * n_loaded * 2; }
 
 int si_device_error(uint32_t* code, int clear) {
+    SI_TRACE("si_device_error");
     if (!code) return fail(SI_ERR_INVALID_ARG, "code is NULL");
     int dev = 0;
     SI_CK(cudaGetDevice(&dev));
@@ -283,6 +299,7 @@ int si_device_error(uint32_t* code, int clear) {
 
 int si_profile_scores(const uint16_t* Wg, const uint16_t* Wu, int d, int N, const uint16_t* X, int T, float* scores,
                       void* stream) {
+    SI_TRACE("si_profile_scores");
     if (!Wg || !Wu || !X || !scores) return fail(SI_ERR_INVALID_ARG, "NULL pointer");
     if (d < 64 || d % 64 || N < 1 || T < 1) return fail(SI_ERR_INVALID_ARG, "need d % 64 == 0, N >= 1, T >= 1");
     unsigned* err = nullptr;
@@ -306,6 +323,7 @@ int si_profile_scores(const uint16_t* Wg, const uint16_t* Wu, int d, int N, cons
 
 int si_merge_scores(const float* const* scores, const long long* token_counts, int nfiles, int N, float* out,
                     void* stream) {
+    SI_TRACE("si_merge_scores");
     if (!scores || !token_counts || !out) return fail(SI_ERR_INVALID_ARG, "NULL pointer");
     if (nfiles < 1 || nfiles > 16 || N < 1) return fail(SI_ERR_INVALID_ARG, "need 1 <= nfiles <= 16, N >= 1");
     float tok[16];
@@ -318,10 +336,90 @@ int si_merge_scores(const float* const* scores, const long long* token_counts, i
     return SI_OK;
 }
 
+// ----------------------------------------------------------- score files
+
+namespace {
+
+constexpr char kScoreMagic[8] = {'S', 'I', 'S', 'C', 'O', 'R', 'E', '1'};
+
+// 32-bit FNV-1a (offset basis 2166136261, prime 16777619) over a byte range,
+// continuing from h
+uint32_t fnv1a(const void* data, size_t n, uint32_t h) {
+    const unsigned char* p = static_cast<const unsigned char*>(data);
+    for (size_t i = 0; i < n; ++i) {
+        h ^= p[i];
+        h *= 16777619u;
+    }
+    return h;
+}
+
+struct ScoreHeader {
+    char magic[8];
+    int32_t n;
+    int32_t zero;
+    int64_t tokens;
+};
+static_assert(sizeof(ScoreHeader) == 24, "score file header is 24 bytes");
+
+}  // namespace
+
+int si_scores_save(const char* path, const float* scores, int N, long long token_count) {
+    SI_TRACE("si_scores_save");
+    if (!path || !scores) return fail(SI_ERR_INVALID_ARG, "NULL pointer");
+    if (N < 1 || token_count < 1) return fail(SI_ERR_INVALID_ARG, "need N >= 1 and token_count >= 1");
+    ScoreHeader h = {};
+    std::memcpy(h.magic, kScoreMagic, 8);
+    h.n = N;
+    h.zero = 0;
+    h.tokens = token_count;
+    uint32_t sum = fnv1a(&h, sizeof(h), 2166136261u);
+    sum = fnv1a(scores, (size_t)N * sizeof(float), sum);
+    const std::string tmp = std::string(path) + ".tmp";
+    FILE* f = std::fopen(tmp.c_str(), "wb");
+    if (!f) return fail(SI_ERR_INVALID_ARG, "cannot open the score file for writing");
+    const bool ok = std::fwrite(&h, sizeof(h), 1, f) == 1 &&
+                    std::fwrite(scores, sizeof(float), (size_t)N, f) == (size_t)N &&
+                    std::fwrite(&sum, sizeof(sum), 1, f) == 1;
+    const bool closed = std::fclose(f) == 0;
+    if (!ok || !closed || std::rename(tmp.c_str(), path) != 0) {
+        std::remove(tmp.c_str());
+        return fail(SI_ERR_INVALID_ARG, "cannot write the score file");
+    }
+    return SI_OK;
+}
+
+int si_scores_load(const char* path, float* scores, int capacity, int* N_out, long long* token_count_out) {
+    SI_TRACE("si_scores_load");
+    if (!path || !N_out || !token_count_out) return fail(SI_ERR_INVALID_ARG, "NULL pointer");
+    FILE* f = std::fopen(path, "rb");
+    if (!f) return fail(SI_ERR_INVALID_ARG, "cannot open the score file");
+    ScoreHeader h = {};
+    const bool head = std::fread(&h, sizeof(h), 1, f) == 1;
+    if (!head || std::memcmp(h.magic, kScoreMagic, 8) != 0 || h.n < 1 || h.zero != 0 || h.tokens < 1) {
+        std::fclose(f);
+        return fail(SI_ERR_INVALID_ARG, "not a score file (magic, N or token count)");
+    }
+    std::vector<float> v((size_t)h.n);
+    uint32_t stored = 0;
+    unsigned char extra;
+    const bool body = std::fread(v.data(), sizeof(float), v.size(), f) == v.size() &&
+                      std::fread(&stored, sizeof(stored), 1, f) == 1 && std::fread(&extra, 1, 1, f) == 0;
+    std::fclose(f);
+    if (!body) return fail(SI_ERR_INVALID_ARG, "score file is short or has trailing bytes");
+    uint32_t sum = fnv1a(&h, sizeof(h), 2166136261u);
+    sum = fnv1a(v.data(), v.size() * sizeof(float), sum);
+    if (sum != stored) return fail(SI_ERR_INVALID_ARG, "score file checksum does not match");
+    *N_out = h.n;
+    *token_count_out = h.tokens;
+    if (scores && capacity >= h.n) std::memcpy(scores, v.data(), v.size() * sizeof(float));
+    return SI_OK;
+}
+
 // ------------------------------------------------------------------ a2
 
 int si_pack_loaded(const uint16_t* Wg, const uint16_t* Wu, const uint16_t* Wd, int d, int N, const float* task_scores,
                    const float* model_scores, double gamma, double delta, si_layer** out, void* stream) {
+    SI_TRACE("si_pack_loaded");
     if (!out) return fail(SI_ERR_INVALID_ARG, "out is NULL");
     *out = nullptr;
     if (!Wg || !Wu || !Wd || !task_scores || !model_scores) return fail(SI_ERR_INVALID_ARG, "NULL pointer");
@@ -366,6 +464,7 @@ int si_pack_loaded(const uint16_t* Wg, const uint16_t* Wu, const uint16_t* Wd, i
 }
 
 int si_layer_info(const si_layer* L, int* d, int* N, int* n_loaded, int* n_static, int* n_pad) {
+    SI_TRACE("si_layer_info");
     if (!L) return fail(SI_ERR_INVALID_ARG, "layer is NULL");
     if (d) *d = L->d;
     if (N) *N = L->N;
@@ -377,6 +476,7 @@ int si_layer_info(const si_layer* L, int* d, int* N, int* n_loaded, int* n_stati
 
 int si_layer_buffers(const si_layer* L, const int32_t** loaded_idx, const uint8_t** is_static,
                      const uint16_t** packed) {
+    SI_TRACE("si_layer_buffers");
     if (!L) return fail(SI_ERR_INVALID_ARG, "layer is NULL");
     if (loaded_idx) *loaded_idx = L->loaded;
     if (is_static) *is_static = L->is_static;
@@ -385,12 +485,14 @@ int si_layer_buffers(const si_layer* L, const int32_t** loaded_idx, const uint8_
 }
 
 int si_layer_norms(const si_layer* L, const float** norms) {
+    SI_TRACE("si_layer_norms");
     if (!L || !norms) return fail(SI_ERR_INVALID_ARG, "NULL pointer");
     *norms = L->wnorm;
     return SI_OK;
 }
 
 int si_layer_set_salience(si_layer* L, int weight_aware) {
+    SI_TRACE("si_layer_set_salience");
     if (!L) return fail(SI_ERR_INVALID_ARG, "layer is NULL");
     if (weight_aware != 0 && weight_aware != 1) return fail(SI_ERR_INVALID_ARG, "weight_aware must be 0 or 1");
     L->salience = weight_aware;
@@ -398,6 +500,7 @@ int si_layer_set_salience(si_layer* L, int weight_aware) {
 }
 
 int si_layer_destroy(si_layer* L) {
+    SI_TRACE("si_layer_destroy");
     if (!L) return SI_OK;
     cudaDeviceSynchronize();
     destroy_layer(L);
@@ -408,6 +511,7 @@ int si_layer_destroy(si_layer* L) {
 
 int si_select_from_absact(si_layer* L, const float* absA, int ld, int T, int B, int alpha, double phi, int32_t* S,
                           uint32_t* topmask, uint32_t* counts, void* stream) {
+    SI_TRACE("si_select_from_absact");
     if (!L || !absA || !S) return fail(SI_ERR_INVALID_ARG, "NULL pointer");
     if (T < 1 || B < 1 || ld < L->n_loaded) return fail(SI_ERR_INVALID_ARG, "need T, B >= 1 and ld >= n_loaded");
     if (alpha < 1 || alpha > L->n_loaded) return fail(SI_ERR_INVALID_ARG, "need 1 <= alpha <= n_loaded");
@@ -442,6 +546,7 @@ int absact_core(si_layer* L, const uint16_t* X, int M, float* A, cudaStream_t st
 }  // namespace
 
 int si_prefill_absact(si_layer* L, const uint16_t* X, int T, int B, float* absact_out, void* stream) {
+    SI_TRACE("si_prefill_absact");
     if (!L || !X || !absact_out) return fail(SI_ERR_INVALID_ARG, "NULL pointer");
     if (reinterpret_cast<uintptr_t>(absact_out) & 15u) return fail(SI_ERR_INVALID_ARG, "absact_out must be 16-byte aligned");
     if (T < 1 || B < 1) return fail(SI_ERR_INVALID_ARG, "need T, B >= 1");
@@ -450,11 +555,13 @@ int si_prefill_absact(si_layer* L, const uint16_t* X, int T, int B, float* absac
 }
 
 int si_set_gemm_tile(int bnn) {
+    SI_TRACE("si_set_gemm_tile");
     if (si::set_gemm_tile(bnn) != cudaSuccess) return fail(SI_ERR_INVALID_ARG, "bnn must be 0, 64, 80, 96, 112 or 128");
     return SI_OK;
 }
 
 int si_gemm_tile_for(int M, int N, int* bnn) {
+    SI_TRACE("si_gemm_tile_for");
     if (!bnn) return fail(SI_ERR_INVALID_ARG, "NULL pointer");
     if (M < 1 || N < 1) return fail(SI_ERR_INVALID_ARG, "need M, N >= 1");
     const int b = si::gemm_tile_for(M, N);
@@ -465,6 +572,7 @@ int si_gemm_tile_for(int M, int N, int* bnn) {
 
 int si_select_dynamic(si_layer* L, const uint16_t* X, int T, int B, int alpha, double phi, int32_t* S,
                       float* absact_out, void* stream) {
+    SI_TRACE("si_select_dynamic");
     if (!L || !X || !S) return fail(SI_ERR_INVALID_ARG, "NULL pointer");
     if (reinterpret_cast<uintptr_t>(absact_out) & 15u) return fail(SI_ERR_INVALID_ARG, "absact_out must be 16-byte aligned");
     if (T < 1 || B < 1) return fail(SI_ERR_INVALID_ARG, "need T, B >= 1");
@@ -501,6 +609,7 @@ int si_select_dynamic(si_layer* L, const uint16_t* X, int T, int B, int alpha, d
 
 int si_expand_clusters(si_layer* L, const int32_t* S, int n_sel, int cluster, int32_t* S_out, int* n_out,
                        void* stream) {
+    SI_TRACE("si_expand_clusters");
     if (!L || !S_out || !n_out || (n_sel > 0 && !S)) return fail(SI_ERR_INVALID_ARG, "NULL pointer");
     if (cluster < 1) return fail(SI_ERR_INVALID_ARG, "cluster size must be >= 1");
     if (n_sel < 0 || n_sel > L->n_loaded) return fail(SI_ERR_INVALID_ARG, "need 0 <= n_sel <= n_loaded");
@@ -519,6 +628,7 @@ int si_expand_clusters(si_layer* L, const int32_t* S, int n_sel, int cluster, in
 }
 
 int si_decode_plan(si_layer* L, const int32_t* S, int n_sel, int B, void* stream) {
+    SI_TRACE("si_decode_plan");
     if (!L || (!S && n_sel > 0)) return fail(SI_ERR_INVALID_ARG, "NULL pointer");
     if (B < 1 || B > 8) return fail(SI_ERR_INVALID_ARG, "need 1 <= B <= 8");
     if (n_sel < 0 || n_sel > L->n_loaded) return fail(SI_ERR_INVALID_ARG, "need 0 <= n_sel <= n_loaded");
@@ -558,11 +668,13 @@ int sparse_decode_impl(si_layer* L, const int32_t* S, int n_sel, int B, const ui
 
 int si_sparse_ffn_decode(si_layer* L, const int32_t* S, int n_sel, int B, const uint16_t* x, float* y,
                          void* stream) {
+    SI_TRACE("si_sparse_ffn_decode");
     return sparse_decode_impl(L, S, n_sel, B, x, y, stream, false);
 }
 
 int si_sparse_ffn_decode_residual(si_layer* L, const int32_t* S, int n_sel, int B, const uint16_t* x, float* y,
                                   void* stream) {
+    SI_TRACE("si_sparse_ffn_decode_residual");
     if (B != 1) return fail(SI_ERR_UNSUPPORTED, "the residual form is implemented for B == 1");
     return sparse_decode_impl(L, S, n_sel, B, x, y, stream, true);
 }
@@ -623,6 +735,7 @@ extern "C" {
 // ------------------------------------------------------------------ SpAx
 
 int spax_encode(const uint16_t* Wd, int d, int N, int bits, int group, spax_layer** out, void* stream) {
+    SI_TRACE("spax_encode");
     if (!out) return fail(SI_ERR_INVALID_ARG, "out is NULL");
     *out = nullptr;
     if (!Wd) return fail(SI_ERR_INVALID_ARG, "NULL pointer");
@@ -679,6 +792,7 @@ int spax_encode(const uint16_t* Wd, int d, int N, int bits, int group, spax_laye
 }
 
 int spax_layer_info(const spax_layer* L, int* d, int* N, int* bits, int* group, int* ngp) {
+    SI_TRACE("spax_layer_info");
     if (!L) return fail(SI_ERR_INVALID_ARG, "layer is NULL");
     if (d) *d = L->d;
     if (N) *N = L->N;
@@ -689,6 +803,7 @@ int spax_layer_info(const spax_layer* L, int* d, int* N, int* bits, int* group, 
 }
 
 int spax_layer_buffers(const spax_layer* L, const uint16_t** WdT, const uint8_t** codes, const float** params) {
+    SI_TRACE("spax_layer_buffers");
     if (!L) return fail(SI_ERR_INVALID_ARG, "layer is NULL");
     if (WdT) *WdT = L->WdT;
     if (codes) *codes = L->codes;
@@ -697,6 +812,7 @@ int spax_layer_buffers(const spax_layer* L, const uint16_t** WdT, const uint8_t*
 }
 
 int spax_layer_destroy(spax_layer* L) {
+    SI_TRACE("spax_layer_destroy");
     if (!L) return SI_OK;
     cudaDeviceSynchronize();
     destroy_spax(L);
@@ -784,11 +900,13 @@ int tiered_core(spax_layer* L, const float* a, long long k_top, long long k_mid,
 extern "C" {
 
 int spax_dense_act(const uint16_t* Wg, const uint16_t* Wu, int d, int N, const uint16_t* x, float* a, void* stream) {
+    SI_TRACE("spax_dense_act");
     return dense_act_core(Wg, Wu, d, N, x, a, nullptr, nullptr, (cudaStream_t)stream);
 }
 
 int spax_tiered_down(spax_layer* L, const float* a, double top_frac, double mid_frac, float* y, int32_t* top_idx,
                      int32_t* mid_idx, void* stream) {
+    SI_TRACE("spax_tiered_down");
     if (!L || !a || !y) return fail(SI_ERR_INVALID_ARG, "NULL pointer");
     long long k_top = 0, k_mid = 0;
     int rc = tier_counts(L, top_frac, mid_frac, &k_top, &k_mid);
@@ -800,6 +918,7 @@ int spax_tiered_down(spax_layer* L, const float* a, double top_frac, double mid_
 
 int spax_select_decode(spax_layer* L, const uint16_t* Wg, const uint16_t* Wu, const int32_t* rows, int n_rows,
                        const uint16_t* x, double top_frac, double mid_frac, float* y, float* a_out, void* stream) {
+    SI_TRACE("spax_select_decode");
     if (!L || !Wg || !Wu || !x || !y || (n_rows > 0 && !rows)) return fail(SI_ERR_INVALID_ARG, "NULL pointer");
     if (n_rows < 0 || n_rows > L->N) return fail(SI_ERR_INVALID_ARG, "need 0 <= n_rows <= N");
     if (!(top_frac >= 0.0 && mid_frac >= 0.0 && top_frac + mid_frac <= 1.0))
@@ -826,6 +945,7 @@ int spax_select_decode(spax_layer* L, const uint16_t* Wg, const uint16_t* Wu, co
 
 int spax_ffn_decode(spax_layer* L, const uint16_t* Wg, const uint16_t* Wu, const uint16_t* x, double top_frac,
                     double mid_frac, float* y, float* a_out, void* stream) {
+    SI_TRACE("spax_ffn_decode");
     if (!L || !y) return fail(SI_ERR_INVALID_ARG, "NULL pointer");
     long long k_top = 0, k_mid = 0;
     int rc = tier_counts(L, top_frac, mid_frac, &k_top, &k_mid);
@@ -862,6 +982,7 @@ extern "C" {
 // ------------------------------------------------------- a7: decode stack
 
 int si_stack_create(si_layer* const* layers, int L, si_stack** out) {
+    SI_TRACE("si_stack_create");
     if (!out) return fail(SI_ERR_INVALID_ARG, "out is NULL");
     *out = nullptr;
     if (!layers) return fail(SI_ERR_INVALID_ARG, "NULL pointer");
@@ -907,6 +1028,7 @@ int si_stack_create(si_layer* const* layers, int L, si_stack** out) {
 }
 
 int si_stack_plan(si_stack* K, const int32_t* const* S, const int* n_sel, void* stream) {
+    SI_TRACE("si_stack_plan");
     if (!K || !S || !n_sel) return fail(SI_ERR_INVALID_ARG, "NULL pointer");
     bool same = K->planned;
     for (int l = 0; l < K->L; ++l) {
@@ -942,6 +1064,7 @@ int si_stack_plan(si_stack* K, const int32_t* const* S, const int* n_sel, void* 
 }
 
 int si_sparse_ffn_decode_stack(si_stack* K, float* h, uint16_t* x_out, void* stream) {
+    SI_TRACE("si_sparse_ffn_decode_stack");
     if (!K || !h) return fail(SI_ERR_INVALID_ARG, "NULL pointer");
     if (!K->planned) return fail(SI_ERR_INVALID_ARG, "call si_stack_plan before decoding");
     if ((reinterpret_cast<uintptr_t>(h) & 15u) || (reinterpret_cast<uintptr_t>(x_out) & 15u))
@@ -964,6 +1087,7 @@ int si_sparse_ffn_decode_stack(si_stack* K, float* h, uint16_t* x_out, void* str
 }
 
 int si_stack_destroy(si_stack* K) {
+    SI_TRACE("si_stack_destroy");
     if (!K) return SI_OK;
     cudaDeviceSynchronize();
     destroy_stack(K);
@@ -1023,12 +1147,14 @@ extern "C" {
 
 int spax_gate_up(const spax_layer* gate, const spax_layer* up, const uint16_t* x, double top_frac, double mid_frac,
                  float* a, int32_t* top_idx, int32_t* mid_idx, void* stream) {
+    SI_TRACE("spax_gate_up");
     return gate_up_core(gate, up, x, top_frac, mid_frac, a, top_idx, mid_idx, nullptr, nullptr, (cudaStream_t)stream);
 }
 
 int spax_all_decode(spax_layer* down, const spax_layer* gate, const spax_layer* up, const uint16_t* x,
                     double in_top_frac, double in_mid_frac, double top_frac, double mid_frac, float* y,
                     float* a_out, void* stream) {
+    SI_TRACE("spax_all_decode");
     if (!down || !gate || !up || !y) return fail(SI_ERR_INVALID_ARG, "NULL pointer");
     if (down->N != gate->d || down->d != gate->N)
         return fail(SI_ERR_INVALID_ARG, "the down encoding's columns must be the gate/up encodings' rows");

@@ -25,6 +25,9 @@
  *   - Pointers are DEVICE pointers unless the argument is marked (host).
  *     The caller owns inputs and outputs; the library owns the si_layer /
  *     spax_layer handles and everything inside them.
+ *   - Every entry point that launches work or waits on the device opens an
+ *     NVTX range named after itself for the length of the call (visible to
+ *     Nsight tools; a pointer check when none is attached).
  *   - bf16 tensors are passed as uint16_t bit patterns. HF layouts:
  *     Wg, Wu are [N x d] row-major (neuron n = row n), Wd is [d x N]
  *     row-major (neuron n = column n). Activations X are [rows x d].
@@ -130,6 +133,26 @@ int si_profile_scores(const uint16_t *Wg, const uint16_t *Wu, int d, int N,
  * 1 <= nfiles <= 16. */
 int si_merge_scores(const float *const *scores, const long long *token_counts, int nfiles,
                     int N, float *out, void *stream);
+
+/* Score files, [SI] section 3: the profiler's per-neuron scores of one
+ * calibration set are stored in a score file with the number of tokens they
+ * were summed over, so that files from several sets can be merged later
+ * (si_merge_scores) and the merged scores ranked (si_pack_loaded).
+ * File layout (little-endian): the 8 bytes "SISCORE1", int32 N, int32 0,
+ * int64 token_count, N float32 scores, then a uint32 FNV-1a checksum of
+ * every preceding byte.
+ *   si_scores_save: scores (host) fp32 [N], N >= 1, token_count >= 1;
+ *     writes `path` (replacing it) through a temporary file and a rename.
+ *   si_scores_load: reads `path`; *N_out and *token_count_out (host)
+ *     receive the stored N and count; scores (host) fp32 [capacity]
+ *     receives the scores when capacity >= N (when it is smaller, or scores
+ *     is NULL, only *N_out and *token_count_out are set and the call returns
+ *     SI_OK, so a caller can size its buffer first).
+ * SI_ERR_INVALID_ARG for NULL path / counts, N < 1, token_count < 1, a
+ * missing or short file, another magic, or a checksum that does not match;
+ * SI_ERR_CUDA never (host only: no CUDA call). */
+int si_scores_save(const char *path, const float *scores, int N, long long token_count);
+int si_scores_load(const char *path, float *scores, int capacity, int *N_out, long long *token_count_out);
 
 /* ------------------------------------------------- a2: selective loading */
 
