@@ -655,6 +655,11 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_sparse_decode_mma(SparseDeco
                        /*trigger=*/true);
 }
 
+// The overwrite form (y = FFN(x)) sums the CTAs' partials either through
+// the cluster and a fixed-order final pass (CR: clustered launches with a
+// partial buffer) or with the 64-bit fixed-point accumulator (no partial
+// buffer: the allocation-free entry point); both are deterministic. The
+// residual form (y += FFN(x)) adds each CTA's sum with vector atomics.
 // Batch-1 decode with decoupled warps: neuron i belongs to warp i % 8 and ring
 // stage i % R. Each warp computes a = silu(g.x) * (u.x) for its neuron and
 // accumulates a * down into its own register partial of y; there is no
@@ -668,7 +673,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_sparse_decode_mma(SparseDeco
 // and a consumer waits for its number to appear before the parity wait.
 constexpr int kB1MaxStages = 32;  // stages of the batch-1 ring (their record numbers sit in the aux area)
 
-template <int MAXC>
+template <int MAXC, bool CR>
 __global__ void __launch_bounds__(kDecThreads, 1) k_sparse_decode_b1(SparseDecodeParams P) {
     extern __shared__ __align__(1024) uint8_t smem[];
     const int d = P.d;
@@ -825,7 +830,10 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_sparse_decode_b1(SparseDecod
     }
     if (!P.accumulate) {
         __syncthreads();
-        fixed_point_reduce(reinterpret_cast<float*>(ring), d, P.acc, P.acc_ticket, P.y, P.err, P.err_report);
+        if constexpr (CR)
+            cluster_ticket_reduce4(reinterpret_cast<float*>(ring), d, P.part, P.tickets, P.y);
+        else
+            fixed_point_reduce(reinterpret_cast<float*>(ring), d, P.acc, P.acc_ticket, P.y, P.err, P.err_report);
     }
 }
 
@@ -1888,7 +1896,7 @@ constexpr int kSpareSms = 4;
 
 template <int MAXC>
 cudaError_t launch_sd1(SparseDecodeParams& P, cudaStream_t st) {
-    auto kern = k_sparse_decode_b1<MAXC>;
+    auto kern = k_sparse_decode_b1<MAXC, false>;
     int dev = 0, sms = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -1897,6 +1905,21 @@ cudaError_t launch_sd1(SparseDecodeParams& P, cudaStream_t st) {
     const size_t smem = (size_t)ring_layout(P.R, 6 * P.d, 4 * kB1MaxStages, 2 * P.d).total;
     void* args[] = {&P};
     return launch_clustered(kern, sms > 2 * kSpareSms ? sms - kSpareSms : sms, 1, smem, st, args, /*pdl=*/true);
+}
+
+// The overwrite form with the cluster reduction: clusters from the occupancy
+// of this kernel (as the other clustered decode kernels).
+template <int MAXC>
+cudaError_t launch_sd1_cr(SparseDecodeParams& P, cudaStream_t st) {
+    auto kern = k_sparse_decode_b1<MAXC, true>;
+    const size_t smem = (size_t)ring_layout(P.R, 6 * P.d, 4 * kB1MaxStages, 2 * P.d).total;
+    int grid = 0, cluster = 0;
+    cudaError_t e = cached_grid(kern, smem, &grid, &cluster);
+    if (e != cudaSuccess) return e;
+    if (P.part_floats < (long long)(grid / cluster) * P.d) return cudaErrorInvalidValue;
+    if (P.d % (4 * cluster)) return cudaErrorInvalidValue;  // float4 slices per cluster rank
+    void* args[] = {&P};
+    return launch_clustered(kern, grid, cluster, smem, st, args, /*pdl=*/true);
 }
 
 }  // namespace
@@ -1928,9 +1951,9 @@ int decode_max_partial_floats(int d, int B) {
     return (B > 1 ? sms : sms / 2 + 1) * B * d;
 }
 
-int sparse_decode_b1_stages(int d) {
+int sparse_decode_b1_stages(int d, int extra_static) {
     const int stage = round_up(6 * d, 128);
-    int R = (kSmemBudget - ring_layout(kB1MaxStages, 0, 4 * kB1MaxStages, 2 * d).total) / stage;
+    int R = (kSmemBudget - extra_static - ring_layout(kB1MaxStages, 0, 4 * kB1MaxStages, 2 * d).total) / stage;
     if (R > kB1MaxStages) R = kB1MaxStages;
     // warp w's partial (blocks of 32 chunks: round_up(d, 256) floats) reuses
     // its stage w, then the CTA partial stage 0
@@ -2005,6 +2028,16 @@ cudaError_t launch_sparse_decode(SparseDecodeParams P, int B, cudaStream_t st) {
         if (P2.R >= kMmaBatch) return P.d == 1024 ? launch_sd_mma<8>(P2, B, st) : launch_sd_mma<16>(P2, B, st);
     }
     if (B == 1 && P.pmask == nullptr && (P.n_dev == nullptr || P.stable_plan)) {
+        // the overwrite form with a partial buffer: the cluster reduction
+        // (its static shared memory, a float4 per thread, comes out of the ring)
+        if (!P.accumulate && P.part && P.tickets) {
+            const int Rc = sparse_decode_b1_stages(P.d, (int)sizeof(float4) * kDecThreads + 64);
+            if (Rc >= kConsWarps) {
+                SparseDecodeParams P1 = P;
+                P1.R = Rc;
+                return wide ? launch_sd1_cr<2>(P1, st) : launch_sd1_cr<1>(P1, st);
+            }
+        }
         const int R1 = sparse_decode_b1_stages(P.d);
         if (R1 >= kConsWarps) {
             SparseDecodeParams P1 = P;

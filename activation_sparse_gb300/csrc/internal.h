@@ -169,7 +169,7 @@ cudaError_t launch_sparse_decode_stack(const StackParams& P, cudaStream_t st);
 int noalloc_error_word(unsigned** out);
 
 // decode.cu
-int sparse_decode_b1_stages(int d);
+int sparse_decode_b1_stages(int d, int extra_static = 0);  // extra: static shared memory beyond the usual 2 KB
 int sparse_decode_stages(int d, int B);
 int decode_max_partial_floats(int d, int B);
 cudaError_t launch_sparse_decode(SparseDecodeParams P, int B, cudaStream_t st);
