@@ -90,10 +90,20 @@ __device__ void cluster_ticket_reduce4(const float* ypart, int BD, float* __rest
     __syncthreads();
     if (s_last) {
         __threadfence();
-        // Sum of clusters k = g, g + G, g + 2G, ... of column q, eight loads in flight.
+        // Sum of clusters k = g, g + G, g + 2G, ... of column q, sixteen (then
+        // eight) loads in flight.
         auto sum_clusters = [&](int q, int g, int G) {
             float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
             int k = g;
+            for (; k + 15 * G < ncl; k += 16 * G) {
+                float4 t[16];
+#pragma unroll
+                for (int u = 0; u < 16; ++u) t[u] = __ldcg(part4 + (size_t)(k + u * G) * BD4 + q0 + q);
+#pragma unroll
+                for (int u = 0; u < 16; ++u) {
+                    v.x += t[u].x; v.y += t[u].y; v.z += t[u].z; v.w += t[u].w;
+                }
+            }
             for (; k + 7 * G < ncl; k += 8 * G) {
                 float4 t[8];
 #pragma unroll
