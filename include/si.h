@@ -107,7 +107,7 @@ int si_sparse_layers(int L, int first, int last, uint8_t *sparse, int *n_sparse)
  * words) of SI_DEVERR_* values. Synchronises the device; allocates nothing. */
 #define SI_DEVERR_WAIT_TIMEOUT 1u   /* a bounded mbarrier wait ran out */
 #define SI_DEVERR_COUNT 2u          /* an index or count check failed (bad S / tier list, count mismatch) */
-#define SI_DEVERR_RANGE 4u          /* a decode partial exceeded the fixed-point accumulator's range (|y| >= 2^23) */
+#define SI_DEVERR_RANGE 4u          /* a decode partial exceeded a fixed-point accumulator's range (|y| >= 2^23) */
 /* With SI_DEVERR_WAIT_TIMEOUT, bits 8-15 name the kernel whose wait ran out
  * (1 sparse decode, 2 dense activation pass, 3 tiered down-projection,
  * 4 activation GEMM, 5 decode stack) and bits 16-19 the barrier (1 stage
@@ -286,9 +286,14 @@ int si_decode_plan(si_layer *layer, const int32_t *S, int n_sel, int B, void *st
  *   y[b, :] = sum over p in S[b] of a_{loaded[p]}(x_b) * Wd[:, loaded[p]].
  * Reads only the selected packed records (gate row, up row, down column) with
  * bulk copies and reduces over neurons inside the kernel, split over neurons
- * across the SMs. For B == 1 the CTA partials are summed exactly in 64-bit
- * fixed point (2^-32 resolution); for B > 1 through cluster shared memory and
- * then in a fixed cross-cluster order. Either way results are deterministic.
+ * across the SMs. For B == 1 the CTA partials are summed through cluster
+ * shared memory and then in a fixed cross-cluster order. For 2 <= B <= 8 at
+ * d = 1024 or 2048 the gate/up and down products run on the tensor cores
+ * (bf16 operands, fp32 accumulation; a enters as two bf16 terms, so it is
+ * applied to within 2^-18 |a|) and the CTA partials meet in a grid-wide
+ * reduction in a fixed CTA order (a cooperative launch, one CTA per SM);
+ * other B > 1 go through cluster shared memory and a fixed cross-cluster
+ * order. Either way results are deterministic.
  *   S int32 [B x n_sel] ascending positions (as written by the selection
  *   calls); x bf16 [B x d]; y fp32 [B x d] (overwritten).
  * For B > 1, si_decode_plan(layer, S, n_sel, B) must have been called with
