@@ -177,7 +177,7 @@ int dense_act_stages(int d);
 cudaError_t launch_dense_act(DenseActParams P, cudaStream_t st);
 cudaError_t launch_abs_hist(const float* a, int N, unsigned* hist, int32_t* slab, cudaStream_t st);
 int tiered_down_ring(int d, int aux_floats, int rec_bytes);
-int tiered_max_partial_floats(int d);  // partial floats the tiered kernel needs (one per CTA)
+int tiered_max_partial_floats(int d);  // partial floats for the tiered kernel (at most one per CTA, one CTA per SM)
 cudaError_t launch_tiered_down(TieredDownParams P, cudaStream_t st);
 int streaming_grid_upper_bound();
 
